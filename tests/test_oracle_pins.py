@@ -1,0 +1,335 @@
+"""Pins for the oracle: values the pages print, closed forms, invariants and
+library special cases. None of these re-types the oracle's own formulas; each
+is a fact fixed by the pages or by the mathematics, chosen so that a dropped
+term, a wrong sign or index, or a transposed operand in the oracle fails one.
+
+Sources: "Rethinking and Improving Relative Position Encoding for Vision
+Transformer" (eqs. 13-18, 25-28; Pitfalls), "Swin 的二维 RPE" (sections 2.2,
+3.1-3.3), "Swin Transformer, section 3.2 and Table 4", and "Implementation:
+Relative Position in Self-Attention" (Testing the Implementation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_golden
+
+R19 = (1.9, 3.8, 15.2)
+
+
+# ---------------------------------------------------------------- eq. 18 g(x)
+
+def test_piecewise_r19_matches_pitfalls_table():
+    rows = read_golden("piecewise_r1p9.txt")
+    alpha, beta, gamma = rows[0]
+    for off, idx in rows[1:]:
+        assert oracle.piecewise_index(off, alpha, beta, gamma) == int(idx), off
+        assert oracle.piecewise_index(-off, alpha, beta, gamma) == -int(idx), off
+
+
+def test_piecewise_r20_nine_buckets_and_shared_pair():
+    rows = read_golden("piecewise_r2p0.txt")
+    alpha, beta, gamma, span = rows[0]
+    a, b = rows[1]
+    assert 2 * int(beta) + 1 == int(span)
+    assert oracle.piecewise_index(a, alpha, beta, gamma) == oracle.piecewise_index(
+        b, alpha, beta, gamma)
+    # the index range is exactly [-int(beta), int(beta)] over a long axis
+    vals = {oracle.piecewise_index(x, alpha, beta, gamma) for x in range(-300, 301)}
+    assert vals == set(range(-int(beta), int(beta) + 1))
+
+
+@pytest.mark.parametrize("ratio", [1.0, 1.9, 2.0, 3.5, 7.0])
+def test_piecewise_identity_below_alpha_and_odd(ratio):
+    alpha, beta, gamma = ratio, 2 * ratio, 8 * ratio
+    for x in range(0, int(np.floor(alpha)) + 1):  # exact for |x| <= alpha (eq. 18)
+        assert oracle.piecewise_index(x, alpha, beta, gamma) == x
+    prev = 0
+    for x in range(0, 200):
+        g = oracle.piecewise_index(x, alpha, beta, gamma)
+        assert oracle.piecewise_index(-x, alpha, beta, gamma) == -g   # odd symmetry
+        assert 0 <= g <= int(beta)                                      # capped at beta
+        assert g >= prev                                                # monotone
+        prev = g
+    # at x = gamma the log share is exactly 1, so the spread is beta itself
+    if float(gamma).is_integer() and float(beta).is_integer():
+        assert oracle.piecewise_index(gamma, alpha, beta, gamma) == int(beta)
+        assert oracle.piecewise_index(-gamma, alpha, beta, gamma) == -int(beta)
+
+
+def test_product_table_has_fifty_entries_with_cls():
+    # Pitfalls: "the Product table has 7 x 7 + 1 = 50 entries" at r = 1.9
+    _, K = oracle.product_bucket_ids(14, 14, *R19)
+    assert K + 1 == 50
+
+
+# ---------------------------------------------------------------- eq. 25 ids
+
+def test_product_ids_range_mirror_centre():
+    H = W = 14
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    assert K == 49 and ids.shape == (196, 196)
+    assert ids.min() == 0 and ids.max() == K - 1
+    assert set(np.unique(ids)) == set(range(K))
+    # g is odd, so swapping query and key mirrors the id: id(j,i) = K-1-id(i,j)
+    assert np.array_equal(ids.T, K - 1 - ids)
+    assert np.all(np.diag(ids) == (K - 1) // 2)
+
+
+def test_product_ids_sign_and_axis_order():
+    # Offsets are query minus key (Swin notes 3.2 worked example), row offset is the
+    # major index (iRPE eq. 25 pseudocode: offsets[...,0] is the row).
+    H = W = 14
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    span = 7
+    at = lambda r, c: r * W + c  # noqa: E731
+    # query (0,0), key (2,2): offset (-2,-2) -> indices (-2,-2) -> (1,1) after +3
+    assert ids[at(0, 0), at(2, 2)] == 1 * span + 1
+    # query (0,0), key (0,1): row 0 -> 3, col -1 -> 2
+    assert ids[at(0, 0), at(0, 1)] == 3 * span + 2
+    # query (0,0), key (1,0): row -1 -> 2, col 0 -> 3 (differs from the above: axes not swapped)
+    assert ids[at(0, 0), at(1, 0)] == 2 * span + 3
+    # far corner: offset (-13,-13) -> (-3,-3) -> id 0; reversed pair -> K-1
+    assert ids[at(0, 0), at(13, 13)] == 0
+    assert ids[at(13, 13), at(0, 0)] == K - 1
+
+
+def test_product_ids_translation_invariant():
+    # the id depends only on the offset between the two positions (Swin notes 2.2)
+    H, W = 9, 11
+    ids, _ = oracle.product_bucket_ids(H, W, *R19)
+    seen = {}
+    for i in range(H * W):
+        for j in range(H * W):
+            key = (i // W - j // W, i % W - j % W)
+            assert seen.setdefault(key, ids[i, j]) == ids[i, j]
+
+
+# ---------------------------------------------------------------- Swin index
+
+def test_swin_worked_example_m3():
+    for M, qr, qc, kr, kc, tr, tc in read_golden("swin_m3_example.txt"):
+        M = int(M)
+        idx, nb = oracle.swin_bias_index(M)
+        side = 2 * M - 1
+        assert nb == side * side == 25
+        i, j = int(qr) * M + int(qc), int(kr) * M + int(kc)
+        assert idx[i, j] == int(tr) * side + int(tc)
+
+
+def test_swin_table_sizes():
+    for M, brute, compact in read_golden("swin_table_sizes.txt"):
+        M = int(M)
+        idx, nb = oracle.swin_bias_index(M)
+        assert nb == int(compact)
+        assert idx.size == int(brute)                 # one entry per pair: M^2 x M^2
+        assert len(np.unique(idx)) == int(compact)    # every table entry is used
+
+
+def test_swin_index_translation_invariant_and_centre():
+    M = 7
+    idx, nb = oracle.swin_bias_index(M)
+    for i in range(M * M):
+        for j in range(M * M):
+            dr, dc = i // M - j // M, i % M - j % M
+            # shifted offsets land in [0, 2M-2] on both axes
+            assert 0 <= idx[i, j] // (2 * M - 1) <= 2 * M - 2
+            assert idx[i, j] == idx[(i // M) * M + i % M, j]
+            if dr == 0 and dc == 0:
+                assert idx[i, j] == (M - 1) * (2 * M - 1) + (M - 1) == 84
+
+
+# ---------------------------------------------------------------- Shaw clip + printed weights
+
+def test_clip_ids_shift():
+    k = 3
+    ids = oracle.clip_ids_1d(6, k)
+    assert ids[0, 0] == k          # offset 0 -> index k
+    assert ids[5, 0] == 0          # offset -5 clipped to -k -> 0
+    assert ids[0, 5] == 2 * k      # offset +5 clipped to +k -> 2k
+    assert ids[2, 1] == k - 1 and ids[1, 2] == k + 1
+
+
+def _shaw_inputs():
+    rs = np.random  # the page's example uses numpy's legacy seeded generator
+    rs.seed(42)
+    X = rs.randn(6, 8)
+    rs.seed(123)
+    s_qk = np.sqrt(2.0 / (8 + 4))
+    Wq, Wk, Wv = rs.randn(8, 4) * s_qk, rs.randn(8, 4) * s_qk, rs.randn(8, 4) * s_qk
+    rs.seed(123)
+    s_tab = np.sqrt(2.0 / (7 + 4))
+    aK = rs.randn(7, 4) * s_tab
+    aV = rs.randn(7, 4) * s_tab
+    return X @ Wq, X @ Wk, X @ Wv, aK, aV
+
+
+def test_shaw_printed_attention_weights():
+    Q, K, V, aK, aV = _shaw_inputs()
+    ids = oracle.clip_ids_1d(6, 3)
+    out, attn = oracle.attention(Q, K, V, ids, 7, tab_k=aK, tab_v=aV, want_attn=True)
+    printed = np.array(read_golden("shaw_weights_6x6.txt"))
+    assert np.max(np.abs(attn - printed)) <= 5e-4 + 1e-12
+    assert np.allclose(attn.sum(axis=1), 1.0, atol=1e-12)
+    # the position term matters here: without it the weights are far off
+    _, plain = oracle.attention(Q, K, V, ids, 7, want_attn=True)
+    assert np.max(np.abs(plain - printed)) > 1e-2
+
+
+# ---------------------------------------------------------------- attention special cases
+
+def _rand(shape, seed):
+    return np.random.default_rng(seed).standard_normal(shape)
+
+
+def _sdpa(q, k, v):
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a))[None, None]  # noqa: E731
+    return torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v))[0, 0].numpy()
+
+
+def test_zero_tables_equal_library_sdpa():
+    H, W, d = 5, 6, 16
+    n = H * W
+    q, k, v = _rand((n, d), 1), _rand((n, d), 2), _rand((n, d), 3)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    z = np.zeros((K, d))
+    out = oracle.attention(q, k, v, ids, K, tab_k=z, tab_q=z, tab_v=z, bias=np.zeros(K))
+    assert np.max(np.abs(out - _sdpa(q, k, v))) < 1e-12
+
+
+def test_constant_key_table_is_softmax_shift():
+    # q.(k_j + c) = q.k_j + q.c: a per-row constant, which softmax removes
+    H, W, d = 4, 5, 8
+    n = H * W
+    q, k, v = _rand((n, d), 4), _rand((n, d), 5), _rand((n, d), 6)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    c = _rand((d,), 7)
+    out = oracle.attention(q, k, v, ids, K, tab_k=np.tile(c, (K, 1)))
+    assert np.max(np.abs(out - _sdpa(q, k, v))) < 1e-12
+
+
+def test_constant_query_table_is_query_shift():
+    # k_j.c is added to logit (i,j): (q_i + c).k_j -- attention with q shifted by c.
+    # A transposed operand (q_i.c) would instead leave the output unchanged.
+    H, W, d = 4, 5, 8
+    n = H * W
+    q, k, v = _rand((n, d), 8), _rand((n, d), 9), _rand((n, d), 10)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    c = _rand((d,), 11)
+    out = oracle.attention(q, k, v, ids, K, tab_q=np.tile(c, (K, 1)))
+    assert np.max(np.abs(out - _sdpa(q + c, k, v))) < 1e-12
+    assert np.max(np.abs(out - _sdpa(q, k, v))) > 1e-3
+
+
+def test_constant_value_table_adds_constant():
+    # sum_j a_ij = 1, so a value table with every row c adds exactly c (eq. 17)
+    H, W, d = 4, 5, 8
+    n = H * W
+    q, k, v = _rand((n, d), 12), _rand((n, d), 13), _rand((n, d), 14)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    c = _rand((d,), 15)
+    out = oracle.attention(q, k, v, ids, K, tab_v=np.tile(c, (K, 1)))
+    assert np.max(np.abs(out - (_sdpa(q, k, v) + c))) < 1e-12
+
+
+def test_hard_bias_selects_one_neighbour_and_its_value_entry():
+    # A bias of -1e4 on every bucket but one forces each query onto the key at that
+    # offset. With offset (0,+1) in query-minus-key terms the chosen key is the left
+    # neighbour (same row, column - 1); the value term then adds R^V at that bucket.
+    H = W = 6
+    n, d = H * W, 8
+    q, k, v = 0.1 * _rand((n, d), 16), 0.1 * _rand((n, d), 17), _rand((n, d), 18)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    target = (0 + 3) * 7 + (1 + 3)  # row offset 0, column offset +1
+    bias = np.full(K, -1e4)
+    bias[target] = 0.0
+    tv = _rand((K, d), 19)
+    out = oracle.attention(q, k, v, ids, K, tab_v=tv, bias=bias)
+    for i in range(n):
+        r, c = divmod(i, W)
+        if c >= 1:
+            assert np.allclose(out[i], v[i - 1] + tv[target], atol=1e-9)
+
+
+def test_efficient_form_equals_per_pair():
+    # eqs. 26-28 re-associate the same sums: QR / KR gathers and per-bucket sums
+    H, W, d = 6, 7, 16
+    n = H * W
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    q, k, v = _rand((n, d), 20), _rand((n, d), 21), _rand((n, d), 22)
+    tk, tq, tv = _rand((K, d), 23), _rand((K, d), 24), _rand((K, d), 25)
+    bias = _rand((K,), 26)
+    a = oracle.attention(q, k, v, ids, K, tab_k=tk, tab_q=tq, tab_v=tv, bias=bias)
+    b = oracle.attention_efficient(q, k, v, ids, K, tab_k=tk, tab_q=tq, tab_v=tv, bias=bias)
+    assert np.max(np.abs(a - b)) < 1e-12
+
+
+def test_swin_constant_table_and_self_mask():
+    M, d, heads = 7, 32, 3
+    n = M * M
+    q, k, v = (_rand((2, heads, n, d), s) for s in (27, 28, 29))
+    zero = oracle.swin_attention(q, k, v, np.zeros(((2 * M - 1) ** 2, heads)), M)
+    for w in range(2):
+        for h in range(heads):
+            assert np.max(np.abs(zero[w, h] - _sdpa(q[w, h], k[w, h], v[w, h]))) < 1e-12
+    const = oracle.swin_attention(q, k, v, np.full(((2 * M - 1) ** 2, heads), 0.7), M)
+    assert np.max(np.abs(const - zero)) < 1e-12
+    mask = np.full(((2 * M - 1) ** 2, heads), -1e4)
+    mask[(M - 1) * (2 * M - 1) + (M - 1), :] = 0.0     # only offset (0,0) survives
+    self_only = oracle.swin_attention(0.1 * q, 0.1 * k, v, mask, M)
+    assert np.max(np.abs(self_only - v)) < 1e-9
+
+
+def test_swin_bias_is_added_after_scaling():
+    # with q = k = 0 the logits are the bias alone, so weights are softmax(B[i, :])
+    M, d = 3, 4
+    n = M * M
+    z = np.zeros((1, 1, n, d))
+    v = _rand((1, 1, n, d), 30)
+    table = _rand(((2 * M - 1) ** 2, 1), 31) * 2.0
+    out = oracle.swin_attention(z, z, v, table, M)
+    idx, _ = oracle.swin_bias_index(M)
+    B = table[idx, 0]
+    a = np.exp(B - B.max(axis=1, keepdims=True))
+    a /= a.sum(axis=1, keepdims=True)
+    assert np.max(np.abs(out[0, 0] - a @ v[0, 0])) < 1e-12
+
+
+def test_irpe_batched_matches_slices_and_rows():
+    H, W, d = 4, 4, 8
+    n = H * W
+    B, heads = 2, 3
+    q, k, v = (_rand((B, heads, n, d), s) for s in (32, 33, 34))
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    tk, tq, tv = (_rand((K, d), s) for s in (35, 36, 37))
+    full = oracle.irpe_attention(q, k, v, H, W, *R19, 7, tab_q=tq, tab_k=tk, tab_v=tv)
+    for b in range(B):
+        for h in range(heads):
+            one = oracle.attention(q[b, h], k[b, h], v[b, h], ids, K, tab_k=tk, tab_q=tq,
+                                   tab_v=tv)
+            assert np.array_equal(one, full[b, h])
+    part = oracle.irpe_attention(q, k, v, H, W, *R19, 7, tab_q=tq, tab_k=tk, tab_v=tv,
+                                 slices=[4], rows=[0, 5, 15])
+    assert np.array_equal(part[1, 1, [0, 5, 15]], full[1, 1, [0, 5, 15]])
+    assert np.all(part[0] == 0)
+
+
+def test_stress_tables_move_output_beyond_tolerance():
+    # negative control: at std 1.0 the position term changes outputs by far more
+    # than the 2e-2 bf16 tolerance, so a kernel that drops a term cannot pass
+    H = W = 14
+    d = 64
+    n = H * W
+    q, k, v = (_rand((1, 1, n, d), s) for s in (38, 39, 40))
+    _, K = oracle.product_bucket_ids(H, W, *R19)
+    for flag, name in ((1, "tab_k"), (2, "tab_q"), (4, "tab_v")):
+        tab = _rand((K, d), 41)
+        with_term = oracle.irpe_attention(q, k, v, H, W, *R19, flag, **{name: tab})
+        without = oracle.irpe_attention(q, k, v, H, W, *R19, 0)
+        assert np.max(np.abs(with_term - without)) > 0.2, name
+    M = 7
+    qs, ks, vs = (_rand((1, 3, 49, 32), s) for s in (42, 43, 44))
+    t = 2.0 * _rand((169, 3), 45)
+    assert np.max(np.abs(oracle.swin_attention(qs, ks, vs, t, M)
+                         - oracle.swin_attention(qs, ks, vs, 0 * t, M))) > 0.2

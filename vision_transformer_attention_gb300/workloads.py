@@ -1,0 +1,141 @@
+"""Seeded synthetic workloads: shapes and input generators, nothing else.
+
+This module holds none of the attention arithmetic. It is the one module that
+both the CUDA path and the oracle receive inputs from, so that a parity test
+compares the two on identical values.
+
+Shapes follow the pages' workloads: DeiT-S uses a 14 x 14 token grid with 6
+heads of 64 channels ("Rethinking and Improving Relative Position Encoding for
+Vision Transformer", Problem; section 4.1), and Swin attends inside 7 x 7
+windows ("Swin Transformer, section 3.2 and Table 4", Conditions). Swin-T
+stage 1 has 3 heads of 32 channels on a 56 x 56 map. No dataset is used:
+q, k, v ~ N(0, 1) and every relative-position table ~ N(0, 0.02^2), drawn in
+fp32 from a CPU ``torch.Generator`` and then cast to the working dtype.
+Seeds: q 0, k 1, v 2, table t (Q, K, V, or the Swin bias) 3 + t, each offset
+by ``seed``.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+FLAG_K = 1
+FLAG_Q = 2
+FLAG_V = 4
+
+# The iRPE index-function constants scale with a ratio r as alpha = r,
+# beta = 2r, gamma = 8r; the DeiT Product configuration uses r = 1.9
+# (iRPE page, Paper-vs-code list, "Product and the ratio").
+IRPE_RATIO = 1.9
+
+
+def index_constants(ratio: float = IRPE_RATIO):
+    return float(ratio), 2.0 * ratio, 8.0 * ratio
+
+
+@dataclasses.dataclass(frozen=True)
+class SwinConfig:
+    name: str
+    num_windows: int
+    heads: int
+    M: int
+    d: int
+    dtype: str  # "bf16" or "f32"
+
+    @property
+    def n(self) -> int:
+        return self.M * self.M
+
+    @property
+    def tokens(self) -> int:
+        return self.num_windows * self.n
+
+
+@dataclasses.dataclass(frozen=True)
+class IrpeConfig:
+    name: str
+    B: int
+    heads: int
+    H: int
+    W: int
+    d: int
+    flags: int
+    dtype: str
+    ratio: float = IRPE_RATIO
+
+    @property
+    def N(self) -> int:
+        return self.H * self.W
+
+    @property
+    def num_buckets(self) -> int:
+        span = 2 * int(2.0 * self.ratio) + 1
+        return span * span
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.N
+
+
+CONFIGS = {
+    # 4 windows of 7x7, 3 heads, d = 32, fp32 (the small parity case)
+    "swin_w7_small_fp32": SwinConfig("swin_w7_small_fp32", 4, 3, 7, 32, "f32"),
+    # Swin-T stage 1: 56x56 map = 64 windows, batch 32 -> 2048 windows
+    "swin_t_stage1": SwinConfig("swin_t_stage1", 2048, 3, 7, 32, "bf16"),
+    # iRPE-K at the DeiT-S shape, 14x14 grid, no class token
+    "irpe_k_deit_s": IrpeConfig("irpe_k_deit_s", 64, 6, 14, 14, 64, FLAG_K, "bf16"),
+    # iRPE on queries, keys and values, same shape
+    "irpe_qkv_deit_s": IrpeConfig("irpe_qkv_deit_s", 64, 6, 14, 14, 64,
+                                  FLAG_Q | FLAG_K | FLAG_V, "bf16"),
+    # high-resolution global attention, 56x56 grid
+    "irpe_k_56x56": IrpeConfig("irpe_k_56x56", 8, 6, 56, 56, 64, FLAG_K, "bf16"),
+}
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return _TORCH_DTYPE[name]
+
+
+def _normal(shape, seed, std=1.0):
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return torch.randn(*shape, generator=g, dtype=torch.float32) * std
+
+
+def swin_inputs(num_windows, heads, M, d, dtype="bf16", table_std=0.02, seed=0):
+    """q, k, v [num_windows, heads, M*M, d] and the bias table [(2M-1)^2, heads]."""
+    dt = _TORCH_DTYPE[dtype]
+    n = M * M
+    shape = (num_windows, heads, n, d)
+    q = _normal(shape, seed + 0).to(dt)
+    k = _normal(shape, seed + 1).to(dt)
+    v = _normal(shape, seed + 2).to(dt)
+    table = _normal(((2 * M - 1) ** 2, heads), seed + 3, table_std)  # fp32
+    return {"q": q, "k": k, "v": v, "table": table}
+
+
+def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02, seed=0):
+    """q, k, v [B, heads, N, d] and head-shared tables [num_buckets, d] for the
+    enabled terms (None for a disabled one)."""
+    dt = _TORCH_DTYPE[dtype]
+    shape = (B, heads, N, d)
+    out = {
+        "q": _normal(shape, seed + 0).to(dt),
+        "k": _normal(shape, seed + 1).to(dt),
+        "v": _normal(shape, seed + 2).to(dt),
+    }
+    for t, (name, flag) in enumerate((("tab_q", FLAG_Q), ("tab_k", FLAG_K), ("tab_v", FLAG_V))):
+        out[name] = (_normal((num_buckets, d), seed + 3 + t, table_std).to(dt)
+                     if flags & flag else None)
+    return out
+
+
+def config_inputs(cfg, table_std=0.02, seed=0):
+    if isinstance(cfg, SwinConfig):
+        return swin_inputs(cfg.num_windows, cfg.heads, cfg.M, cfg.d, cfg.dtype,
+                           table_std, seed)
+    return irpe_inputs(cfg.B, cfg.heads, cfg.N, cfg.d, cfg.num_buckets, cfg.flags,
+                       cfg.dtype, table_std, seed)
