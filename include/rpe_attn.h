@@ -1,0 +1,154 @@
+/*
+ * rpe_attn.h -- C ABI of the GB300 relative-position attention library
+ * (libvta_gb300.so). Plain pointers and sizes only; no C++ or torch types.
+ *
+ * Sources, by page title and section:
+ *   iRPE  = "Rethinking and Improving Relative Position Encoding for Vision
+ *           Transformer": Method (eq. 13 unified logit, eq. 15 contextual key,
+ *           eq. 16 contextual query, eq. 17 contextual value, eq. 18 piecewise
+ *           index, eq. 25 Product mapping, eqs. 26-28 efficient computation).
+ *   SWIN  = "Swin Transformer, section 3.2 and Table 4": SoftMax(QK^T/sqrt(d) + B)V.
+ *   SWIN2D= "Swin 的二维 RPE" (Swin's 2D RPE), sections 3.1-3.2: the compact
+ *           (2M-1) x (2M-1) table read at the offset shifted by M-1.
+ *
+ * Conventions shared by every call
+ *   - Tokens of an H x W grid are numbered row-major: token i sits at
+ *     (i / W, i % W). An offset is query minus key, (dr, dc) = (r_i - r_j,
+ *     c_i - c_j).
+ *   - Device pointers must be 16-byte aligned and point to contiguous
+ *     row-major memory of the stated shape. The caller owns every buffer;
+ *     the library never frees or keeps a caller pointer after the call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream). Argument errors are detected on the
+ *     host before any launch and return RPE_ERR_INVALID_ARG or
+ *     RPE_ERR_UNSUPPORTED; a failed launch returns RPE_ERR_CUDA.
+ *   - Every wait inside a kernel is bounded (2 s of GPU time). A wait that
+ *     runs out sets a bit in a per-device status word and the kernel returns
+ *     early, leaving its output undefined; rpe_device_status() reads the word.
+ *     The word is the library's only device allocation (256 bytes per
+ *     device, made on the first call on that device).
+ *   - There is no CPU fallback: without a usable sm_103 GPU the calls
+ *     return RPE_ERR_CUDA.
+ */
+#ifndef VTA_GB300_RPE_ATTN_H
+#define VTA_GB300_RPE_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+enum {
+    RPE_OK = 0,
+    RPE_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or flag      */
+    RPE_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement     */
+    RPE_ERR_CUDA = 3,        /* a CUDA runtime / driver call failed              */
+    RPE_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (device status) */
+};
+
+/* Offset-to-bucket mappings (iRPE section 3.2). Only Product is built. */
+enum { RPE_MAP_PRODUCT = 0 };
+
+/* Which contextual terms rpe_attn_fwd adds (iRPE eqs. 15-17). */
+enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4 };
+
+/* Element types of q, k, v, out and the iRPE tables. */
+enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
+
+/*
+ * rpe_build_bucket_ids -- iRPE eq. 18 and eq. 25, evaluated on the GPU in
+ * double precision.
+ *
+ * For an H x W grid and index-function constants 0 < alpha <= beta <= gamma
+ * (the code's ratio r gives alpha = r, beta = 2r, gamma = 8r), computes the
+ * piecewise index g of every axis offset and pairs the row and column
+ * indices into the Product bucket
+ *     id = (g(dr) + h) * (2h + 1) + (g(dc) + h),   h = int(beta).
+ * Outputs (device, int32, written on `stream`):
+ *   bucket_lut [(2H-1) * (2W-1)]  id of offset (dr, dc) at
+ *                                 (dr + H - 1) * (2W - 1) + (dc + W - 1).
+ *                                 rpe_attn_fwd consumes this form: every
+ *                                 mapping on the pages is translation
+ *                                 invariant, so the N x N map is this table
+ *                                 read at each pair's offset.
+ *   ids        [N * N] or NULL    the expanded map (query i, key j at i*N + j),
+ *                                 N = H * W, read from the same table.
+ *   num_buckets (host int*)       set to (2h + 1)^2.
+ * Errors (RPE_ERR_INVALID_ARG): H or W < 1, N*N >= 2^31, alpha <= 0,
+ * alpha > beta or beta > gamma or a non-finite constant, mode other than
+ * RPE_MAP_PRODUCT, a NULL bucket_lut or num_buckets, (2h+1)^2 > 256.
+ */
+int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
+                         double gamma, int32_t *bucket_lut, int32_t *ids,
+                         int *num_buckets, void *stream);
+
+/*
+ * rpe_attn_fwd -- iRPE contextual attention on an H x W grid (eqs. 13, 15-17),
+ * forward only, the contextual terms computed the efficient way (eqs. 26-28).
+ *
+ *   e_ij  = ( q_i.k_j + [K] q_i.R^K[id] + [Q] k_j.R^Q[id] ) / sqrt(d)
+ *   out_i = sum_j softmax_j(e_ij) * ( v_j + [V] R^V[id] ),   id = id(i, j)
+ *
+ * q, k, v, out : device [B, heads, N, d], N = H * W, element type `dtype`.
+ * table_q/k/v  : device [num_buckets, d], same element type, shared by all
+ *                heads; NULL for a term whose bit is not set in `terms` (a
+ *                table whose bit is off is not read).
+ * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids (or
+ *                any table of ids in [0, num_buckets) indexed the same way;
+ *                an id outside that range gives undefined output).
+ * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention).
+ * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
+ * accumulation, probabilities rounded to bf16 before the value products);
+ * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 64;
+ * N <= 65536. Anything else returns RPE_ERR_UNSUPPORTED.
+ */
+int rpe_attn_fwd(const void *q, const void *k, const void *v,
+                 const void *table_q, const void *table_k, const void *table_v,
+                 const int32_t *bucket_lut, int num_buckets,
+                 int B, int heads, int H, int W, int d,
+                 unsigned terms, int dtype, void *out, void *stream);
+
+/*
+ * swin_window_attn_fwd -- Swin window attention with the relative bias
+ * (SWIN; SWIN2D 3.1-3.2), forward only:
+ *
+ *   out = SoftMax( Q K^T / sqrt(d) + B ) V,
+ *   B[i, j] = table[ (dr + M - 1) * (2M - 1) + (dc + M - 1) ][ head ]
+ *
+ * q, k, v, out : device [num_windows, heads, M*M, d], element type `dtype`
+ *                (windows already partitioned; token i of a window sits at
+ *                (i / M, i % M)).
+ * bias_table   : device float32 [(2M-1)^2, heads] (bucket-major).
+ * Supported: RPE_DTYPE_BF16 with M == 7 and d in {32, 64} (tcgen05 tensor
+ * cores); RPE_DTYPE_F32 with 2 <= M <= 8 and d <= 64 (fp32 on CUDA cores).
+ */
+int swin_window_attn_fwd(const void *q, const void *k, const void *v,
+                         const float *bias_table, int num_windows, int heads,
+                         int M, int d, int dtype, void *out, void *stream);
+
+/*
+ * rpe_device_status -- synchronises the current device and returns, through
+ * *status, the word the kernels set when a bounded wait ran out (0 = none).
+ * Clears the word when `clear` is non-zero. Returns RPE_ERR_TIMEOUT if any
+ * bit was set, RPE_ERR_CUDA if synchronising failed, else RPE_OK.
+ */
+int rpe_device_status(unsigned *status, int clear);
+
+/*
+ * rpe_wait_probe -- runs the bounded-wait routine every kernel uses on a
+ * barrier that nothing ever arrives at, with a bound of `limit_ns`
+ * nanoseconds (1 ms if 0), so that a test can see the wait run out and set
+ * the status word without faulting or hanging the GPU.
+ */
+int rpe_wait_probe(uint64_t limit_ns, void *stream);
+
+/* rpe_status_string -- a static description of a status code. */
+const char *rpe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VTA_GB300_RPE_ATTN_H */

@@ -1,0 +1,132 @@
+"""GPU parity: the CUDA library, called through its C ABI, against the oracle.
+
+Tolerances (written here, derived in the design doc): bucket ids bit-exact;
+bf16 attention <= 2e-2 max abs error (bf16 inputs, fp32 accumulation,
+probabilities rounded to bf16 before the value products); fp32 attention
+<= 1e-4 max abs error.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vision_transformer_attention_gb300 import api, workloads
+from vision_transformer_attention_gb300.workloads import CONFIGS, FLAG_K, FLAG_Q, FLAG_V
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+R19 = workloads.index_constants(1.9)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    assert api.rpe_device_status(clear=True) == 0
+
+
+def _dev(d):
+    return {k: (None if t is None else t.cuda()) for k, t in d.items()}
+
+
+def _maxerr(gpu, ref):
+    return float(np.max(np.abs(gpu.detach().float().cpu().numpy().astype(np.float64) - ref)))
+
+
+# ------------------------------------------------------------------ bucket ids
+
+@pytest.mark.parametrize("H,W,ratio", [(14, 14, 1.9), (56, 56, 1.9), (5, 9, 1.9), (1, 7, 1.9),
+                                       (14, 14, 2.0), (9, 4, 3.5), (1, 1, 1.9)])
+def test_bucket_ids_bit_exact(H, W, ratio):
+    a, b, g = workloads.index_constants(ratio)
+    lut, ids, nb = api.rpe_build_bucket_ids(H, W, a, b, g, with_ids=True)
+    ref, nb_ref = oracle.product_bucket_ids(H, W, a, b, g)
+    assert nb == nb_ref
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ Swin
+
+def _swin_case(nw, heads, d, dtype, table_std=0.02, seed=0):
+    inp = workloads.swin_inputs(nw, heads, 7, d, dtype, table_std, seed)
+    g = _dev(inp)
+    out = api.swin_window_attn_fwd(g["q"], g["k"], g["v"], g["table"], 7)
+    return inp, out
+
+
+@pytest.mark.parametrize("table_std", [0.02, 2.0])
+def test_swin_fp32_small_config(table_std):
+    cfg = CONFIGS["swin_w7_small_fp32"]
+    inp, out = _swin_case(cfg.num_windows, cfg.heads, cfg.d, "f32", table_std)
+    ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7)
+    assert _maxerr(out, ref) <= TOL_F32
+    if table_std > 1:  # negative control: the bias matters far beyond the tolerance
+        plain = oracle.swin_attention(inp["q"], inp["k"], inp["v"], 0 * inp["table"], 7)
+        assert np.max(np.abs(plain - ref)) > 50 * TOL_F32
+
+
+@pytest.mark.parametrize("nw,heads,d", [(4, 3, 32), (5, 3, 32), (1, 1, 32), (3, 5, 64), (37, 3, 32)])
+@pytest.mark.parametrize("table_std", [0.02, 2.0])
+def test_swin_bf16_small(nw, heads, d, table_std):
+    inp, out = _swin_case(nw, heads, d, "bf16", table_std, seed=nw)
+    ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7)
+    assert _maxerr(out, ref) <= TOL_BF16
+
+
+def test_swin_bf16_swin_t_stage1_sampled():
+    cfg = CONFIGS["swin_t_stage1"]
+    inp, out = _swin_case(cfg.num_windows, cfg.heads, cfg.d, "bf16")
+    units = cfg.num_windows * cfg.heads
+    rng = np.random.default_rng(0)
+    sl = np.unique(np.concatenate([rng.choice(units, 96, replace=False), [0, 1, units - 2, units - 1]]))
+    ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7, slices=sl)
+    got = out.reshape(units, 49, cfg.d)[torch.as_tensor(sl, device=out.device)]
+    ref = ref.reshape(units, 49, cfg.d)[sl]
+    assert _maxerr(got, ref) <= TOL_BF16
+    # property at any size: every output row is a convex combination of its window's v rows
+    v = inp["v"].float().reshape(units, 49, cfg.d).cuda()
+    o = out.float().reshape(units, 49, cfg.d)
+    assert torch.all(o <= v.amax(dim=1, keepdim=True) + TOL_BF16)
+    assert torch.all(o >= v.amin(dim=1, keepdim=True) - TOL_BF16)
+
+
+def test_swin_bf16_repeat_is_deterministic():
+    inp, out1 = _swin_case(9, 3, 32, "bf16")
+    g = _dev(inp)
+    out2 = api.swin_window_attn_fwd(g["q"], g["k"], g["v"], g["table"], 7)
+    assert torch.equal(out1, out2)
+
+
+# ------------------------------------------------------------------ iRPE, fp32 path
+
+@pytest.mark.parametrize("H,W,flags", [(4, 5, FLAG_K), (7, 7, FLAG_Q | FLAG_K | FLAG_V),
+                                       (14, 14, FLAG_K | FLAG_V), (3, 30, FLAG_Q)])
+def test_irpe_fp32_small(H, W, flags):
+    B, heads, d = 2, 3, 64
+    nb = 49
+    inp = workloads.irpe_inputs(B, heads, H * W, d, nb, flags, "f32", table_std=1.0)
+    g = _dev(inp)
+    lut, _, nb_dev = api.rpe_build_bucket_ids(H, W, *R19)
+    assert nb_dev == nb
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ref = oracle.irpe_attention(inp["q"], inp["k"], inp["v"], H, W, *R19, flags,
+                                tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= TOL_F32
+
+
+# ------------------------------------------------------------------ bounded waits
+
+def test_wait_probe_times_out_and_reports():
+    assert api.rpe_device_status(clear=True) == 0
+    api.rpe_wait_probe(200_000)  # 0.2 ms bound on a barrier nothing arrives at
+    status = api.rpe_device_status(clear=True)
+    assert status != 0
+    assert api.rpe_device_status(clear=True) == 0
+    # the context is still usable afterwards
+    inp, out = _swin_case(2, 3, 32, "bf16")
+    ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7)
+    assert _maxerr(out, ref) <= TOL_BF16

@@ -1,0 +1,116 @@
+"""Thin Python binding of the C ABI (include/rpe_attn.h), one function per
+entry point and with the same names. It only marshals torch CUDA tensors
+into pointers and sizes: every step of the computation runs in the
+library's CUDA kernels, on the tensors' device and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import check
+
+_DTYPES = {torch.bfloat16: _lib.RPE_DTYPE_BF16, torch.float32: _lib.RPE_DTYPE_F32}
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype=None, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}")
+
+
+def rpe_build_bucket_ids(H, W, alpha, beta, gamma, device="cuda", with_ids=False,
+                         mode=_lib.RPE_MAP_PRODUCT):
+    """iRPE eq. 18 + eq. 25 on the GPU. Returns (bucket_lut, ids or None, num_buckets):
+    bucket_lut int32 [(2H-1)*(2W-1)] indexed by offset, ids int32 [N, N]."""
+    device = torch.device(device)
+    lut = torch.empty((2 * H - 1) * (2 * W - 1), dtype=torch.int32, device=device)
+    ids = torch.empty((H * W, H * W), dtype=torch.int32, device=device) if with_ids else None
+    nb = ctypes.c_int(0)
+    with torch.cuda.device(device):
+        check("rpe_build_bucket_ids", _lib.lib().rpe_build_bucket_ids(
+            H, W, mode, float(alpha), float(beta), float(gamma), _ptr(lut), _ptr(ids),
+            ctypes.byref(nb), _stream(lut)))
+    return lut, ids, nb.value
+
+
+def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, table_k=None,
+                 table_v=None, out=None):
+    """iRPE contextual attention (eqs. 13, 15-17) on q, k, v [B, heads, H*W, d]."""
+    _need(q, "q")
+    B, heads, N, d = q.shape
+    if q.dtype not in _DTYPES:
+        raise TypeError("q must be bfloat16 or float32")
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    _need(bucket_lut, "bucket_lut", torch.int32, ((2 * H - 1) * (2 * W - 1),), q.device)
+    tabs = {"table_q": (table_q, _lib.RPE_TERM_Q), "table_k": (table_k, _lib.RPE_TERM_K),
+            "table_v": (table_v, _lib.RPE_TERM_V)}
+    for name, (t, bit) in tabs.items():
+        if terms & bit:
+            _need(t, name, q.dtype, (num_buckets, d), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", q.dtype, q.shape, q.device)
+    use = lambda t, bit: _ptr(t) if terms & bit else None  # noqa: E731
+    with torch.cuda.device(q.device):
+        check("rpe_attn_fwd", _lib.lib().rpe_attn_fwd(
+            _ptr(q), _ptr(k), _ptr(v), use(table_q, _lib.RPE_TERM_Q),
+            use(table_k, _lib.RPE_TERM_K), use(table_v, _lib.RPE_TERM_V), _ptr(bucket_lut),
+            num_buckets, B, heads, H, W, d, terms, _DTYPES[q.dtype], _ptr(out), _stream(q)))
+    return out
+
+
+def swin_window_attn_fwd(q, k, v, bias_table, M, out=None):
+    """Swin window attention SoftMax(QK^T/sqrt(d) + B)V on [windows, heads, M*M, d]."""
+    _need(q, "q")
+    nw, heads, n, d = q.shape
+    if q.dtype not in _DTYPES:
+        raise TypeError("q must be bfloat16 or float32")
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    _need(bias_table, "bias_table", torch.float32, ((2 * M - 1) ** 2, heads), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", q.dtype, q.shape, q.device)
+    with torch.cuda.device(q.device):
+        check("swin_window_attn_fwd", _lib.lib().swin_window_attn_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), nw, heads, M, d, _DTYPES[q.dtype],
+            _ptr(out), _stream(q)))
+    return out
+
+
+def rpe_device_status(clear=True):
+    """Synchronises the device; returns the in-kernel timeout status word (0 = none)."""
+    st = ctypes.c_uint(0)
+    rc = _lib.lib().rpe_device_status(ctypes.byref(st), int(bool(clear)))
+    if rc not in (_lib.RPE_OK, _lib.RPE_ERR_TIMEOUT):
+        check("rpe_device_status", rc)
+    return st.value
+
+
+def rpe_wait_probe(limit_ns=1_000_000):
+    """Runs the bounded wait on a barrier nothing arrives at (a timeout self-test)."""
+    check("rpe_wait_probe", _lib.lib().rpe_wait_probe(
+        int(limit_ns), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)))

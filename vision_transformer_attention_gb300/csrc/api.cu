@@ -1,0 +1,270 @@
+// api.cu -- the C ABI declared in include/rpe_attn.h: argument checks, the
+// per-device status word, TMA tensor-map encoding and the kernel launches.
+// Every check happens on the host before any launch; nothing here computes
+// attention on the CPU.
+#include "rpe_attn.h"
+#include "vta_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+namespace vta {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned *g_status[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int status_of(cudaError_t err) { return err == cudaSuccess ? RPE_OK : RPE_ERR_CUDA; }
+
+// Kernel of rpe_wait_probe: waits on a barrier that nothing arrives at.
+__global__ void wait_probe_kernel(WaitCtl wc) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_wait(&bar, 0, wc, kStatusTimeoutProbe, nullptr);
+    }
+}
+
+}  // namespace
+
+unsigned *device_status_word() {
+    const int dev = current_device();
+    if (dev < 0) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_status[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, 256) != cudaSuccess) return nullptr;
+        if (cudaMemset(p, 0, 256) != cudaSuccess) {
+            cudaFree(p);
+            return nullptr;
+        }
+        g_status[dev] = static_cast<unsigned *>(p);
+    }
+    return g_status[dev];
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        g_sms[dev] = n > 0 ? n : 1;
+    }
+    return g_sms[dev];
+}
+
+bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *base,
+                       const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                       CUtensorMapSwizzle swizzle) {
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return false;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    cuuint64_t gdim[5];
+    cuuint64_t gstride[4];
+    cuuint32_t bdim[5];
+    cuuint32_t estride[5];
+    for (int i = 0; i < rank; ++i) {
+        gdim[i] = dims[i];
+        bdim[i] = box[i];
+        estride[i] = 1;
+        if (i + 1 < rank) gstride[i] = strides_bytes[i];
+    }
+    const CUresult r = g_encode(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base),
+                                gdim, gstride, bdim, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t stream) {
+    unsigned *status = device_status_word();
+    if (status == nullptr) return cudaErrorMemoryAllocation;
+    wait_probe_kernel<<<1, 32, 0, stream>>>(WaitCtl{status, limit_ns});
+    return cudaGetLastError();
+}
+
+}  // namespace vta
+
+using namespace vta;
+
+extern "C" {
+
+int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, double gamma,
+                         int32_t *bucket_lut, int32_t *ids, int *num_buckets, void *stream) {
+    if (H < 1 || W < 1 || mode != RPE_MAP_PRODUCT || bucket_lut == nullptr ||
+        num_buckets == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (!std::isfinite(alpha) || !std::isfinite(beta) || !std::isfinite(gamma) || alpha <= 0.0 ||
+        alpha > beta || beta > gamma || beta >= 127.0)
+        return RPE_ERR_INVALID_ARG;
+    const long long n = static_cast<long long>(H) * W;
+    if (n * n >= (1LL << 31) || H > 32768 || W > 32768) return RPE_ERR_INVALID_ARG;
+    const int half = static_cast<int>(beta);
+    const int span = 2 * half + 1;
+    if (span * span > 256) return RPE_ERR_INVALID_ARG;
+    if (!aligned16(bucket_lut) || (ids != nullptr && !aligned16(ids))) return RPE_ERR_INVALID_ARG;
+    *num_buckets = span * span;
+    return status_of(launch_build_bucket_lut(H, W, alpha, beta, gamma, bucket_lut, ids,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_q,
+                 const void *table_k, const void *table_v, const int32_t *bucket_lut,
+                 int num_buckets, int B, int heads, int H, int W, int d, unsigned terms, int dtype,
+                 void *out, void *stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bucket_lut == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
+    if ((terms & ~7u) != 0) return RPE_ERR_INVALID_ARG;
+    if (((terms & RPE_TERM_K) && table_k == nullptr) || ((terms & RPE_TERM_Q) && table_q == nullptr) ||
+        ((terms & RPE_TERM_V) && table_v == nullptr))
+        return RPE_ERR_INVALID_ARG;
+    if (dtype != RPE_DTYPE_BF16 && dtype != RPE_DTYPE_F32) return RPE_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, out, bucket_lut,
+                          (terms & RPE_TERM_Q) ? table_q : nullptr,
+                          (terms & RPE_TERM_K) ? table_k : nullptr,
+                          (terms & RPE_TERM_V) ? table_v : nullptr};
+    for (const void *p : ptrs)
+        if (p != nullptr && !aligned16(p)) return RPE_ERR_INVALID_ARG;
+    const long long N = static_cast<long long>(H) * W;
+    const long long slices = static_cast<long long>(B) * heads;
+    if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == RPE_DTYPE_F32) {
+        if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
+        F32AttnArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.out = static_cast<float *>(out);
+        a.slices = static_cast<int>(slices);
+        a.heads = heads;
+        a.N = static_cast<int>(N);
+        a.d = d;
+        a.H = H;
+        a.W = W;
+        a.lut = bucket_lut;
+        a.num_buckets = num_buckets;
+        a.tab_k = (terms & RPE_TERM_K) ? static_cast<const float *>(table_k) : nullptr;
+        a.tab_q = (terms & RPE_TERM_Q) ? static_cast<const float *>(table_q) : nullptr;
+        a.tab_v = (terms & RPE_TERM_V) ? static_cast<const float *>(table_v) : nullptr;
+        a.bias = nullptr;
+        a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+        return status_of(launch_attn_f32(a, st));
+    }
+    if (d != 64) return RPE_ERR_UNSUPPORTED;
+    RpeBf16Args a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.tab_q = (terms & RPE_TERM_Q) ? table_q : nullptr;
+    a.tab_k = (terms & RPE_TERM_K) ? table_k : nullptr;
+    a.tab_v = (terms & RPE_TERM_V) ? table_v : nullptr;
+    a.out = out;
+    a.lut = bucket_lut;
+    a.num_buckets = num_buckets;
+    a.B = B;
+    a.heads = heads;
+    a.H = H;
+    a.W = W;
+    a.d = d;
+    a.terms = terms;
+    return status_of(launch_rpe_bf16(a, st));
+}
+
+int swin_window_attn_fwd(const void *q, const void *k, const void *v, const float *bias_table,
+                         int num_windows, int heads, int M, int d, int dtype, void *out,
+                         void *stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bias_table == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (num_windows < 1 || heads < 1 || M < 1 || d < 1) return RPE_ERR_INVALID_ARG;
+    if (dtype != RPE_DTYPE_BF16 && dtype != RPE_DTYPE_F32) return RPE_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, out, bias_table};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
+    const long long units = static_cast<long long>(num_windows) * heads;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == RPE_DTYPE_F32) {
+        if (M < 2 || M > 8 || d > 64 || units > 65535) return RPE_ERR_UNSUPPORTED;
+        F32AttnArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.out = static_cast<float *>(out);
+        a.slices = static_cast<int>(units);
+        a.heads = heads;
+        a.N = M * M;
+        a.d = d;
+        a.H = M;
+        a.W = M;
+        a.lut = nullptr;  // the bucket of a pair is its shifted, flattened offset
+        a.num_buckets = (2 * M - 1) * (2 * M - 1);
+        a.bias = bias_table;
+        a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+        return status_of(launch_attn_f32(a, st));
+    }
+    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30))
+        return RPE_ERR_UNSUPPORTED;
+    SwinBf16Args a{q, k, v, out, bias_table, num_windows, heads, M, d};
+    return status_of(launch_swin_bf16(a, st));
+}
+
+int rpe_device_status(unsigned *status, int clear) {
+    if (status == nullptr) return RPE_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RPE_ERR_CUDA;
+    unsigned *word = device_status_word();
+    if (word == nullptr) return RPE_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaMemcpy(&host, word, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RPE_ERR_CUDA;
+    if (clear && host != 0 && cudaMemset(word, 0, sizeof(host)) != cudaSuccess) return RPE_ERR_CUDA;
+    *status = host;
+    return host ? RPE_ERR_TIMEOUT : RPE_OK;
+}
+
+int rpe_wait_probe(uint64_t limit_ns, void *stream) {
+    const unsigned long long lim = limit_ns ? limit_ns : 1000000ull;
+    if (lim > kDefaultWaitNs) return RPE_ERR_INVALID_ARG;
+    return status_of(launch_wait_probe(lim, static_cast<cudaStream_t>(stream)));
+}
+
+const char *rpe_status_string(int status) {
+    switch (status) {
+        case RPE_OK: return "ok";
+        case RPE_ERR_INVALID_ARG: return "invalid argument";
+        case RPE_ERR_UNSUPPORTED: return "unsupported shape, type or size";
+        case RPE_ERR_CUDA: return "CUDA error";
+        case RPE_ERR_TIMEOUT: return "an in-kernel wait timed out";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// attn_f32.cu -- fp32 relative-position attention on CUDA cores.
+//
+// The exact-precision path (fp32 inputs, fp32 arithmetic, expf), used where a
+// result within 1e-4 of the fp64 definition is required: tf32 tensor-core
+// products round operands to 10 mantissa bits and would miss that bound.
+//
+// One thread owns one query row. Logits follow the unified form of
+// "Rethinking and Improving Relative Position Encoding for Vision Transformer"
+// (eq. 13, with the contextual key / query terms of eqs. 15-16 inside the
+// 1/sqrt(d) scaling) and the Swin form of "Swin Transformer, section 3.2"
+// (bias added after the scaling). The value term is eq. 17. The softmax takes
+// two passes over the keys, one for the row maximum and normaliser and one
+// for the weighted sum, so nothing needs rescaling.
+#include "vta_internal.h"
+
+#include <cmath>
+
+namespace vta {
+namespace {
+
+constexpr int kRows = 64;  // query rows per block (one per thread)
+constexpr int kKeys = 64;  // keys staged in shared memory per step
+constexpr int kMaxD = 64;
+
+struct SmemF32 {
+    float k[kKeys][kMaxD];
+    float v[kKeys][kMaxD];
+};
+
+__device__ __forceinline__ int bucket_of(const F32AttnArgs &a, int i, int j) {
+    const int cols = 2 * a.W - 1;
+    const int off = (i / a.W - j / a.W + a.H - 1) * cols + (i % a.W - j % a.W + a.W - 1);
+    return a.lut ? __ldg(a.lut + off) : off;
+}
+
+__device__ __forceinline__ float logit(const F32AttnArgs &a, const float (&qi)[kMaxD],
+                                       const float *kj, int id, int head) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxD; ++c)
+        if (c < a.d) s = fmaf(qi[c], kj[c], s);
+    if (a.tab_k) {
+        const float *r = a.tab_k + static_cast<size_t>(id) * a.d;
+#pragma unroll
+        for (int c = 0; c < kMaxD; ++c)
+            if (c < a.d) s = fmaf(qi[c], __ldg(r + c), s);
+    }
+    if (a.tab_q) {
+        const float *r = a.tab_q + static_cast<size_t>(id) * a.d;
+        for (int c = 0; c < a.d; ++c) s = fmaf(kj[c], __ldg(r + c), s);
+    }
+    s *= a.scale;
+    if (a.bias) s += __ldg(a.bias + static_cast<size_t>(id) * a.heads + head);
+    return s;
+}
+
+__global__ void __launch_bounds__(kRows) attn_f32_kernel(F32AttnArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    SmemF32 &sm = *reinterpret_cast<SmemF32 *>(smem_raw);
+    const int slice = blockIdx.y;
+    const int head = slice % a.heads;
+    const int i = blockIdx.x * kRows + threadIdx.x;
+    const bool row_ok = i < a.N;
+    const size_t base = static_cast<size_t>(slice) * a.N * a.d;
+    const float *q = a.q + base;
+    const float *k = a.k + base;
+    const float *v = a.v + base;
+
+    float qi[kMaxD];
+#pragma unroll
+    for (int c = 0; c < kMaxD; ++c)
+        qi[c] = (row_ok && c < a.d) ? q[static_cast<size_t>(i) * a.d + c] : 0.f;
+
+    // pass 1: row maximum and normaliser, online over key blocks
+    float m = -INFINITY, l = 0.f;
+    for (int j0 = 0; j0 < a.N; j0 += kKeys) {
+        const int nk = min(kKeys, a.N - j0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nk * a.d; e += blockDim.x)
+            sm.k[e / a.d][e % a.d] = k[static_cast<size_t>(j0) * a.d + e];
+        __syncthreads();
+        if (row_ok) {
+            for (int jj = 0; jj < nk; ++jj) {
+                const float x = logit(a, qi, sm.k[jj], bucket_of(a, i, j0 + jj), head);
+                if (x > m) {
+                    l = l * expf(m - x) + 1.f;
+                    m = x;
+                } else {
+                    l += expf(x - m);
+                }
+            }
+        }
+    }
+    const float inv_l = 1.f / l;
+
+    // pass 2: weighted sum of the values plus the value-side table (eq. 17)
+    float acc[kMaxD];
+#pragma unroll
+    for (int c = 0; c < kMaxD; ++c) acc[c] = 0.f;
+    for (int j0 = 0; j0 < a.N; j0 += kKeys) {
+        const int nk = min(kKeys, a.N - j0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nk * a.d; e += blockDim.x) {
+            sm.k[e / a.d][e % a.d] = k[static_cast<size_t>(j0) * a.d + e];
+            sm.v[e / a.d][e % a.d] = v[static_cast<size_t>(j0) * a.d + e];
+        }
+        __syncthreads();
+        if (row_ok) {
+            for (int jj = 0; jj < nk; ++jj) {
+                const int id = bucket_of(a, i, j0 + jj);
+                const float p = expf(logit(a, qi, sm.k[jj], id, head) - m) * inv_l;
+#pragma unroll
+                for (int c = 0; c < kMaxD; ++c)
+                    if (c < a.d) acc[c] = fmaf(p, sm.v[jj][c], acc[c]);
+                if (a.tab_v) {
+                    const float *r = a.tab_v + static_cast<size_t>(id) * a.d;
+#pragma unroll
+                    for (int c = 0; c < kMaxD; ++c)
+                        if (c < a.d) acc[c] = fmaf(p, __ldg(r + c), acc[c]);
+                }
+            }
+        }
+    }
+    if (row_ok) {
+        float *o = a.out + base + static_cast<size_t>(i) * a.d;
+#pragma unroll
+        for (int c = 0; c < kMaxD; ++c)
+            if (c < a.d) o[c] = acc[c];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream) {
+    const size_t smem = sizeof(SmemF32);
+    cudaError_t err = cudaFuncSetAttribute(attn_f32_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
+    dim3 grid((a.N + kRows - 1) / kRows, a.slices);
+    attn_f32_kernel<<<grid, kRows, smem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace vta

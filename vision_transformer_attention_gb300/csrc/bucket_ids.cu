@@ -1,0 +1,74 @@
+// bucket_ids.cu -- iRPE eq. 18 (piecewise index) and eq. 25 (Product mapping)
+// evaluated on the GPU in double precision.
+//
+// "Rethinking and Improving Relative Position Encoding for Vision Transformer",
+// Method: an axis offset x keeps its own integer index while |x| <= alpha; past
+// alpha the index grows with log(|x| / alpha) / log(gamma / alpha), scaled into
+// [alpha, beta], is rounded, capped at beta and truncated toward zero after the
+// sign is applied. The Product id pairs the row and column indices into one
+// entry of a (2h+1) x (2h+1) table with h = int(beta) (Pitfalls: the table is
+// sized from int(beta), not from beta).
+//
+// A pair's id depends only on its offset, so the attention kernels read ids
+// from a table indexed by offset: lut[(dr + H - 1) * (2W - 1) + dc + W - 1].
+#include "vta_internal.h"
+
+#include <algorithm>
+#include <cmath>
+
+namespace vta {
+namespace {
+
+__device__ int piecewise_index(int offset, double alpha, double beta, double gamma) {
+    const double x = static_cast<double>(offset);
+    const double ax = fabs(x);
+    if (ax <= alpha) return static_cast<int>(rint(x));  // rint: round half to even
+    const double share = log(ax / alpha) / log(gamma / alpha);
+    const double spread = rint(alpha + share * (beta - alpha));
+    const double capped = fmin(beta, spread);
+    return static_cast<int>(x > 0.0 ? capped : -capped);  // the cast truncates toward zero
+}
+
+__global__ void build_lut_kernel(int H, int W, double alpha, double beta, double gamma,
+                                 int32_t *lut) {
+    const int cols = 2 * W - 1;
+    const int total = (2 * H - 1) * cols;
+    const int half = static_cast<int>(beta);
+    const int span = 2 * half + 1;
+    for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
+        const int dr = e / cols - (H - 1);
+        const int dc = e % cols - (W - 1);
+        const int gr = piecewise_index(dr, alpha, beta, gamma);
+        const int gc = piecewise_index(dc, alpha, beta, gamma);
+        lut[e] = (gr + half) * span + (gc + half);
+    }
+}
+
+__global__ void expand_ids_kernel(int H, int W, const int32_t *__restrict__ lut,
+                                  int32_t *__restrict__ ids) {
+    const int N = H * W;
+    const int cols = 2 * W - 1;
+    const long long total = static_cast<long long>(N) * N;
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(e / N), j = static_cast<int>(e % N);
+        const int dr = i / W - j / W, dc = i % W - j % W;
+        ids[e] = lut[(dr + H - 1) * cols + (dc + W - 1)];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_build_bucket_lut(int H, int W, double alpha, double beta, double gamma,
+                                    int32_t *lut, int32_t *ids, cudaStream_t stream) {
+    const int total = (2 * H - 1) * (2 * W - 1);
+    build_lut_kernel<<<(total + 255) / 256, 256, 0, stream>>>(H, W, alpha, beta, gamma, lut);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess || ids == nullptr) return err;
+    const long long n2 = static_cast<long long>(H * W) * (H * W);
+    const int blocks = static_cast<int>(std::min<long long>((n2 + 255) / 256, 8LL * sm_count()));
+    expand_ids_kernel<<<blocks, 256, 0, stream>>>(H, W, lut, ids);
+    return cudaGetLastError();
+}
+
+}  // namespace vta

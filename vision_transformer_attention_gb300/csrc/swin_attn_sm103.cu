@@ -1,0 +1,328 @@
+// swin_attn_sm103.cu -- Swin window attention with the relative-position bias
+// on sm_103a tensor cores (tcgen05 + TMEM + TMA), bf16 in, fp32 accumulate.
+//
+// What it computes ("Swin Transformer, section 3.2 and Table 4"):
+//     out = SoftMax(Q K^T / sqrt(d) + B) V inside every M x M window, where
+// B[i, j] is read from the compact (2M-1) x (2M-1) per-head table at the
+// pair's offset shifted by M-1 and flattened row-major ("Swin 的二维 RPE",
+// sections 3.1-3.2).
+//
+// Design. A (window, head) pair -- a "unit" -- has n = M*M <= 64 tokens, so
+// two units share one 128-row tensor-core tile: unit 2t sits in rows 0..63
+// of tile t and unit 2t+1 in rows 64..127. One 3D TMA box per operand
+// ([2 units][64 rows][d], rows past n zero-filled) stages Q, K and V. A
+// single M=128, N=128 MMA gives every query row its own unit's scores in
+// one 64-column half of S (the other half, cross-unit, is ignored). One
+// thread per row reads its half from TMEM, adds the bias from a shared-memory
+// copy of the table (the per-key offset is a compile-time immediate because
+// M is a template parameter), takes the softmax in base 2 and writes bf16
+// probabilities into the K-major P operand; the cross-unit half of P stays
+// zero, so a single M=128, N=d, K=128 MMA gives P V. The epilogue scales by
+// 1/rowsum, converts to bf16 and leaves through a TMA store that drops the
+// padding rows. No n x n bias is ever formed in global memory.
+//
+// The kernel is persistent (grid = a multiple of the SM count), double-
+// buffers Q/K/V so the next tile's loads overlap this tile's work, and runs
+// two CTAs per SM at d = 32 so one CTA's softmax overlaps the other's copies.
+#include "vta_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <cmath>
+
+namespace vta {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int M, int D>
+struct SwinTile {
+    static constexpr int kN = M * M;            // tokens per window
+    static constexpr int kRowBytes = D * 2;     // one bf16 row of q/k/v/out
+    static constexpr uint32_t kSwz = (D == 32) ? kSwizzle64B : kSwizzle128B;
+    static constexpr int kSbo = 8 * kRowBytes;  // stride between 8-row groups
+    static constexpr int kOperBytes = 128 * kRowBytes;
+    static constexpr int kStageBytes = 3 * kOperBytes;
+    static constexpr int kPBlockBytes = 128 * 128;  // [128 rows][64 keys] bf16
+    static constexpr int kPBytes = 2 * kPBlockBytes;
+    static constexpr int kNB = (2 * M - 1) * (2 * M - 1);
+    static constexpr int kNBPad = (kNB + 3) & ~3;
+    static constexpr int kMaxHeads = 32;
+    static constexpr int kSmemFixed = 1024 + 2 * kStageBytes + kPBytes + kOperBytes;
+    static int smem_bytes(int heads) { return kSmemFixed + heads * kNBPad * 4; }
+    static constexpr int kCtasPerSm = (D == 32) ? 2 : 1;
+    static_assert(kN <= 64, "a window must fit one 64-row slot");
+};
+
+template <int M, int D>
+__global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
+    swin_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                     const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ bias_table,
+                     int heads, int units, int tiles, float scale_log2e, WaitCtl wc) {
+    using T = SwinTile<M, D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stage_base = smem;
+    uint8_t *p_base = smem + 2 * T::kStageBytes;
+    uint8_t *o_stage = p_base + T::kPBytes;
+    float *bias_s = reinterpret_cast<float *>(o_stage + T::kOperBytes);
+
+    __shared__ __align__(8) uint64_t bar_load[2];
+    __shared__ __align__(8) uint64_t bar_s;
+    __shared__ __align__(8) uint64_t bar_o;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+
+    if (tid == 0) {
+        mbar_init(&bar_load[0], 1);
+        mbar_init(&bar_load[1], 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
+    }
+    if (warp == 0) tmem_alloc(&tmem_base_s, 128);
+
+    // Bias table -> shared memory, head-major, pre-multiplied by log2(e).
+    for (int e = tid; e < heads * T::kNB; e += blockDim.x) {
+        const int h = e / T::kNB, b = e % T::kNB;
+        bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * heads + h) * kLog2e;
+    }
+    // P starts all zero; each thread later rewrites only its own unit's half,
+    // so the cross-unit half stays zero for the whole kernel.
+    for (int e = tid; e < T::kPBytes / 16; e += blockDim.x)
+        st_shared_v4(smem_u32(p_base) + e * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+    const WaitCtl drain{wc.status, kDefaultWaitNs};
+
+    // Thread 0's bookkeeping of work in flight, for draining after an abort.
+    uint32_t loads_pending = 0;  // bit s: stage s has a load not yet waited for
+    uint32_t load_uses[2] = {0, 0};
+    uint64_t *mma_bar_pending = nullptr;
+    uint32_t mma_parity_pending = 0;
+
+    auto issue_load = [&](int tile, int stage) {
+        uint8_t *sb = stage_base + stage * T::kStageBytes;
+        mbar_arrive_expect_tx(&bar_load[stage], 3 * T::kOperBytes);
+        tma_load_3d(sb, &tm_q, &bar_load[stage], 0, 0, 2 * tile);
+        tma_load_3d(sb + T::kOperBytes, &tm_k, &bar_load[stage], 0, 0, 2 * tile);
+        tma_load_3d(sb + 2 * T::kOperBytes, &tm_v, &bar_load[stage], 0, 0, 2 * tile);
+        loads_pending |= 1u << stage;
+    };
+
+    if (tid == 0 && static_cast<int>(blockIdx.x) < tiles) issue_load(blockIdx.x, 0);
+
+    // Per-thread constants: which unit slot and which row of it this thread owns.
+    const int slot = tid >> 6;
+    const int r = tid & 63;
+    const int rr = (r < T::kN) ? r : 0;
+    const int bias_base = (rr / M) * (2 * M - 1) + (rr % M) + (M - 1) * (2 * M - 1) + (M - 1);
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t prow = smem_u32(p_base) + slot * T::kPBlockBytes + tid * 128;
+
+    int it = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
+        const int stage = it & 1;
+        uint8_t *sb = stage_base + stage * T::kStageBytes;
+
+        // ---- thread 0: prefetch the next tile, then S = Q K^T for this one
+        if (tid == 0 && !abort_flag) {
+            const int next = tile + gridDim.x;
+            if (next < tiles) issue_load(next, stage ^ 1);
+            if (mbar_wait(&bar_load[stage], load_uses[stage] & 1, wc, kStatusTimeoutLoad,
+                          &abort_flag)) {
+                loads_pending &= ~(1u << stage);
+                ++load_uses[stage];
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = smem_desc(smem_u32(sb) + kk * 32, 16, T::kSbo, T::kSwz);
+                    const uint64_t b =
+                        smem_desc(smem_u32(sb + T::kOperBytes) + kk * 32, 16, T::kSbo, T::kSwz);
+                    mma_bf16_ss(tmem, a, b, kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bar_s);
+                mma_bar_pending = &bar_s;
+                mma_parity_pending = it & 1;
+            }
+        }
+
+        // ---- every thread: softmax of its own row over its own unit's keys
+        const int unit = 2 * tile + slot;
+        const bool row_ok = (r < T::kN) && (unit < units);
+        float l = 1.f;
+        if (mbar_wait(&bar_s, it & 1, wc, kStatusTimeoutMma, &abort_flag)) {
+            if (tid == 0) mma_bar_pending = nullptr;
+            tc_fence_after();
+            uint32_t s0[32], s1[32];
+            const uint32_t taddr = tmem + lane_off + slot * 64;
+            tmem_ld32(taddr, s0);
+            tmem_ld32(taddr + 32, s1);
+            tmem_ld_wait();
+            const int h = (unit < units ? unit : 0) % heads;
+            const float *bp = bias_s + h * T::kNBPad + bias_base;
+            float x[T::kN];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < T::kN; ++j) {
+                constexpr int kSide = 2 * M - 1;
+                const int kterm = (j / M) * kSide + (j % M);
+                const float s = __uint_as_float(j < 32 ? s0[j & 31] : s1[j & 31]);
+                x[j] = fmaf(s, scale_log2e, bp[-kterm]);
+                mx = fmaxf(mx, x[j]);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < T::kN; ++j) {
+                x[j] = ex2_approx(x[j] - mx);
+                sum += x[j];
+            }
+            l = sum;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j0 = c * 8 + 2 * e;
+                    const float a = (row_ok && j0 < T::kN) ? x[j0 < T::kN ? j0 : 0] : 0.f;
+                    const float b = (row_ok && j0 + 1 < T::kN) ? x[j0 + 1 < T::kN ? j0 + 1 : 0] : 0.f;
+                    w[e] = pack_bf16x2(a, b);
+                }
+                st_shared_v4(prow + ((c ^ (tid & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+        }
+        if (tid == 0) bulk_wait_read_all();  // the staging buffer is free again
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // ---- thread 0: O = P V
+        if (tid == 0 && !abort_flag) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint64_t a = smem_desc(
+                    smem_u32(p_base) + (kk >> 2) * T::kPBlockBytes + (kk & 3) * 32, 16, 1024,
+                    kSwizzle128B);
+                const uint64_t b = smem_desc(
+                    smem_u32(sb + 2 * T::kOperBytes) + kk * 16 * T::kRowBytes, 16, T::kSbo, T::kSwz);
+                mma_bf16_ss(tmem, a, b, kIdescO, kk > 0 ? 1u : 0u);
+            }
+            mma_commit(&bar_o);
+            mma_bar_pending = &bar_o;
+            mma_parity_pending = it & 1;
+        }
+
+        // ---- every thread: normalise its row and stage it for the TMA store
+        if (mbar_wait(&bar_o, it & 1, wc, kStatusTimeoutMma, &abort_flag)) {
+            if (tid == 0) mma_bar_pending = nullptr;
+            tc_fence_after();
+            const float inv = row_ok ? 1.f / l : 0.f;
+            const uint32_t orow = smem_u32(o_stage) + tid * T::kRowBytes;
+#pragma unroll
+            for (int half = 0; half < D / 32; ++half) {
+                uint32_t o[32];
+                tmem_ld32(tmem + lane_off + half * 32, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int chunk = half * 4 + c;
+                    const int phys = (D == 32) ? (chunk ^ ((tid >> 1) & 3)) : (chunk ^ (tid & 7));
+                    st_shared_v4(orow + (phys << 4),
+                                 pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv,
+                                             __uint_as_float(o[8 * c + 1]) * inv),
+                                 pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv,
+                                             __uint_as_float(o[8 * c + 3]) * inv),
+                                 pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv,
+                                             __uint_as_float(o[8 * c + 5]) * inv),
+                                 pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv,
+                                             __uint_as_float(o[8 * c + 7]) * inv));
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        const int aborted = __syncthreads_or(abort_flag);
+        if (aborted) break;
+        if (tid == 0) {
+            tma_store_3d(&tm_o, o_stage, 0, 0, 2 * tile);
+            bulk_commit_group();
+        }
+    }
+
+    // ---- drain: nothing of this CTA may be in flight when it exits
+    if (tid == 0) {
+        for (int s = 0; s < 2; ++s)
+            if (loads_pending & (1u << s))
+                mbar_wait(&bar_load[s], load_uses[s] & 1, drain, kStatusTimeoutDrain, nullptr);
+        if (mma_bar_pending != nullptr)
+            mbar_wait(mma_bar_pending, mma_parity_pending, drain, kStatusTimeoutDrain, nullptr);
+        bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+    }
+}
+
+template <int M, int D>
+cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
+    using T = SwinTile<M, D>;
+    if (a.heads > T::kMaxHeads) return cudaErrorInvalidValue;
+    const int units = a.num_windows * a.heads;
+    const int tiles = (units + 1) / 2;
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(T::kN),
+                              static_cast<uint64_t>(units)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(T::kN) * D * 2};
+    const uint32_t box[3] = {static_cast<uint32_t>(D), 64, 2};
+    const CUtensorMapSwizzle swz =
+        (D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box, swz) ||
+        !encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box, swz) ||
+        !encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box, swz) ||
+        !encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, swz))
+        return cudaErrorInvalidValue;
+    const int smem = T::smem_bytes(a.heads);
+    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           T::smem_bytes(T::kMaxHeads));
+    if (err != cudaSuccess) return err;
+    unsigned *status = device_status_word();
+    if (status == nullptr) return cudaErrorMemoryAllocation;
+    const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
+    const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
+    swin_bf16_kernel<M, D><<<grid, 128, smem, stream>>>(
+        tq, tk, tv, to, a.bias_table, a.heads, units, tiles, scale_log2e,
+        WaitCtl{status, kDefaultWaitNs});
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream) {
+    if (a.M == 7 && a.d == 32) return launch_swin_tmpl<7, 32>(a, stream);
+    if (a.M == 7 && a.d == 64) return launch_swin_tmpl<7, 64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace vta

@@ -1,0 +1,64 @@
+// vta_internal.h -- host-side declarations shared by the .cu files of the
+// library (launchers, tensor maps and the device status word). Not part of
+// the C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace vta {
+
+struct WaitCtl;
+
+// Device status word of the current device (allocated on first use; NULL if
+// that failed) and the default bound on in-kernel waits.
+unsigned *device_status_word();
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point.
+// dims / strides are innermost-first; strides_bytes has rank-1 entries.
+bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *base,
+                       const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                       CUtensorMapSwizzle swizzle);
+
+// ---- launchers (each returns the cudaError_t of its launch) ----
+
+cudaError_t launch_build_bucket_lut(int H, int W, double alpha, double beta, double gamma,
+                                    int32_t *lut, int32_t *ids, cudaStream_t stream);
+
+struct F32AttnArgs {
+    const float *q, *k, *v;
+    float *out;
+    int slices, heads, N, d, H, W;
+    const int32_t *lut;  // offset -> bucket; NULL: the bucket is the offset index
+    int num_buckets;
+    const float *tab_k, *tab_q, *tab_v;  // [num_buckets, d] or NULL
+    const float *bias;                   // [num_buckets, heads] or NULL
+    float scale;
+};
+cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
+
+struct SwinBf16Args {
+    const void *q, *k, *v;
+    void *out;
+    const float *bias_table;
+    int num_windows, heads, M, d;
+};
+cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream);
+
+struct RpeBf16Args {
+    const void *q, *k, *v, *tab_q, *tab_k, *tab_v;
+    void *out;
+    const int32_t *lut;
+    int num_buckets, B, heads, H, W, d;
+    unsigned terms;
+};
+cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
+
+}  // namespace vta
