@@ -96,8 +96,8 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                heads; NULL for a term whose bit is not set in `terms` (a
  *                table whose bit is off is not read).
  * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids (or
- *                any table of ids in [0, num_buckets) indexed the same way;
- *                an id outside that range gives undefined output).
+ *                any table of ids indexed the same way; an id outside
+ *                [0, num_buckets) is clamped into that range).
  * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention).
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);

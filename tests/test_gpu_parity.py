@@ -130,3 +130,94 @@ def test_wait_probe_times_out_and_reports():
     inp, out = _swin_case(2, 3, 32, "bf16")
     ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7)
     assert _maxerr(out, ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------------ iRPE, bf16 tensor-core path
+
+def _irpe_run(B, heads, H, W, flags, table_std=0.02, seed=0, inp=None):
+    nb = 49
+    if inp is None:
+        inp = workloads.irpe_inputs(B, heads, H * W, 64, nb, flags, "bf16", table_std, seed)
+    g = _dev(inp)
+    lut, _, nb_dev = api.rpe_build_bucket_ids(H, W, *R19)
+    assert nb_dev == nb
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    return inp, out
+
+
+def _irpe_ref(inp, H, W, flags, slices=None, rows=None):
+    return oracle.irpe_attention(inp["q"], inp["k"], inp["v"], H, W, *R19, flags,
+                                 tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"],
+                                 slices=slices, rows=rows)
+
+
+ALL_TERMS = [0, FLAG_K, FLAG_Q, FLAG_V, FLAG_K | FLAG_Q, FLAG_K | FLAG_V, FLAG_Q | FLAG_V,
+             FLAG_Q | FLAG_K | FLAG_V]
+
+
+@pytest.mark.parametrize("flags", ALL_TERMS)
+@pytest.mark.parametrize("table_std", [0.02, 1.0])
+def test_irpe_bf16_terms_deit_grid(flags, table_std):
+    # 14x14: two query tiles (128 + 68 rows) and two key tiles (128 + 68 keys)
+    inp, out = _irpe_run(2, 3, 14, 14, flags, table_std, seed=flags)
+    assert _maxerr(out, _irpe_ref(inp, 14, 14, flags)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("H,W,flags", [(4, 5, FLAG_K), (1, 1, FLAG_K), (3, 43, FLAG_Q | FLAG_K | FLAG_V),
+                                       (16, 16, FLAG_K), (20, 13, FLAG_K | FLAG_V),
+                                       (7, 64, FLAG_Q | FLAG_K)])
+def test_irpe_bf16_ragged_grids(H, W, flags):
+    inp, out = _irpe_run(1, 5, H, W, flags, table_std=1.0, seed=H * W)
+    assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
+
+
+def test_irpe_bf16_online_rescale_path():
+    # keys of the later tiles get far larger logits than the first tile's, so the
+    # running max jumps by more than 2^8 and the accumulator must be rescaled
+    H, W, flags = 20, 20, FLAG_K | FLAG_V
+    inp = workloads.irpe_inputs(1, 2, H * W, 64, 49, flags, "bf16", 1.0, seed=5)
+    k = inp["k"].float()
+    k[:, :, 128:256] *= 6.0
+    k[:, :, 256:] *= 12.0
+    inp["k"] = k.to(torch.bfloat16)
+    _, out = _irpe_run(1, 2, H, W, flags, inp=inp)
+    assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
+
+
+@pytest.mark.parametrize("name", ["irpe_k_deit_s", "irpe_qkv_deit_s"])
+def test_irpe_bf16_deit_s_configs_sampled(name):
+    cfg = CONFIGS[name]
+    inp, out = _irpe_run(cfg.B, cfg.heads, cfg.H, cfg.W, cfg.flags)
+    S = cfg.B * cfg.heads
+    rng = np.random.default_rng(1)
+    sl = np.unique(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
+    ref = _irpe_ref(inp, cfg.H, cfg.W, cfg.flags, slices=sl).reshape(S, cfg.N, 64)[sl]
+    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("flags", [FLAG_K, FLAG_Q | FLAG_K | FLAG_V])
+def test_irpe_bf16_56x56_sampled(flags):
+    cfg = CONFIGS["irpe_k_56x56"]
+    inp, out = _irpe_run(cfg.B, cfg.heads, cfg.H, cfg.W, flags)
+    S = cfg.B * cfg.heads
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(1500, 1530),
+                                     np.arange(cfg.N - 40, cfg.N)]))
+    sl = np.array([0, 17, S - 1])
+    ref = _irpe_ref(inp, cfg.H, cfg.W, flags, slices=sl, rows=rows)
+    ref = ref.reshape(S, cfg.N, 64)[sl][:, rows]
+    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_BF16
+    # any size: rows are convex combinations of v (plus the value term when on)
+    if not flags & FLAG_V:
+        v = inp["v"].float().cuda()
+        o = out.float()
+        assert torch.all(o <= v.amax(dim=2, keepdim=True) + TOL_BF16)
+        assert torch.all(o >= v.amin(dim=2, keepdim=True) - TOL_BF16)
+
+
+def test_irpe_bf16_repeat_is_deterministic():
+    inp, out1 = _irpe_run(2, 2, 14, 14, FLAG_Q | FLAG_K | FLAG_V, 1.0)
+    _, out2 = _irpe_run(2, 2, 14, 14, FLAG_Q | FLAG_K | FLAG_V, 1.0, inp=inp)
+    assert torch.equal(out1, out2)

@@ -1,8 +1,600 @@
-// rpe_attn_sm103.cu -- iRPE contextual attention on sm_103a tensor cores.
+// rpe_attn_sm103.cu -- iRPE contextual attention on sm_103a tensor cores
+// (tcgen05 + TMEM + TMA), bf16 in, fp32 accumulate.
+//
+// What it computes ("Rethinking and Improving Relative Position Encoding for
+// Vision Transformer", Method, eqs. 13 and 15-17), per (batch, head) slice:
+//     e_ij  = ( q_i.k_j + [K] q_i.R^K[id] + [Q] k_j.R^Q[id] ) / sqrt(d)
+//     out_i = sum_j softmax_j(e_ij) ( v_j + [V] R^V[id] ),   id = id(i, j)
+// with the contextual terms taken the efficient way of eqs. 26-28: every
+// query is dotted with every bucket vector once (QR = Q R^K^T, a small
+// tensor-core product per query tile), every key likewise (KR = K R^Q^T per
+// key tile), and a score picks its term by bucket id; the value term sums the
+// probabilities per bucket (PB) and multiplies by R^V once per query tile.
+// Bucket ids come from a shared-memory copy of the offset table built by
+// rpe_build_bucket_ids; no n x n bias or id map is read from global memory.
+//
+// Structure (one CTA per SM, persistent over (slice, 128-query tile) items):
+//   warp 4  TMA producer: Q tile, then 128-key K/V tiles into a ring.
+//   warp 5  MMA issuer:   QR = Q R^K^T, S = Q K^T (+ KR = K R^Q^T) into one of
+//                         two TMEM score buffers, O += P V, O += PB R^V.
+//   warps 0-3 softmax:    one thread per query row. Reads its score row from
+//                         TMEM, adds the gathered terms, keeps a running max
+//                         and sum (online softmax over key tiles; the O
+//                         accumulator is rescaled only when the max grows by
+//                         more than 2^8, otherwise the stale max is kept),
+//                         writes bf16 probabilities as the K-major A operand
+//                         of P V, then normalises O and stores it.
+// Hand-offs use mbarriers; every wait is bounded (see sm103_ptx.cuh).
 #include "vta_internal.h"
+#include "sm103_ptx.cuh"
+
+#include <algorithm>
+#include <cmath>
 
 namespace vta {
+namespace {
 
-cudaError_t launch_rpe_bf16(const RpeBf16Args &, cudaStream_t) { return cudaErrorNotSupported; }
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kD = 64;           // head dim (bytes per row: 128)
+constexpr int kBM = 128;         // query rows per tile
+constexpr int kBN = 128;         // keys per tile
+constexpr int kTileBytes = 128 * 128;  // one 128-row bf16 tile of q / k / v
+constexpr int kKRStride = 65;    // floats per key row of KR in shared memory (odd)
+constexpr float kRescaleLog2 = 8.f;    // keep a stale max while the new one is within 2^8
+
+// TMEM column map (512 columns allocated: the CTA owns the whole SM)
+constexpr uint32_t kColS = 0;     // two 128-column score buffers
+constexpr uint32_t kColO = 256;   // 64 columns, output accumulator
+constexpr uint32_t kColQR = 320;  // 64 columns, Q R^K^T
+constexpr uint32_t kColKR = 384;  // two 64-column buffers, K R^Q^T
+
+constexpr int kThreads = 192;
+
+struct RpeParams {
+    int N, H, W, nb, nkt, qtiles, items, nst;
+    uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
+        off_lut;
+    int lut_len;
+    const int32_t *lut;
+    __nv_bfloat16 *out;
+    float c;  // log2(e) / sqrt(d)
+    WaitCtl wc;
+};
+
+struct Bars {
+    uint64_t tab_full, q_full, q_empty, qr_full, qr_empty, o_full, o_empty, p_full, p_empty;
+    uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
+};
+
+__device__ __forceinline__ bool bar_red_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void softmax_bar() { named_bar_sync(1, 128); }
+
+template <bool HK, bool HQ, bool HV>
+__global__ void __launch_bounds__(kThreads, 1)
+    rpe_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_rk,
+                    const __grid_constant__ CUtensorMap tm_rq,
+                    const __grid_constant__ CUtensorMap tm_rv, const RpeParams P) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ Bars bars;
+    __shared__ uint32_t tmem_base_s;
+    __shared__ volatile int abort_flag;
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const WaitCtl &wc = P.wc;
+    const WaitCtl drain{wc.status, kDefaultWaitNs};
+
+    uint8_t *sQ = smem + P.off_q;
+    uint8_t *sKV = smem + P.off_kv;  // stage s: K at s*2*kTileBytes, V after it
+    uint8_t *sP = smem + P.off_p;
+    float *sQR = reinterpret_cast<float *>(smem + P.off_qr);
+    float *sKR = reinterpret_cast<float *>(smem + P.off_kr);
+    float *sPB = reinterpret_cast<float *>(smem + P.off_pb);
+    int *sKterm = reinterpret_cast<int *>(smem + P.off_kterm);
+    uint8_t *sLut = smem + P.off_lut;
+
+    if (tid == 0) {
+        mbar_init(&bars.tab_full, 1);
+        mbar_init(&bars.q_full, 1);
+        mbar_init(&bars.q_empty, 1);
+        mbar_init(&bars.qr_full, 1);
+        mbar_init(&bars.qr_empty, 128);
+        mbar_init(&bars.o_full, 1);
+        mbar_init(&bars.o_empty, 128);
+        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.p_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.kv_full[i], 1);
+            mbar_init(&bars.kv_empty[i], 1);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.s_empty[i], 128);
+        }
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_base_s, 512);
+    // bucket-id table: int32 in global -> uint8 in shared memory
+    // (ids are clamped into [0, nb) so a bad table can never index past shared memory)
+    for (int e = tid; e < P.lut_len; e += kThreads) {
+        const int id = __ldg(P.lut + e);
+        sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            uint32_t tab_bytes = 0;
+            if (HK) tab_bytes += kTileBytes / 2;
+            if (HQ) tab_bytes += kTileBytes / 2;
+            if (HV) tab_bytes += kTileBytes / 2;
+            if (tab_bytes) {
+                mbar_arrive_expect_tx(&bars.tab_full, tab_bytes);
+                if (HK) tma_load_2d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0);
+                if (HQ) tma_load_2d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0);
+                if (HV) tma_load_2d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0);
+            }
+            int g = 0, w = 0;
+            int last_kv_use[2] = {-1, -1};
+            int last_q = -1;
+            for (int item = blockIdx.x; item < P.items; item += gridDim.x, ++w) {
+                const int slice = item / P.qtiles, qt = item % P.qtiles;
+                if (!mbar_wait(&bars.q_empty, (w & 1) ^ 1, wc, kStatusTimeoutSync, &abort_flag)) break;
+                mbar_arrive_expect_tx(&bars.q_full, kTileBytes);
+                tma_load_3d(sQ, &tm_q, &bars.q_full, 0, qt * kBM, slice);
+                last_q = w;
+                bool ok = true;
+                for (int kt = 0; kt < P.nkt; ++kt, ++g) {
+                    const int st = g % P.nst, use = g / P.nst;
+                    if (!mbar_wait(&bars.kv_empty[st], (use & 1) ^ 1, wc, kStatusTimeoutSync,
+                                   &abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *kb = sKV + st * 2 * kTileBytes;
+                    mbar_arrive_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
+                    tma_load_3d(kb, &tm_k, &bars.kv_full[st], 0, kt * kBN, slice);
+                    tma_load_3d(kb + kTileBytes, &tm_v, &bars.kv_full[st], 0, kt * kBN, slice);
+                    last_kv_use[st] = use;
+                }
+                if (!ok) break;
+            }
+            // drain: the most recent load on every barrier has landed
+            if (tab_bytes) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+            if (last_q >= 0) mbar_wait(&bars.q_full, last_q & 1, drain, kStatusTimeoutDrain, nullptr);
+            for (int st = 0; st < 2; ++st)
+                if (last_kv_use[st] >= 0)
+                    mbar_wait(&bars.kv_full[st], last_kv_use[st] & 1, drain, kStatusTimeoutDrain,
+                              nullptr);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t kIdT = idesc_bf16(128, 64, false, false);   // Q R^K^T, K R^Q^T
+            constexpr uint32_t kIdO = idesc_bf16(128, 64, false, true);    // P V, PB R^V
+            const uint32_t aQ = smem_u32(sQ);
+            uint64_t *last_bar = nullptr;
+            uint32_t last_par = 0;
+            auto commit = [&](uint64_t *bar, uint32_t parity) {
+                mma_commit(bar);
+                last_bar = bar;
+                last_par = parity;
+            };
+            bool ok = true;
+            if (HK || HQ || HV) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+            int g = 0, w = 0, pr = 0;
+            for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++w) {
+                if (!(ok = mbar_wait(&bars.q_full, w & 1, wc, kStatusTimeoutLoad, &abort_flag))) break;
+                tc_fence_after();
+                if (HK) {
+                    if (!(ok = mbar_wait(&bars.qr_empty, (w & 1) ^ 1, wc, kStatusTimeoutSync,
+                                         &abort_flag)))
+                        break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + kColQR, smem_desc(aQ + kk * 32, 16, 1024, kSwizzle128B),
+                                    smem_desc(smem_u32(smem + P.off_rk) + kk * 32, 16, 1024,
+                                              kSwizzle128B),
+                                    kIdT, kk > 0);
+                    commit(&bars.qr_full, w & 1);
+                }
+                // S for key tile g (and KR with it); returns false on abort
+                auto issue_s = [&](int gg, int kt) -> bool {
+                    const int st = gg % P.nst, b = gg & 1;
+                    if (!mbar_wait(&bars.kv_full[st], (gg / P.nst) & 1, wc, kStatusTimeoutLoad,
+                                   &abort_flag))
+                        return false;
+                    if (!mbar_wait(&bars.s_empty[b], ((gg >> 1) & 1) ^ 1, wc, kStatusTimeoutSync,
+                                   &abort_flag))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t aK = smem_u32(sKV + st * 2 * kTileBytes);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + kColS + b * 128,
+                                    smem_desc(aQ + kk * 32, 16, 1024, kSwizzle128B),
+                                    smem_desc(aK + kk * 32, 16, 1024, kSwizzle128B), kIdS, kk > 0);
+                    if (HQ)
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(tmem + kColKR + b * 64,
+                                        smem_desc(aK + kk * 32, 16, 1024, kSwizzle128B),
+                                        smem_desc(smem_u32(smem + P.off_rq) + kk * 32, 16, 1024,
+                                                  kSwizzle128B),
+                                        kIdT, kk > 0);
+                    commit(&bars.s_full[b], (gg >> 1) & 1);
+                    if (kt == P.nkt - 1) commit(&bars.q_empty, w & 1);
+                    return true;
+                };
+                if (!(ok = issue_s(g, 0))) break;
+                for (int kt = 0; kt < P.nkt; ++kt, ++g) {
+                    if (kt + 1 < P.nkt && !(ok = issue_s(g + 1, kt + 1))) break;
+                    if (kt == 0 && !(ok = mbar_wait(&bars.o_empty, (w & 1) ^ 1, wc,
+                                                    kStatusTimeoutSync, &abort_flag)))
+                        break;
+                    if (!(ok = mbar_wait(&bars.p_full, pr & 1, wc, kStatusTimeoutSync, &abort_flag)))
+                        break;
+                    ++pr;
+                    tc_fence_after();
+                    const int st = g % P.nst;
+                    const uint32_t aV = smem_u32(sKV + st * 2 * kTileBytes + kTileBytes);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_ss(tmem + kColO,
+                                    smem_desc(smem_u32(sP) + (kk >> 2) * kTileBytes + (kk & 3) * 32,
+                                              16, 1024, kSwizzle128B),
+                                    smem_desc(aV + kk * 2048, 16, 1024, kSwizzle128B), kIdO,
+                                    (kt > 0 || kk > 0) ? 1u : 0u);
+                    commit(&bars.p_empty, (pr - 1) & 1);
+                    commit(&bars.kv_empty[st], (g / P.nst) & 1);
+                }
+                if (!ok) break;
+                if (HV) {
+                    if (!(ok = mbar_wait(&bars.p_full, pr & 1, wc, kStatusTimeoutSync, &abort_flag)))
+                        break;
+                    ++pr;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(tmem + kColO,
+                                    smem_desc(smem_u32(sP) + kk * 32, 16, 1024, kSwizzle128B),
+                                    smem_desc(smem_u32(smem + P.off_rv) + kk * 2048, 16, 1024,
+                                              kSwizzle128B),
+                                    kIdO, 1u);
+                    commit(&bars.p_empty, (pr - 1) & 1);
+                }
+                commit(&bars.o_full, w & 1);
+            }
+            // drain: tcgen05 work completes in order, so the last commit covers it all
+            if (last_bar != nullptr) mbar_wait(last_bar, last_par, drain, kStatusTimeoutDrain, nullptr);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax warps 0-3
+        const int t = tid;  // query row within the tile == TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const int cols = 2 * P.W - 1;
+        float *qr_t = sQR + t;
+        float *pb_t = sPB + t;
+        const uint32_t prow = smem_u32(sP) + t * 128;
+        int g = 0, w = 0, pw = 0;
+        for (int item = blockIdx.x; item < P.items; item += gridDim.x, ++w) {
+            const int slice = item / P.qtiles, qt = item % P.qtiles;
+            const int i = qt * kBM + t;
+            const int ic = i < P.N ? i : P.N - 1;
+            const int base_i = (ic / P.W) * cols + (ic % P.W) + (P.H - 1) * cols + (P.W - 1);
+            const uint8_t *lut_i = sLut + base_i;
+            if (HK) {
+                bool ok = __all_sync(~0u, mbar_wait(&bars.qr_full, w & 1, wc, kStatusTimeoutMma,
+                                                    &abort_flag));
+                if (!bar_red_and(ok)) break;
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(tmem + lane_off + kColQR, r0);
+                tmem_ld32(tmem + lane_off + kColQR + 32, r1);
+                tmem_ld_wait();
+#pragma unroll
+                for (int b = 0; b < 64; ++b)
+                    if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
+                tc_fence_before();
+                mbar_arrive(&bars.qr_empty);
+            }
+            if (HV)
+                for (int b = 0; b < P.nb; ++b) pb_t[b * 128] = 0.f;
+            float m = -INFINITY, l = 0.f;
+            bool aborted = false;
+            for (int kt = 0; kt < P.nkt; ++kt, ++g) {
+                const int b = g & 1;
+                bool ok = __all_sync(~0u, mbar_wait(&bars.s_full[b], (g >> 1) & 1, wc,
+                                                    kStatusTimeoutMma, &abort_flag));
+                if (!bar_red_and(ok)) {  // also: everyone is done with the previous tile
+                    aborted = true;
+                    break;
+                }
+                tc_fence_after();
+                const int kbase = kt * kBN;
+                {
+                    const int j = kbase + t < P.N ? kbase + t : P.N - 1;  // clamp padding keys
+                    sKterm[t] = (j / P.W) * cols + (j % P.W);
+                }
+                if (HQ) {
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tmem + lane_off + kColKR + b * 64, r0);
+                    tmem_ld32(tmem + lane_off + kColKR + b * 64 + 32, r1);
+                    tmem_ld_wait();
+                    float *kr = sKR + t * kKRStride;
+#pragma unroll
+                    for (int bb = 0; bb < 64; ++bb)
+                        if (bb < P.nb) kr[bb] = __uint_as_float(bb < 32 ? r0[bb & 31] : r1[bb & 31]) * P.c;
+                }
+                softmax_bar();
+                uint32_t s[128];
+                {
+                    uint32_t *s0 = s, *s1 = s + 32, *s2 = s + 64, *s3 = s + 96;
+                    tmem_ld32(tmem + lane_off + kColS + b * 128, *reinterpret_cast<uint32_t(*)[32]>(s0));
+                    tmem_ld32(tmem + lane_off + kColS + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(s1));
+                    tmem_ld32(tmem + lane_off + kColS + b * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(s2));
+                    tmem_ld32(tmem + lane_off + kColS + b * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(s3));
+                    tmem_ld_wait();
+                }
+                tc_fence_before();
+                mbar_arrive(&bars.s_empty[b]);  // S[b] and KR[b] are read
+
+                // pass 1: logits in log2 units, running max
+                const int nvalid = min(kBN, P.N - kbase);
+                const int4 *kt4 = reinterpret_cast<const int4 *>(sKterm);
+                float mloc = -INFINITY;
+#pragma unroll
+                for (int q4 = 0; q4 < 32; ++q4) {
+                    const int4 kv = kt4[q4];
+                    const int kts[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int jj = q4 * 4 + e;
+                        float x = __uint_as_float(s[jj]) * P.c;
+                        if (HK || HQ || HV) {
+                            const int id = lut_i[-kts[e]];
+                            if (HK) x += qr_t[id * 128];
+                            if (HQ) x += sKR[jj * kKRStride + id];
+                        }
+                        x = (jj < nvalid) ? x : -INFINITY;
+                        s[jj] = __float_as_uint(x);
+                        mloc = fmaxf(mloc, x);
+                    }
+                }
+                // lazy rescale: move the reference max only when it grows by > 2^8
+                float alpha = 1.f;
+                if (mloc > m + kRescaleLog2) {
+                    alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mloc);
+                    m = mloc;
+                    l *= alpha;
+                    if (HV)
+                        for (int bb = 0; bb < P.nb; ++bb) pb_t[bb * 128] *= alpha;
+                }
+                // P buffer free (the previous P V is done) -> rescale O if needed
+                ok = __all_sync(~0u, mbar_wait(&bars.p_empty, (pw & 1) ^ 1, wc, kStatusTimeoutMma,
+                                               &abort_flag));
+                ++pw;
+                if (!ok) {
+                    aborted = true;
+                    continue;  // the next tile's reduction breaks out uniformly
+                }
+                tc_fence_after();
+                if (kt > 0 && __any_sync(~0u, alpha < 1.f)) {
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(tmem + lane_off + kColO, o0);
+                    tmem_ld32(tmem + lane_off + kColO + 32, o1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        o0[c] = __float_as_uint(__uint_as_float(o0[c]) * alpha);
+                        o1[c] = __float_as_uint(__uint_as_float(o1[c]) * alpha);
+                    }
+                    tmem_st32(tmem + lane_off + kColO, o0);
+                    tmem_st32(tmem + lane_off + kColO + 32, o1);
+                    tmem_st_wait();
+                }
+                // pass 2: probabilities -> P (bf16, K-major, 128B swizzle), row sum, PB
+                float sum = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 16; ++ch) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int j0 = ch * 8 + 2 * e;
+                        const float p0 = ex2_approx(__uint_as_float(s[j0]) - m);
+                        const float p1 = ex2_approx(__uint_as_float(s[j0 + 1]) - m);
+                        sum += p0 + p1;
+                        if (HV) {
+                            if (j0 < nvalid) pb_t[static_cast<int>(lut_i[-sKterm[j0]]) * 128] += p0;
+                            if (j0 + 1 < nvalid)
+                                pb_t[static_cast<int>(lut_i[-sKterm[j0 + 1]]) * 128] += p1;
+                        }
+                        wv[e] = pack_bf16x2(p0, p1);
+                    }
+                    const int blk = ch >> 3, c = ch & 7;
+                    st_shared_v4(prow + blk * kTileBytes + ((c ^ (t & 7)) << 4), wv[0], wv[1],
+                                 wv[2], wv[3]);
+                }
+                l += sum;
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars.p_full);
+            }
+            if (!bar_red_and(!aborted)) break;  // uniform across the four softmax warps
+            if (HV) {
+                // PB (bf16, buckets >= nb zero) into P's first block for O += PB R^V
+                bool ok = __all_sync(~0u, mbar_wait(&bars.p_empty, (pw & 1) ^ 1, wc,
+                                                    kStatusTimeoutMma, &abort_flag));
+                ++pw;
+                if (!bar_red_and(ok)) break;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint32_t wv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int b0 = c * 8 + 2 * e;
+                        const float v0 = b0 < P.nb ? pb_t[b0 * 128] : 0.f;
+                        const float v1 = b0 + 1 < P.nb ? pb_t[(b0 + 1) * 128] : 0.f;
+                        wv[e] = pack_bf16x2(v0, v1);
+                    }
+                    st_shared_v4(prow + ((c ^ (t & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(&bars.p_full);
+            }
+            // epilogue: O / l -> bf16 -> global
+            bool ok = __all_sync(~0u, mbar_wait(&bars.o_full, w & 1, wc, kStatusTimeoutMma,
+                                                &abort_flag));
+            if (!bar_red_and(ok)) break;
+            tc_fence_after();
+            uint32_t o0[32], o1[32];
+            tmem_ld32(tmem + lane_off + kColO, o0);
+            tmem_ld32(tmem + lane_off + kColO + 32, o1);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars.o_empty);
+            if (i < P.N) {
+                const float inv = 1.f / l;
+                uint4 *dst = reinterpret_cast<uint4 *>(P.out + (static_cast<size_t>(slice) * P.N + i) * kD);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t *src = c < 4 ? o0 + 8 * c : o1 + 8 * (c - 4);
+                    uint4 v;
+                    v.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
+                    v.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
+                    v.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
+                    v.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
+                    dst[c] = v;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    asm volatile("barrier.sync 0;" ::: "memory");
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
+
+template <bool HK, bool HQ, bool HV>
+cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
+    const int N = a.H * a.W;
+    const int slices = a.B * a.heads;
+    RpeParams p{};
+    p.N = N;
+    p.H = a.H;
+    p.W = a.W;
+    p.nb = a.num_buckets;
+    p.nkt = (N + kBN - 1) / kBN;
+    p.qtiles = (N + kBM - 1) / kBM;
+    p.items = slices * p.qtiles;
+    p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
+    p.lut = a.lut;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
+
+    const uint32_t smem_cap = 227 * 1024 - 1024;  // leave room for the static barriers
+    for (int nst = 2; nst >= 1; --nst) {
+        uint32_t off = 0;
+        p.off_q = off;
+        off += kTileBytes;
+        p.off_kv = off;
+        off += nst * 2 * kTileBytes;
+        p.off_p = off;
+        off += 2 * kTileBytes;
+        p.off_rk = off;
+        if (HK) off += kTileBytes / 2;
+        p.off_rq = off;
+        if (HQ) off += kTileBytes / 2;
+        p.off_rv = off;
+        if (HV) off += kTileBytes / 2;
+        p.off_qr = off;
+        if (HK) off += align_up(p.nb * 512, 1024);
+        p.off_kr = off;
+        if (HQ) off += align_up(128 * kKRStride * 4, 1024);
+        p.off_pb = off;
+        if (HV) off += align_up(p.nb * 512, 1024);
+        p.off_kterm = off;
+        off += 512;
+        p.off_lut = off;
+        off += align_up(p.lut_len, 16);
+        const uint32_t total = 1024 + std::max<uint32_t>(off, 120 * 1024);
+        if (total <= smem_cap) {
+            p.nst = nst;
+            unsigned *status = device_status_word();
+            if (status == nullptr) return cudaErrorMemoryAllocation;
+            p.wc = WaitCtl{status, kDefaultWaitNs};
+            const uint64_t dims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(N),
+                                      static_cast<uint64_t>(slices)};
+            const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(N) * kD * 2};
+            const uint32_t box[3] = {kD, 128, 1};
+            const uint64_t tdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(a.num_buckets)};
+            const uint64_t tstrides[1] = {kD * 2};
+            const uint32_t tbox[2] = {kD, 64};
+            CUtensorMap tq, tk, tv, trk, trq, trv;
+            const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+            const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+            if (!encode_tensor_map(&tq, bf, 3, a.q, dims, strides, box, sw) ||
+                !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box, sw) ||
+                !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box, sw))
+                return cudaErrorInvalidValue;
+            // tables not in use get a valid (never read) map over q
+            const void *rk = HK ? a.tab_k : a.q, *rq = HQ ? a.tab_q : a.q, *rv = HV ? a.tab_v : a.q;
+            if (!encode_tensor_map(&trk, bf, 2, rk, tdims, tstrides, tbox, sw) ||
+                !encode_tensor_map(&trq, bf, 2, rq, tdims, tstrides, tbox, sw) ||
+                !encode_tensor_map(&trv, bf, 2, rv, tdims, tstrides, tbox, sw))
+                return cudaErrorInvalidValue;
+            cudaError_t err = cudaFuncSetAttribute(rpe_bf16_kernel<HK, HQ, HV>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(total));
+            if (err != cudaSuccess) return err;
+            const int grid = std::min(p.items, sm_count());
+            rpe_bf16_kernel<HK, HQ, HV><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, trq, trv, p);
+            return cudaGetLastError();
+        }
+    }
+    return cudaErrorInvalidValue;  // the bucket table does not fit in shared memory
+}
+
+}  // namespace
+
+cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream) {
+    const bool k = a.terms & 1u, q = a.terms & 2u, v = a.terms & 4u;
+    if (!k && !q && !v) return launch_tmpl<false, false, false>(a, stream);
+    if (k && !q && !v) return launch_tmpl<true, false, false>(a, stream);
+    if (!k && q && !v) return launch_tmpl<false, true, false>(a, stream);
+    if (!k && !q && v) return launch_tmpl<false, false, true>(a, stream);
+    if (k && q && !v) return launch_tmpl<true, true, false>(a, stream);
+    if (k && !q && v) return launch_tmpl<true, false, true>(a, stream);
+    if (!k && q && v) return launch_tmpl<false, true, true>(a, stream);
+    return launch_tmpl<true, true, true>(a, stream);
+}
 
 }  // namespace vta
