@@ -251,8 +251,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return true;
                 };
                 if (!(ok = issue_s(g, 0))) break;
+                // With two K/V stages the next tile's S is issued before this tile's
+                // P V, so the tensor core works while the softmax warps do; with one
+                // stage the next tile's load needs this P V to free the stage first.
+                const bool early_s = P.nst > 1;
                 for (int kt = 0; kt < P.nkt; ++kt, ++g) {
-                    if (kt + 1 < P.nkt && !(ok = issue_s(g + 1, kt + 1))) break;
+                    if (early_s && kt + 1 < P.nkt && !(ok = issue_s(g + 1, kt + 1))) break;
                     if (kt == 0 && !(ok = mbar_wait(&bars.o_empty, (w & 1) ^ 1, wc,
                                                     kStatusTimeoutSync, &abort_flag)))
                         break;
@@ -270,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (kt > 0 || kk > 0) ? 1u : 0u);
                     commit(&bars.p_empty, (pr - 1) & 1);
                     commit(&bars.kv_empty[st], (g / P.nst) & 1);
+                    if (!early_s && kt + 1 < P.nkt && !(ok = issue_s(g + 1, kt + 1))) break;
                 }
                 if (!ok) break;
                 if (HV) {
