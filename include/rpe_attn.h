@@ -129,6 +129,38 @@ int swin_window_attn_fwd(const void *q, const void *k, const void *v,
                          int M, int d, int dtype, void *out, void *stream);
 
 /*
+ * swin_window_attn_fwd_noalloc -- swin_window_attn_fwd for callers that must
+ * not allocate device memory. The pages have no counterpart: this is a
+ * library-integration entry point, not part of the method.
+ *
+ * Same arguments, layouts, math and output as swin_window_attn_fwd on its
+ * bf16 path (dtype is implicitly RPE_DTYPE_BF16; M == 7, d in {32, 64},
+ * heads <= 32; anything else returns RPE_ERR_UNSUPPORTED). The difference is
+ * where the kernel's scratch lives. swin_window_attn_fwd allocates a small
+ * status buffer with cudaMalloc on its first call on a device; some callers
+ * cannot allow that (pipelines that forbid allocation once running, processes
+ * whose device memory is reserved up front by a pooling allocator, code that
+ * runs only where allocation is not permitted). This variant instead uses a
+ * fixed file-scope device array of 256 bytes (64 words) that every GPU which
+ * loads the library holds until the process exits; a call needs one word of
+ * it (its status word), whatever the problem size, and a request needing more
+ * than the array holds would return RPE_ERR_UNSUPPORTED. The call itself
+ * performs no cudaMalloc, cudaFree or other allocation.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call clears the status word (an async memset on `stream`) before
+ *     its kernel runs; the array otherwise keeps the last call's contents.
+ *   - All calls share the array, so calls that overlap on the GPU (different
+ *     streams, no ordering between them) race on the status word.
+ *   - A bounded-wait timeout inside this variant sets a bit in its own word,
+ *     not in the word rpe_device_status reads.
+ */
+int swin_window_attn_fwd_noalloc(const void *q, const void *k, const void *v,
+                                 const float *bias_table, int num_windows, int heads,
+                                 int M, int d, void *out, void *stream);
+
+/*
  * rpe_device_status -- synchronises the current device and returns, through
  * *status, the word the kernels set when a bounded wait ran out (0 = none).
  * Clears the word when `clear` is non-zero. Returns RPE_ERR_TIMEOUT if any

@@ -26,6 +26,7 @@ SIGNATURES = {
     "rpe_build_bucket_ids": (_i, [_i, _i, _i, _d, _d, _d, _p, _p, ctypes.POINTER(_i), _p]),
     "rpe_attn_fwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _u, _i, _p, _p]),
     "swin_window_attn_fwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
+    "swin_window_attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p]),
     "rpe_device_status": (_i, [ctypes.POINTER(_u), _i]),
     "rpe_wait_probe": (_i, [_u64, _p]),
     "rpe_status_string": (ctypes.c_char_p, [_i]),

@@ -24,10 +24,12 @@
 // The kernel is persistent (grid = a multiple of the SM count), double-
 // buffers Q/K/V so the next tile's loads overlap this tile's work, and runs
 // two CTAs per SM at d = 32 so one CTA's softmax overlaps the other's copies.
+#include "rpe_attn.h"
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
 
 #include <cmath>
+#include <mutex>
 
 namespace vta {
 namespace {
@@ -326,3 +328,114 @@ cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream) {
 }
 
 }  // namespace vta
+
+// ---------------------------------------------------------------------------
+// swin_window_attn_fwd_noalloc: the same bf16 Swin kernel for callers that
+// must not allocate device memory.
+//
+// The regular entry point keeps its kernels' status word (the only scratch
+// the kernel writes besides its output) in a 256-byte buffer that the library
+// allocates with cudaMalloc on the first call on each device. Some callers
+// cannot allow that allocation: code that must not call cudaMalloc once it is
+// running (real-time or certified pipelines, processes whose memory is fully
+// reserved up front by a pooling allocator or a framework), and code that
+// only ever runs inside a region where allocation is forbidden. This variant
+// keeps that scratch in a fixed, file-scope device array instead, so a call
+// allocates nothing.
+// ---------------------------------------------------------------------------
+namespace vta {
+namespace {
+
+// Scratch of the no-allocation variant: kNoAllocWords 32-bit words (256 bytes)
+// of device memory that every GPU loading this library holds until the
+// process exits. A call uses word 0 as its kernel's status word.
+constexpr int kNoAllocWords = 64;
+constexpr int kNoAllocWordsPerCall = 1;
+static __device__ __align__(256) unsigned g_swin_noalloc_scratch[kNoAllocWords];
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device. In host code the
+// array's name is only a host-side stand-in, so its device address is looked
+// up once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(unsigned **out) {
+    int dev = -1;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        err = cudaGetSymbolAddress(&ptr, g_swin_noalloc_scratch);
+        if (err != cudaSuccess) return err;
+        g_noalloc_ptr[dev] = static_cast<unsigned *>(ptr);
+    }
+    *out = g_noalloc_ptr[dev];
+    return cudaSuccess;
+}
+
+template <int M, int D>
+cudaError_t launch_swin_noalloc_tmpl(const SwinBf16Args &a, unsigned *status,
+                                     cudaStream_t stream) {
+    using T = SwinTile<M, D>;
+    if (a.heads > T::kMaxHeads) return cudaErrorInvalidValue;
+    const int units = a.num_windows * a.heads;
+    const int tiles = (units + 1) / 2;
+    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(T::kN),
+                              static_cast<uint64_t>(units)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(T::kN) * D * 2};
+    const uint32_t box[3] = {static_cast<uint32_t>(D), 64, 2};
+    const CUtensorMapSwizzle swz =
+        (D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box, swz) ||
+        !encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box, swz) ||
+        !encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box, swz) ||
+        !encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, swz))
+        return cudaErrorInvalidValue;
+    const int smem = T::smem_bytes(a.heads);
+    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           T::smem_bytes(T::kMaxHeads));
+    if (err != cudaSuccess) return err;
+    // the array keeps the previous call's contents: the status word starts at zero
+    err = cudaMemsetAsync(status, 0, kNoAllocWordsPerCall * sizeof(unsigned), stream);
+    if (err != cudaSuccess) return err;
+    const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
+    const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
+    swin_bf16_kernel<M, D><<<grid, 128, smem, stream>>>(tq, tk, tv, to, a.bias_table, a.heads,
+                                                        units, tiles, scale_log2e,
+                                                        WaitCtl{status, kDefaultWaitNs});
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace vta
+
+extern "C" int swin_window_attn_fwd_noalloc(const void *q, const void *k, const void *v,
+                                            const float *bias_table, int num_windows,
+                                            int heads, int M, int d, void *out,
+                                            void *stream) {
+    using namespace vta;
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bias_table == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (num_windows < 1 || heads < 1 || M < 1 || d < 1) return RPE_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, out, bias_table};
+    for (const void *p : ptrs)
+        if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RPE_ERR_INVALID_ARG;
+    const long long units = static_cast<long long>(num_windows) * heads;
+    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30))
+        return RPE_ERR_UNSUPPORTED;
+    // every call needs kNoAllocWordsPerCall words of the fixed array, whatever its shape
+    if (kNoAllocWordsPerCall > kNoAllocWords) return RPE_ERR_UNSUPPORTED;
+    unsigned *status = nullptr;
+    if (noalloc_scratch(&status) != cudaSuccess) return RPE_ERR_CUDA;
+    SwinBf16Args a{q, k, v, out, bias_table, num_windows, heads, M, d};
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t err = (d == 32) ? launch_swin_noalloc_tmpl<7, 32>(a, status, st)
+                                : launch_swin_noalloc_tmpl<7, 64>(a, status, st);
+    return err == cudaSuccess ? RPE_OK : RPE_ERR_CUDA;
+}
