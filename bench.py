@@ -59,6 +59,41 @@ def work_of(cfg):
     return flops, nbytes, cfg.B * cfg.N
 
 
+def workload_config(cfg):
+    from vision_transformer_attention_gb300.workloads import SwinConfig
+    if isinstance(cfg, SwinConfig):
+        return {"workload": cfg.name, "num_windows": cfg.num_windows, "heads": cfg.heads,
+                "window": cfg.M, "n": cfg.n, "d": cfg.d}
+    terms = "".join(t for t, f in (("Q", 2), ("K", 1), ("V", 4)) if cfg.flags & f)
+    return {"workload": cfg.name, "B": cfg.B, "heads": cfg.heads, "grid": [cfg.H, cfg.W],
+            "N": cfg.N, "d": cfg.d, "terms": terms or "none", "num_buckets": cfg.num_buckets,
+            "index_fn": {"alpha": cfg.ratio, "beta": 2 * cfg.ratio, "gamma": 8 * cfg.ratio}}
+
+
+# The kernel that dominates each workload's step, the roofline that bounds it,
+# and its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum
+# from an ncu capture of the kernel as it stands; None when not measured).
+DOMINANT = {
+    "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", None),
+    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,K>", "hbm", None),
+    "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", None),
+    "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", None),
+}
+
+
+def roofline_of(cfg, flops, nbytes, per_step_s, peaks, peak_src):
+    kernel, bound, traffic = DOMINANT.get(cfg.name, ("?", "hbm", None))
+    if bound == "tensor":
+        achieved = flops / per_step_s / 1e12
+        peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved = nbytes / per_step_s / 1e9
+        peak, unit = peaks["hbm_gbs"], "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+            "frac": achieved / peak, "traffic": traffic, "peak_source": peak_src,
+            "kernel": kernel, "alg_bytes_per_launch": nbytes, "alg_flops_per_launch": flops}
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -299,7 +334,7 @@ def gpu_arm(args):
         return float(t.item())
 
     peaks, peak_src = load_peaks()
-    cfg = workloads.CONFIGS[HEADLINE]
+    cfg = workloads.CONFIGS[args.workload]
     flops, nbytes, tokens = work_of(cfg)
     sets = device_sets(cfg, dev, nbytes)
     step = make_step(cfg, sets)
@@ -315,7 +350,6 @@ def gpu_arm(args):
     clocks = clk.summary()
     per_step_s = ms / 1e3 / args.steps
     value = world * tokens / per_step_s
-    achieved_gbs = nbytes / per_step_s / 1e9
     achieved_tflops = flops / per_step_s / 1e12
     del graphs
 
@@ -326,6 +360,8 @@ def gpu_arm(args):
     extra_cfgs = {}
     if not args.headline_only:
         for name in ("swin_t_stage1", "irpe_qkv_deit_s", "irpe_k_56x56"):
+            if name == args.workload:
+                continue
             c = workloads.CONFIGS[name]
             f, b, tk = work_of(c)
             st = make_step(c, device_sets(c, dev, b))
@@ -351,27 +387,23 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step_s * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v, N(0,0.02) R^K; no dataset)",
-        "config": {"workload": HEADLINE, "B": cfg.B, "heads": cfg.heads, "grid": [cfg.H, cfg.W],
-                   "N": cfg.N, "d": cfg.d, "terms": "K", "num_buckets": cfg.num_buckets,
-                   "index_fn": {"alpha": cfg.ratio, "beta": 2 * cfg.ratio, "gamma": 8 * cfg.ratio},
-                   "global_batch": cfg.B * world, "parallelism": f"replicas x{world}",
+        "config": {**workload_config(cfg),
+                   "global_batch": getattr(cfg, "B", getattr(cfg, "num_windows", 0)) * world,
+                   "parallelism": f"replicas x{world}",
                    "l2": f"inputs rotate over {len(sets)} copies ({len(sets) * nbytes / 2**20:.0f} MiB"
                          f" > 3x L2), no flush", "timing": f"CUDA graphs of {args.group} launches"},
         "tflops": achieved_tflops,
         "tc_frac_of_peak": achieved_tflops / peaks["bf16_tflops"],
         "attainable_frac": achieved_tflops / min(peaks["bf16_tflops"],
                                                  flops / nbytes * peaks["hbm_gbs"] / 1e3),
-        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
-                     "traffic": None, "peak_source": peak_src,
-                     "kernel": "rpe_bf16_kernel<K>", "alg_bytes_per_launch": nbytes},
+        "roofline": roofline_of(cfg, flops, nbytes, per_step_s, peaks, peak_src),
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
         "gpu_launches": args.steps,
         "configs_extra": extra_cfgs,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and args.workload == HEADLINE:
         line["cpu_baseline"] = cpu_baseline(cfg, args.cpu_budget)
     print(json.dumps(line), flush=True)
     if dist:
@@ -435,6 +467,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="workload timed for the main line (the headline unless profiling)")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = args.steps if args.steps is not None else 200

@@ -226,3 +226,26 @@ def test_irpe_bf16_repeat_is_deterministic():
     inp, out1 = _irpe_run(2, 2, 14, 14, FLAG_Q | FLAG_K | FLAG_V, 1.0)
     _, out2 = _irpe_run(2, 2, 14, 14, FLAG_Q | FLAG_K | FLAG_V, 1.0, inp=inp)
     assert torch.equal(out1, out2)
+
+
+# ------------------------------------------------------------------ two-warpgroup path (W in {14, 56})
+
+@pytest.mark.parametrize("H,W,flags", [(20, 14, FLAG_K), (10, 56, FLAG_K), (1, 14, FLAG_K),
+                                       (9, 14, 0), (3, 56, 0), (28, 14, FLAG_K)])
+def test_irpe_bf16_pingpong_grids(H, W, flags):
+    # odd and even numbers of query tiles, single-tile grids, ragged last key tile
+    inp, out = _irpe_run(2, 3, H, W, flags, table_std=1.0, seed=H + W)
+    assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
+
+
+def test_irpe_bf16_pingpong_rescale_path():
+    # as test_irpe_bf16_online_rescale_path, on a width served by the two-warpgroup kernel
+    H, W, flags = 28, 14, FLAG_K
+    inp = workloads.irpe_inputs(1, 2, H * W, 64, 49, flags, "bf16", 1.0, seed=7)
+    k = inp["k"].float()
+    k[:, :, 126:252] *= 6.0
+    k[:, :, 252:] *= 12.0
+    inp["k"] = k.to(torch.bfloat16)
+    inp["v"] = (0.5 * inp["v"].float()).to(torch.bfloat16)
+    _, out = _irpe_run(1, 2, H, W, flags, inp=inp)
+    assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16

@@ -59,6 +59,11 @@ struct RpeBf16Args {
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 
+// The two-warpgroup kernel for the key term alone (or no term) on grids whose
+// width it is specialised for. Returns false (and launches nothing) when it
+// does not cover the request; *err then stays untouched.
+bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err);
+
 cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 
 }  // namespace vta
