@@ -37,10 +37,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kD = 64;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-column bf16 tile
 constexpr int kThreads = 384;
-// Register split (launch: 384 threads x 168 = 64,512): control warpgroup 72,
-// softmax warpgroups 208 -> 128 x 72 + 256 x 208 = 62,464.
-constexpr int kRegsControl = 72;
-constexpr int kRegsSoftmax = 208;
+// Register split (launch: 384 threads x 168 = 64,512): control warpgroup 96,
+// softmax warpgroups 200 -> 128 x 96 + 256 x 200 = 63,488.
+constexpr int kRegsControl = 96;
+constexpr int kRegsSoftmax = 200;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxStages = 3;
@@ -56,7 +56,7 @@ struct Geo {
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst;
     uint32_t off_q, off_kv, off_rk, off_qr, off_lut;
-    int lut_len;
+    int lut_len, lut_pad;
     const int32_t *lut;
     __nv_bfloat16 *out;
     float c;  // log2(e) / sqrt(d)
@@ -104,30 +104,102 @@ __device__ __forceinline__ bool wg_red_and(int wg, bool v) {
     return r != 0;
 }
 
-// Pass 1 over one tile: x = S c + QR'[id] in log2 units, columns past the
-// tile (or past the grid, when MASKED) at -inf. Returns the tile maximum.
-template <int W, bool HK, bool MASKED>
-__device__ __forceinline__ float tile_logits(uint32_t (&s)[128], const uint8_t *lut_t,
-                                             const float *qr_t, float c, int nvalid) {
+// One 32-key chunk of a tile for one query row: logits in log2 units
+// (x = S c + QR'[id]; keys past the grid -- only in the last tile -- are set
+// to -inf), an online update of the row's reference max m and sum l, and the
+// chunk's probabilities written into tensor memory as 16 columns of bf16
+// pairs over the already-read scores. The 32 bucket ids are loaded first and
+// the 32 QR' values next, so the two dependent shared-memory loads of each
+// score overlap those of the other 31.
+//
+// The reference max moves only when the chunk's max exceeds it by more than
+// 2^8 (rare after the first chunk); then O (earlier tiles) and the P columns of
+// this tile's earlier chunks are rescaled, warp-uniformly, in tensor memory.
+template <int W, bool HK, int Q>
+__device__ __forceinline__ void softmax_chunk(uint32_t tS, uint32_t tO, const uint8_t *lut_t,
+                                              const float *qr_t, float c, int nvalid,
+                                              bool o_live, float &m, float &l) {
     using G = Geo<W>;
-    float mloc = -INFINITY;
+    if constexpr (Q * 32 < G::KT) {
+        uint32_t s[32];
+        tmem_ld32(tS + Q * 32, s);
+        tmem_ld_wait();
+        float x[32];
+        if constexpr (HK) {
+            int id[32];
 #pragma unroll
-    for (int jj = 0; jj < 128; ++jj) {
-        float x = -INFINITY;
-        if (jj < G::KT) {
-            const int C = (jj / W) * G::COLS + (jj % W);
-            x = __uint_as_float(s[jj]) * c;
-            if (HK) {
-                const int off = (!MASKED || jj < nvalid) ? -C : 0;
-                const int id = lut_t[off];
-                x += qr_t[id * 128];
+            for (int j = 0; j < 32; ++j) {
+                const int jj = Q * 32 + j;
+                const int C = (jj / W) * G::COLS + (jj % W);
+                id[j] = (jj < G::KT) ? lut_t[-C] : 0;
             }
-            if (MASKED && jj >= nvalid) x = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = qr_t[id[j] * 128];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int jj = Q * 32 + j;
+                x[j] = (jj < G::KT) ? fmaf(__uint_as_float(s[j]), c, x[j]) : -INFINITY;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int jj = Q * 32 + j;
+                x[j] = (jj < G::KT) ? __uint_as_float(s[j]) * c : -INFINITY;
+            }
         }
-        s[jj] = __float_as_uint(x);
-        mloc = fmaxf(mloc, x);
+        if (Q * 32 + 32 > nvalid) {  // the chunk reaches past the grid's last row
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (Q * 32 + j >= nvalid) x[j] = -INFINITY;
+        }
+        float cmax = x[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
+        float alpha = 1.f;
+        if (cmax > m + kRescaleLog2) {
+            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - cmax);
+            m = cmax;
+            l *= alpha;
+        }
+        if ((o_live || Q > 0) && __any_sync(~0u, alpha < 1.f)) {
+            tmem_st_wait();
+            if (o_live) {
+#pragma unroll 1
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[16];
+                    tmem_ld16(tO + q * 16, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st16(tO + q * 16, o);
+                }
+            }
+#pragma unroll 1
+            for (int q = 0; q < Q; ++q) {
+                uint32_t pp[16];
+                tmem_ld16(tS + q * 16, pp);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float lo = __uint_as_float(pp[e] << 16) * alpha;
+                    const float hi = __uint_as_float(pp[e] & 0xFFFF0000u) * alpha;
+                    pp[e] = pack_bf16x2(lo, hi);
+                }
+                tmem_st16(tS + q * 16, pp);
+            }
+        }
+        float sum = 0.f;
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const float p0 = ex2_approx(x[2 * e] - m);
+            const float p1 = ex2_approx(x[2 * e + 1] - m);
+            sum += p0 + p1;
+            pk[e] = pack_bf16x2(p0, p1);
+        }
+        l += sum;
+        tmem_st16(tS + Q * 16, pk);
     }
-    return mloc;
 }
 
 template <int W, bool HK>
@@ -154,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s tiles, V at 2s + 1
     uint8_t *sRK = smem + P.off_rk;
     float *sQR = reinterpret_cast<float *>(smem + P.off_qr);  // [2][nb][128]
-    uint8_t *sLut = smem + P.off_lut;
+    uint8_t *sLut = smem + P.off_lut + P.lut_pad;
 
     if (tid == 0) {
         mbar_init(&bars.tab_full, 1);
@@ -176,11 +248,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 512);
-    if (HK)
+    if (HK) {
+        // offset table as bytes, ids clamped into [0, nb). Keys past the last
+        // grid row (masked later) index up to lut_pad bytes before the table;
+        // those bytes hold bucket 0 so every read stays in bounds.
+        for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
         for (int e = tid; e < P.lut_len; e += kThreads) {
             const int id = __ldg(P.lut + e);
             sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
         }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -390,55 +467,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 if (warp_active) {
-                    uint32_t s[128];
-                    tmem_ld32(tS + lane_off, *reinterpret_cast<uint32_t(*)[32]>(s));
-                    tmem_ld32(tS + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-                    tmem_ld32(tS + lane_off + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-                    tmem_ld32(tS + lane_off + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
-                    tmem_ld_wait();
                     const int rj0 = kt * G::R;
                     const int nvalid = min(G::R, P.H - rj0) * W;
                     const uint8_t *lut_t = sLut + (base_i - rj0 * G::COLS);
-                    const float mloc = (nvalid < G::KT)
-                                           ? tile_logits<W, HK, true>(s, lut_t, qr_t, P.c, nvalid)
-                                           : tile_logits<W, HK, false>(s, lut_t, qr_t, P.c, nvalid);
-                    // lazy rescale: the reference max moves only when it grows by > 2^8
-                    float alpha = 1.f;
-                    if (mloc > m + kRescaleLog2) {
-                        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mloc);
-                        m = mloc;
-                        l *= alpha;
-                    }
-                    if (kt > 0 && __any_sync(~0u, alpha < 1.f)) {
-                        // O is stable: the previous P V finished before these scores did.
-                        // 16 columns at a time: the score row still holds 128 registers.
-#pragma unroll 1
-                        for (int q = 0; q < 4; ++q) {
-                            uint32_t o[16];
-                            tmem_ld16(tO + lane_off + q * 16, o);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                            tmem_st16(tO + lane_off + q * 16, o);
-                        }
-                    }
-                    // pass 2: probabilities as bf16 pairs into the score columns
-                    float sum = 0.f;
-                    uint32_t pk0[32], pk1[32];
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const float a0 = ex2_approx(__uint_as_float(s[2 * c]) - m);
-                        const float a1 = ex2_approx(__uint_as_float(s[2 * c + 1]) - m);
-                        const float b0 = ex2_approx(__uint_as_float(s[64 + 2 * c]) - m);
-                        const float b1 = ex2_approx(__uint_as_float(s[64 + 2 * c + 1]) - m);
-                        sum += (a0 + a1) + (b0 + b1);
-                        pk0[c] = pack_bf16x2(a0, a1);
-                        pk1[c] = pack_bf16x2(b0, b1);
-                    }
-                    l += sum;
-                    tmem_st32(tS + lane_off, pk0);
-                    tmem_st32(tS + lane_off + 32, pk1);
+                    const uint32_t tSl = tS + lane_off, tOl = tO + lane_off;
+                    softmax_chunk<W, HK, 0>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
+                    softmax_chunk<W, HK, 1>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
+                    softmax_chunk<W, HK, 2>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
+                    softmax_chunk<W, HK, 3>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
                     tmem_st_wait();
                 }
                 tc_fence_before();
@@ -498,6 +534,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.slices = a.B * a.heads;
     p.items = p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
+    p.lut_pad = static_cast<int>(align_up(G::R * G::COLS, 16));
     p.lut = a.lut;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
@@ -514,7 +551,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_qr = off;
         if (HK) off += align_up(2 * p.nb * 512, 1024);
         p.off_lut = off;
-        if (HK) off += align_up(p.lut_len, 16);
+        if (HK) off += p.lut_pad + align_up(p.lut_len, 16);
         total = 1024 + off;
         p.nst = nst;
         if (total <= cap) break;
