@@ -1,5 +1,6 @@
 // rpe_attn_pingpong_sm103.cu -- iRPE contextual-key attention (or plain
-// attention) on sm_103a with two softmax warpgroups per CTA.
+// attention) on sm_103a: two query tiles per CTA, each softmaxed by eight
+// warps, with the tensor core fed through a ring of tensor-memory slots.
 //
 // Same computation as rpe_attn_sm103.cu for the key term ("Rethinking and
 // Improving Relative Position Encoding for Vision Transformer", eqs. 13, 15
@@ -8,22 +9,37 @@
 // score by bucket id, softmax, P V. This kernel is the fast path for the
 // key-term-only and no-term requests on grids of width W in {14, 56}:
 //
-//   * Two softmax warpgroups, each owning a 128-row query tile of the same
-//     (batch, head) slice, share every K/V tile and take turns on the tensor
-//     core: while one converts its scores, the other's QK^T or PV runs.
-//   * P is written back into the score columns of tensor memory as bf16 and
-//     the PV product reads its A operand from there (no shared-memory copy).
-//   * Key tiles hold whole grid rows (126 keys for W = 14, 112 for W = 56), so
-//     within a tile the offset-table position of key jj is a compile-time
-//     constant: each score's bucket id is one shared-memory byte load at an
-//     immediate offset from a per-tile base.
-//   * Work items (slice, pair of query tiles) are ordered full pairs first so
-//     that the static round-robin assignment stays balanced.
+//   * A CTA takes a pair of 128-row query tiles of one (batch, head) slice;
+//     both share every K/V tile. Each query tile has a softmax group of eight
+//     warps: the two warps that share a tensor-memory lane quarter split each
+//     row's keys in halves, so four warps per SM sub-partition hide one
+//     another's latencies.
+//   * Each group has its own MMA-issuing warp (one thread issuing tcgen05.mma
+//     back to back is limited to roughly one instruction per 100 cycles; two
+//     issuers nearly double the tensor core's intake) and its own ring of two
+//     tensor-memory slots. A "unit" is either QR = Q R^K^T (once per item) or
+//     one tile's scores; unit u goes into slot u mod 2 once unit u-2 has been
+//     consumed (its QR copied out, or its P V issued). Each issuer is an event
+//     loop: it issues a P V the moment its probabilities are ready and the next
+//     unit the moment its inputs have landed.
+//   * Per tile, each half computes its logits x = S c + QR'[id] (log2 units),
+//     writes them back over its scores, and reports its maximum; the two
+//     halves agree on the tile maximum through shared memory. The reference
+//     max m of a row moves only when a tile's max exceeds it by more than 2^8,
+//     in which case O (earlier tiles) is rescaled. Then each half writes its
+//     probabilities as bf16 pairs over its own logits, where the P V product
+//     reads its A operand.
+//   * Key tiles hold whole grid rows (84 keys for W = 14, 56 for W = 56, so
+//     that two score slots and O fit each group's 256 tensor-memory columns);
+//     the offset-table position of key jj of a tile is then a compile-time
+//     constant and each score's bucket id is one shared-memory byte load at an
+//     immediate offset. Keys past the grid (last tile only) get -9984 added by
+//     one extra K = 16 product, so the softmax never tests for them.
 //
-// Warps 0-3: softmax warpgroup 0; 4-7: warpgroup 1; warpgroup 2 (warps 8-11):
-// warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle. Tensor memory
-// (512 columns): warpgroup w owns [256w, 256w + 256): scores / P at +0
-// (128 columns), O at +128 (64), QR at +192 (64).
+// Warps 0-7: group 0 (warp 4h + q: half h, lane quarter q); 8-15: group 1;
+// warpgroup 4 (warps 16-19): 16 TMA producer, 17 and 18 MMA issuers of groups
+// 0 and 1, 19 idle. Tensor memory (512 columns): group w owns [256w, 256w+256):
+// O at +0 (64 columns), slots at +64 and +160 (NS <= 96 columns each).
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -36,27 +52,35 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kD = 64;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-column bf16 tile
-constexpr int kThreads = 384;
-// Register split (launch: 384 threads x 168 = 64,512): control warpgroup 96,
-// softmax warpgroups 200 -> 128 x 96 + 256 x 200 = 63,488.
-constexpr int kRegsControl = 96;
-constexpr int kRegsSoftmax = 200;
-static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * 168, "register split");
+constexpr int kThreads = 640;
+// Register split (launch: 640 threads x 96 = 61,440): control warpgroup 64,
+// softmax warps 104 -> 128 x 64 + 512 x 104 = 61,440.
+constexpr int kRegsLaunch = 96;
+constexpr int kRegsControl = 64;
+constexpr int kRegsSoftmax = 104;
+static_assert(128 * kRegsControl + 512 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxStages = 3;
+constexpr int kSlots = 2;          // score slots per group
+constexpr uint32_t kColSlot0 = 64;  // within the group's 256 columns
+constexpr uint32_t kSlotCols = 96;
+constexpr int kBarPair0 = 3;  // named barriers 3..10: the two warps of a lane quarter
 
 template <int W>
 struct Geo {
-    static constexpr int R = 128 / W;               // grid rows per key tile
+    static constexpr int R = 96 / W;                // grid rows per key tile
     static constexpr int KT = R * W;                // keys per tile
     static constexpr int NS = (KT + 15) / 16 * 16;  // N of QK^T, K of PV
+    static constexpr int HS = NS / 2 / 16 * 16 + ((NS / 2) % 16 ? 16 : 0);  // keys per half
     static constexpr int COLS = 2 * W - 1;          // offset-table row length
+    static_assert(NS <= 96 && HS % 16 == 0 && 2 * HS >= NS, "tile geometry");
 };
 
 struct PPParams {
-    int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst;
-    uint32_t off_q, off_kv, off_rk, off_qr, off_lut;
+    int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
+    uint32_t off_q, off_kv, off_rk, off_qr, off_lut, off_mask, off_xch;
     int lut_len, lut_pad;
+    int nvalid_last;  // keys of the last key tile that lie on the grid
     const int32_t *lut;
     __nv_bfloat16 *out;
     float c;  // log2(e) / sqrt(d)
@@ -64,9 +88,12 @@ struct PPParams {
 };
 
 struct PPBars {
-    uint64_t tab_full, q_full, q_empty;
+    uint64_t tab_full;
+    uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
-    uint64_t qr_full[2], qr_empty[2], s_full[2], p_full[2], o_full[2], o_empty[2];
+    uint64_t slot_full[2][kSlots], slot_done[2][kSlots];
+    uint64_t o_full[2], o_empty[2], pv_done[2];
+    uint64_t fin[2];  // drain of each issuer
 };
 
 struct Item {
@@ -90,13 +117,13 @@ __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
     return r;
 }
 
-// AND-reduction over the 128 threads of softmax warpgroup wg (named barrier 1 + wg).
-__device__ __forceinline__ bool wg_red_and(int wg, bool v) {
+// AND-reduction over the 256 threads of softmax group wg (named barrier 1 + wg).
+__device__ __forceinline__ bool group_red_and(int wg, bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "bar.red.and.pred q, %2, 256, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
         : "r"(v ? 1u : 0u), "r"(1 + wg)
@@ -104,102 +131,119 @@ __device__ __forceinline__ bool wg_red_and(int wg, bool v) {
     return r != 0;
 }
 
-// One 32-key chunk of a tile for one query row: logits in log2 units
-// (x = S c + QR'[id]; keys past the grid -- only in the last tile -- are set
-// to -inf), an online update of the row's reference max m and sum l, and the
-// chunk's probabilities written into tensor memory as 16 columns of bf16
-// pairs over the already-read scores. The 32 bucket ids are loaded first and
-// the 32 QR' values next, so the two dependent shared-memory loads of each
-// score overlap those of the other 31.
-//
-// The reference max moves only when the chunk's max exceeds it by more than
-// 2^8 (rare after the first chunk); then O (earlier tiles) and the P columns of
-// this tile's earlier chunks are rescaled, warp-uniformly, in tensor memory.
-template <int W, bool HK, int Q>
-__device__ __forceinline__ void softmax_chunk(uint32_t tS, uint32_t tO, const uint8_t *lut_t,
-                                              const float *qr_t, float c, int nvalid,
-                                              bool o_live, float &m, float &l) {
-    using G = Geo<W>;
-    if constexpr (Q * 32 < G::KT) {
-        uint32_t s[32];
-        tmem_ld32(tS + Q * 32, s);
+// Multiply this row's O (64 columns) by alpha once the group's previous P V
+// has completed. Out of line: it runs only when a row's reference max moves.
+__device__ __noinline__ void rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
+                                       uint32_t pv_parity, const WaitCtl &wc,
+                                       volatile int *abort) {
+    if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort))) return;
+    tc_fence_after();
+#pragma unroll 1
+    for (int r = 0; r < 4; ++r) {
+        uint32_t o[16];
+        tmem_ld16(tO + r * 16, o);
         tmem_ld_wait();
-        float x[32];
-        if constexpr (HK) {
-            int id[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int jj = Q * 32 + j;
-                const int C = (jj / W) * G::COLS + (jj % W);
-                id[j] = (jj < G::KT) ? lut_t[-C] : 0;
-            }
-#pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = qr_t[id[j] * 128];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int jj = Q * 32 + j;
-                x[j] = (jj < G::KT) ? fmaf(__uint_as_float(s[j]), c, x[j]) : -INFINITY;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int jj = Q * 32 + j;
-                x[j] = (jj < G::KT) ? __uint_as_float(s[j]) * c : -INFINITY;
-            }
-        }
-        if (Q * 32 + 32 > nvalid) {  // the chunk reaches past the grid's last row
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (Q * 32 + j >= nvalid) x[j] = -INFINITY;
-        }
-        float cmax = x[0];
-#pragma unroll
-        for (int j = 1; j < 32; ++j) cmax = fmaxf(cmax, x[j]);
-        float alpha = 1.f;
-        if (cmax > m + kRescaleLog2) {
-            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - cmax);
-            m = cmax;
-            l *= alpha;
-        }
-        if ((o_live || Q > 0) && __any_sync(~0u, alpha < 1.f)) {
-            tmem_st_wait();
-            if (o_live) {
-#pragma unroll 1
-                for (int q = 0; q < 4; ++q) {
-                    uint32_t o[16];
-                    tmem_ld16(tO + q * 16, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st16(tO + q * 16, o);
-                }
-            }
-#pragma unroll 1
-            for (int q = 0; q < Q; ++q) {
-                uint32_t pp[16];
-                tmem_ld16(tS + q * 16, pp);
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float lo = __uint_as_float(pp[e] << 16) * alpha;
-                    const float hi = __uint_as_float(pp[e] & 0xFFFF0000u) * alpha;
-                    pp[e] = pack_bf16x2(lo, hi);
-                }
-                tmem_st16(tS + q * 16, pp);
-            }
-        }
-        float sum = 0.f;
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const float p0 = ex2_approx(x[2 * e] - m);
-            const float p1 = ex2_approx(x[2 * e + 1] - m);
-            sum += p0 + p1;
-            pk[e] = pack_bf16x2(p0, p1);
-        }
-        l += sum;
-        tmem_st16(tS + Q * 16, pk);
+        for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+        tmem_st16(tO + r * 16, o);
     }
+    tmem_st_wait();
+}
+
+// One half (H2 = 0: keys [0, HS) of the tile, 1: keys [HS, 2 HS)) of one row's tile.
+template <int W, bool HK, int H2>
+struct HalfTile {
+    using G = Geo<W>;
+    static constexpr int J0 = G::HS * H2;                       // first key of the half
+    static constexpr int NK = (G::KT - J0 < G::HS) ? G::KT - J0 : G::HS;  // keys of the half
+    static constexpr int NQ = (NK + 15) / 16;                   // 16-key chunks holding them
+
+    // Pass 1: x = S c + QR'[id] over the half's keys, stored back over the
+    // scores, 16 keys at a time; returns the half's max.
+    static __device__ __forceinline__ float logits(uint32_t tS, const uint8_t *lut_t,
+                                                   const float *qr_t, float c) {
+        float mx = -INFINITY;
+        const float2 c2 = make_float2(c, c);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int jc = J0 + 16 * q;
+            float qv[16];
+            if constexpr (HK) {
+                int id[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int jj = jc + j;
+                    const int C = (jj / W) * G::COLS + (jj % W);
+                    id[j] = (jj < G::KT) ? lut_t[-C] : 0;
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) qv[j] = qr_t[id[j] * 128];
+            } else {
+#pragma unroll
+                for (int j = 0; j < 16; ++j) qv[j] = 0.f;
+            }
+            uint32_t s[16];
+            tmem_ld16(tS + jc, s);
+            tmem_ld_wait();
+            float x[16];
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                const float2 r = ffma2(make_float2(__uint_as_float(s[j]), __uint_as_float(s[j + 1])),
+                                       c2, make_float2(qv[j], qv[j + 1]));
+                x[j] = (jc + j < G::KT) ? r.x : -INFINITY;
+                x[j + 1] = (jc + j + 1 < G::KT) ? r.y : -INFINITY;
+            }
+            const float a = fmax3(x[0], x[1], x[2]), b = fmax3(x[3], x[4], x[5]);
+            const float d = fmax3(x[6], x[7], x[8]), e = fmax3(x[9], x[10], x[11]);
+            const float f = fmax3(x[12], x[13], x[14]);
+            mx = fmax3(mx, fmax3(a, b, d), fmax3(e, f, x[15]));
+            uint32_t xs[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xs[j] = __float_as_uint(x[j]);
+            tmem_st16(tS + jc, xs);
+        }
+        return mx;
+    }
+
+    // Pass 2: p = 2^(x - m) as bf16 pairs; chunk q's 8 columns go to J0 + 8q,
+    // over logits already read. Keys past the tile contribute 0. Returns sum p.
+    static __device__ __forceinline__ float probs(uint32_t tS, float m) {
+        tmem_st_wait();
+        float sum = 0.f;
+        const float2 nm = make_float2(-m, -m);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            const int jc = J0 + 16 * q;
+            uint32_t xs[16];
+            tmem_ld16(tS + jc, xs);
+            tmem_ld_wait();
+            float2 p[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float2 d = fadd2(make_float2(__uint_as_float(xs[2 * e]), __uint_as_float(xs[2 * e + 1])), nm);
+                p[e] = make_float2(jc + 2 * e < G::KT ? ex2_approx(d.x) : 0.f,
+                                   jc + 2 * e + 1 < G::KT ? ex2_approx(d.y) : 0.f);
+            }
+            uint32_t pk[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(p[e].x, p[e].y);
+            tmem_st8(tS + J0 + 8 * q, pk);
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) p[j] = fadd2(p[2 * j], p[2 * j + 1]);
+            sum += p[0].x + p[0].y;
+        }
+        return sum;
+    }
+};
+
+// Tensor-memory column (relative to the slot) of the A operand of P V step kk
+// (keys 16 kk .. 16 kk + 15): half kk*16 / HS, chunk within it.
+template <int W>
+__device__ __forceinline__ constexpr uint32_t p_col(int kk) {
+    using G = Geo<W>;
+    return static_cast<uint32_t>((16 * kk / G::HS) * G::HS + ((16 * kk) % G::HS) / 2);
 }
 
 template <int W, bool HK>
@@ -222,27 +266,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl &wc = P.wc;
     const WaitCtl drain{wc.status, kDefaultWaitNs};
 
-    uint8_t *sQ = smem + P.off_q;    // two query tiles
+    uint8_t *sQ = smem + P.off_q;    // nq buffers of two query tiles
     uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s tiles, V at 2s + 1
     uint8_t *sRK = smem + P.off_rk;
     float *sQR = reinterpret_cast<float *>(smem + P.off_qr);  // [2][nb][128]
     uint8_t *sLut = smem + P.off_lut + P.lut_pad;
+    float *sXch = reinterpret_cast<float *>(smem + P.off_xch);  // [2 groups][2 halves][128]
 
     if (tid == 0) {
         mbar_init(&bars.tab_full, 1);
-        mbar_init(&bars.q_full, 1);
-        mbar_init(&bars.q_empty, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.q_full[i], 1);
+            mbar_init(&bars.q_empty[i], 2);  // one arrival per group issuer
+            mbar_init(&bars.o_full[i], 1);
+            mbar_init(&bars.o_empty[i], 256);
+            mbar_init(&bars.pv_done[i], 1);
+            mbar_init(&bars.fin[i], 1);
+            for (int s = 0; s < kSlots; ++s) {
+                mbar_init(&bars.slot_full[i][s], 1);
+                mbar_init(&bars.slot_done[i][s], 256);
+            }
+        }
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bars.kv_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 1);
-        }
-        for (int w = 0; w < 2; ++w) {
-            mbar_init(&bars.qr_full[w], 1);
-            mbar_init(&bars.qr_empty[w], 128);
-            mbar_init(&bars.s_full[w], 1);
-            mbar_init(&bars.p_full[w], 128);
-            mbar_init(&bars.o_full[w], 1);
-            mbar_init(&bars.o_empty[w], 128);
+            mbar_init(&bars.kv_empty[i], 2);  // one arrival per group issuer
         }
         abort_flag = 0;
         fence_mbar_init();
@@ -250,22 +297,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) tmem_alloc(&tmem_base_s, 512);
     if (HK) {
         // offset table as bytes, ids clamped into [0, nb). Keys past the last
-        // grid row (masked later) index up to lut_pad bytes before the table;
-        // those bytes hold bucket 0 so every read stays in bounds.
+        // grid row index up to lut_pad bytes before the table; those bytes hold
+        // bucket 0 so every read stays in bounds (those scores are masked).
         for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
         for (int e = tid; e < P.lut_len; e += kThreads) {
             const int id = __ldg(P.lut + e);
             sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
         }
     }
+    // Masking operands for the last key tile (128 rows x 16 bf16, K-major, 32-byte
+    // swizzle): A has -9984 in column 0 of every row, B has 1 in column 0 of
+    // every key row past the grid, so A B^T adds -9984 to exactly those scores.
+    {
+        uint8_t *mk = smem + P.off_mask;
+        for (int e = tid; e < 2 * 4096 / 16; e += kThreads) st_shared_v4(smem_u32(mk) + e * 16, 0u, 0u, 0u, 0u);
+        __syncthreads();
+        if (tid < 128) {
+            const int r = tid;
+            const int off = r * 32 + ((r >> 2) & 1) * 16;  // where column 0 of row r lives
+            *reinterpret_cast<uint16_t *>(mk + off) = 0xC61Cu;  // bf16 -9984
+            if (r >= P.nvalid_last) *reinterpret_cast<uint16_t *>(mk + 4096 + off) = 0x3F80u;  // bf16 1
+        }
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
+    const int units_qr = HK ? 1 : 0;  // QR units per group and item
 
-    if (warp >= 8) {
+    if (warp >= 16) {
         regs_dealloc<kRegsControl>();
-        if (warp == 8) {
+        if (warp == 16) {
             // -------------------------------------------- TMA producer
             if (lane == 0) {
                 prefetch_tmap(&tm_q);
@@ -275,20 +338,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
                     tma_load_2d(sRK, &tm_rk, &bars.tab_full, 0, 0);
                 }
-                int g = 0, it = 0, last_q = -1;
+                int g = 0, it = 0;
+                int last_q[2] = {-1, -1};
                 int last_use[kMaxStages] = {-1, -1, -1};
                 bool ok = true;
                 for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++it) {
                     const Item I = decode_item(P, item);
-                    if (!(ok = mbar_wait(&bars.q_empty, (it & 1) ^ 1, wc, kStatusTimeoutSync,
+                    const int qb = it % P.nq, quse = it / P.nq;
+                    if (!(ok = mbar_wait(&bars.q_empty[qb], (quse & 1) ^ 1, wc, kStatusTimeoutSync,
                                          &abort_flag)))
                         break;
-                    mbar_arrive_expect_tx(&bars.q_full, (I.has_b ? 2 : 1) * kTileBytes);
-                    tma_load_3d(sQ, &tm_q, &bars.q_full, 0, I.qt0 * 128, I.slice);
+                    uint8_t *qd = sQ + qb * 2 * kTileBytes;
+                    mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes);
+                    tma_load_3d(qd, &tm_q, &bars.q_full[qb], 0, I.qt0 * 128, I.slice);
                     if (I.has_b)
-                        tma_load_3d(sQ + kTileBytes, &tm_q, &bars.q_full, 0, (I.qt0 + 1) * 128,
+                        tma_load_3d(qd + kTileBytes, &tm_q, &bars.q_full[qb], 0, (I.qt0 + 1) * 128,
                                     I.slice);
-                    last_q = it;
+                    last_q[qb] = quse;
                     for (int kt = 0; kt < P.nkt; ++kt, ++g) {
                         const int st = g % P.nst, use = g / P.nst;
                         if (!(ok = mbar_wait(&bars.kv_empty[st], (use & 1) ^ 1, wc,
@@ -304,201 +370,272 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // drain: the most recent load on every barrier has landed
                 if (HK) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
-                if (last_q >= 0)
-                    mbar_wait(&bars.q_full, last_q & 1, drain, kStatusTimeoutDrain, nullptr);
+                for (int b = 0; b < 2; ++b)
+                    if (last_q[b] >= 0)
+                        mbar_wait(&bars.q_full[b], last_q[b] & 1, drain, kStatusTimeoutDrain, nullptr);
                 for (int st = 0; st < kMaxStages; ++st)
                     if (last_use[st] >= 0)
                         mbar_wait(&bars.kv_full[st], last_use[st] & 1, drain, kStatusTimeoutDrain,
                                   nullptr);
             }
             __syncwarp();
-        } else if (warp == 9) {
-            // -------------------------------------------- MMA issuer
+        } else if (warp == 17 || warp == 18) {
+            // -------------------------------------------- MMA issuer of group w
+            // An event loop: each pass consumes the oldest pending unit if the
+            // group has released it (issuing its P V at once) and issues the next
+            // unit if its inputs have landed and a slot is free. For items the
+            // group sits out, it still releases the item's Q buffer and K/V
+            // stages, each after the matching load has landed. A pass that makes
+            // no progress for the wait bound aborts the kernel.
+            const int w = warp - 17;
             if (lane == 0) {
                 constexpr uint32_t kIdS = idesc_bf16(128, G::NS, false, false);
                 constexpr uint32_t kIdQR = idesc_bf16(128, 64, false, false);
                 constexpr uint32_t kIdO = idesc_bf16(128, 64, false, true);
-                uint64_t *last_bar = nullptr;
-                uint32_t last_par = 0;
-                auto commit = [&](uint64_t *bar, uint32_t parity) {
-                    mma_commit(bar);
-                    last_bar = bar;
-                    last_par = parity;
-                };
-                auto issue_s = [&](int w, int st) {
-                    const uint32_t aQ = smem_u32(sQ + w * kTileBytes);
-                    const uint32_t aK = smem_u32(sKV + st * 2 * kTileBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(tmem + w * 256, smem_desc(aQ + kk * 32, 16, 1024, kSwizzle128B),
-                                    smem_desc(aK + kk * 32, 16, 1024, kSwizzle128B), kIdS, kk > 0);
-                };
+                const uint64_t hi128 = smem_desc(0, 16, 1024, kSwizzle128B);
+                const uint32_t tG = tmem + w * 256;
+                const uint32_t aQ = smem_u32(sQ + w * kTileBytes);
+                const uint32_t aKV = smem_u32(sKV);
+                // pending units, oldest first: bits 0-3 stage, 4 QR unit, 5 first
+                // tile of the item, 6 last tile of the item
+                uint32_t pend0 = 0, pend1 = 0;
+                int np = 0;
+                uint32_t u = 0;  // units issued
+                int ci_cons = 0;
                 bool ok = true;
                 if (HK) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
-                int g = 0, it = 0;
-                int ci[2] = {0, 0}, cs[2] = {0, 0}, cp[2] = {0, 0};
-                for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++it) {
+                // generator state: ph 0 = QR unit, 1 = tile units, 2 = sit-out
+                int it = 0, item = blockIdx.x, g = 0, qb = 0, ph = 0, kt = 0;
+                bool q_ready = false;
+                auto enter_item = [&]() {
                     const Item I = decode_item(P, item);
-                    const int nw = I.has_b ? 2 : 1;
-                    if (!(ok = mbar_wait(&bars.q_full, it & 1, wc, kStatusTimeoutLoad, &abort_flag)))
-                        break;
-                    tc_fence_after();
-                    if (HK) {
-                        for (int w = 0; w < nw && ok; ++w) {
-                            if (!(ok = mbar_wait(&bars.qr_empty[w], (ci[w] & 1) ^ 1, wc,
-                                                 kStatusTimeoutSync, &abort_flag)))
-                                break;
-                            tc_fence_after();
-                            const uint32_t aQ = smem_u32(sQ + w * kTileBytes);
+                    qb = it % P.nq;
+                    ph = (w == 1 && !I.has_b) ? 2 : (HK ? 0 : 1);
+                    kt = 0;
+                    q_ready = false;
+                };
+                if (item < P.items) enter_item();
+                unsigned long long idle_since = 0;
+                while (ok) {
+                    bool progress = false;
+                    // 1. consume the oldest pending unit if the group has released it
+                    if (np > 0) {
+                        const uint32_t x = pend0;
+                        const uint32_t cu = u - np;  // its unit index
+                        bool ready = mbar_test(&bars.slot_done[w][cu % kSlots], (cu / kSlots) & 1);
+                        if (ready && (x & 0x30u) == 0x20u)
+                            ready = mbar_test(&bars.o_empty[w], (ci_cons & 1) ^ 1);
+                        if (ready) {
+                            pend0 = pend1;
+                            --np;
+                            progress = true;
+                            if (!(x & 0x10u)) {
+                                tc_fence_after();
+                                const int st = x & 0xF;
+                                const uint64_t dV = smem_desc(aKV + (st * 2 + 1) * kTileBytes, 16, 1024, kSwizzle128B);
+                                const uint32_t aP = tG + kColSlot0 + (cu % kSlots) * kSlotCols;
+                                const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
 #pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ss(tmem + w * 256 + 192,
-                                            smem_desc(aQ + kk * 32, 16, 1024, kSwizzle128B),
-                                            smem_desc(smem_u32(sRK) + kk * 32, 16, 1024,
-                                                      kSwizzle128B),
-                                            kIdQR, kk > 0);
-                            commit(&bars.qr_full[w], ci[w] & 1);
-                        }
-                        if (!ok) break;
-                    }
-                    {
-                        const int st = g % P.nst;
-                        if (!(ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc,
-                                             kStatusTimeoutLoad, &abort_flag)))
-                            break;
-                        tc_fence_after();
-                        for (int w = 0; w < nw; ++w) {
-                            issue_s(w, st);
-                            commit(&bars.s_full[w], cs[w] & 1);
-                            ++cs[w];
-                        }
-                        if (P.nkt == 1) commit(&bars.q_empty, it & 1);
-                    }
-                    for (int kt = 0; ok && kt < P.nkt; ++kt, ++g) {
-                        const int st = g % P.nst;
-                        const bool last = kt == P.nkt - 1;
-                        const int stn = (g + 1) % P.nst;
-                        for (int w = 0; w < nw; ++w) {
-                            if (!(ok = mbar_wait(&bars.p_full[w], cp[w] & 1, wc,
-                                                 kStatusTimeoutSync, &abort_flag)))
-                                break;
-                            ++cp[w];
-                            if (kt == 0 && !(ok = mbar_wait(&bars.o_empty[w], (ci[w] & 1) ^ 1, wc,
-                                                            kStatusTimeoutSync, &abort_flag)))
-                                break;
-                            tc_fence_after();
-                            const uint32_t aV = smem_u32(sKV + st * 2 * kTileBytes + kTileBytes);
-#pragma unroll
-                            for (int kk = 0; kk < G::NS / 16; ++kk)
-                                mma_bf16_ts(tmem + w * 256 + 128, tmem + w * 256 + kk * 8,
-                                            smem_desc(aV + kk * 2048, 16, 1024, kSwizzle128B), kIdO,
-                                            (kt > 0 || kk > 0) ? 1u : 0u);
-                            if (last) {
-                                commit(&bars.o_full[w], ci[w] & 1);
-                            } else {
-                                // this warpgroup's next scores overwrite its P only after
-                                // the P V above (tcgen05.mma from one thread run in order)
-                                if (w == 0 &&
-                                    !(ok = mbar_wait(&bars.kv_full[stn], ((g + 1) / P.nst) & 1, wc,
-                                                     kStatusTimeoutLoad, &abort_flag)))
-                                    break;
-                                issue_s(w, stn);
-                                commit(&bars.s_full[w], cs[w] & 1);
-                                ++cs[w];
-                                if (w == nw - 1 && kt + 1 == P.nkt - 1) commit(&bars.q_empty, it & 1);
+                                for (int kk = 0; kk < G::NS / 16; ++kk)
+                                    mma_bf16_ts(tG, aP + p_col<W>(kk), dV + kk * (2048 >> 4), kIdO,
+                                                kk > 0 ? 1u : acc0);
+                                mma_commit(&bars.pv_done[w]);
+                                mma_commit(&bars.kv_empty[st]);
+                                if (x & 0x40u) {
+                                    mma_commit(&bars.o_full[w]);
+                                    ++ci_cons;
+                                }
                             }
                         }
-                        if (!ok) break;
-                        commit(&bars.kv_empty[st], (g / P.nst) & 1);
                     }
-                    for (int w = 0; w < nw; ++w) ++ci[w];
+                    // 2. next unit (or sit-out release) once its inputs have landed
+                    const bool has_next = item < P.items;
+                    if (has_next && (ph == 2 || np < kSlots)) {
+                        bool ready = q_ready;
+                        if (!ready && mbar_test(&bars.q_full[qb], (it / P.nq) & 1)) ready = q_ready = true;
+                        const int st = g % P.nst;
+                        if (ready && ph >= 1) ready = mbar_test(&bars.kv_full[st], (g / P.nst) & 1);
+                        if (ready) {
+                            progress = true;
+                            bool item_done = false;
+                            if (ph == 2) {
+                                // sit-out: release this tile's stage (and, at the end, Q)
+                                mbar_arrive(&bars.kv_empty[st]);
+                                ++g;
+                                if (kt == P.nkt - 1) {
+                                    mbar_arrive(&bars.q_empty[qb]);
+                                    item_done = true;
+                                } else {
+                                    ++kt;
+                                }
+                            } else {
+                                tc_fence_after();
+                                const uint32_t slot = u % kSlots;
+                                const uint64_t dQ = hi128 | ((aQ + qb * 2 * kTileBytes) >> 4);
+                                const uint32_t dS = tG + kColSlot0 + slot * kSlotCols;
+                                uint32_t code;
+                                if (ph == 0) {
+                                    const uint64_t dRK = hi128 | (smem_u32(sRK) >> 4);
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_bf16_ss(dS, dQ + kk * 2, dRK + kk * 2, kIdQR, kk > 0);
+                                    code = 0x10u;
+                                    ph = 1;
+                                } else {
+                                    const uint64_t dK = hi128 | ((aKV + st * 2 * kTileBytes) >> 4);
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk)
+                                        mma_bf16_ss(dS, dQ + kk * 2, dK + kk * 2, kIdS, kk > 0);
+                                    const bool last = kt == P.nkt - 1;
+                                    if (last && P.nvalid_last < G::KT) {
+                                        const uint64_t dMA = smem_desc(smem_u32(smem + P.off_mask), 16, 256, kSwizzle32B);
+                                        mma_bf16_ss(dS, dMA, dMA + (4096 >> 4), kIdS, 1u);
+                                    }
+                                    code = static_cast<uint32_t>(st) | (kt == 0 ? 0x20u : 0u) | (last ? 0x40u : 0u);
+                                    ++g;
+                                    if (last) {
+                                        item_done = true;
+                                    } else {
+                                        ++kt;
+                                    }
+                                }
+                                mma_commit(&bars.slot_full[w][slot]);
+                                if (item_done) mma_commit(&bars.q_empty[qb]);
+                                if (np == 0) pend0 = code; else pend1 = code;
+                                ++np;
+                                ++u;
+                            }
+                            if (item_done) {
+                                ++it;
+                                item += gridDim.x;
+                                if (item < P.items) enter_item();
+                            }
+                        }
+                    }
+                    if (!has_next && np == 0) break;
+                    if (progress) {
+                        idle_since = 0;
+                    } else {
+                        if (abort_flag) break;
+                        const unsigned long long now = global_ns();
+                        if (idle_since == 0) {
+                            idle_since = now;
+                        } else if (now - idle_since > wc.limit_ns) {
+                            atomicOr(wc.status, kStatusTimeoutSync);
+                            abort_flag = 1;
+                            ok = false;
+                        }
+                    }
                 }
-                // drain: tcgen05 work completes in order, so the last commit covers it all
-                if (last_bar != nullptr)
-                    mbar_wait(last_bar, last_par, drain, kStatusTimeoutDrain, nullptr);
+                // drain: a last commit completes after every product this thread issued
+                mma_commit(&bars.fin[w]);
+                mbar_wait(&bars.fin[w], 0, drain, kStatusTimeoutDrain, nullptr);
             }
             __syncwarp();
         }
     } else {
         regs_alloc<kRegsSoftmax>();
-        // ------------------------------------------------ softmax warpgroups
-        const int wg = warp >> 2;
-        const int lw = warp & 3;
-        const int t = tid & 127;
-        const uint32_t lane_off = static_cast<uint32_t>(lw * 32) << 16;
-        const uint32_t tS = tmem + wg * 256, tO = tS + 128, tQR = tS + 192;
+        // ------------------------------------------------ softmax groups
+        const int wg = warp >> 3;        // query tile of the pair
+        const int h = (warp >> 2) & 1;  // half of each row's keys
+        const int lq = warp & 3;         // tensor-memory lane quarter
+        const int t = lq * 32 + lane;    // row within the query tile
+        const int pair_bar = kBarPair0 + wg * 4 + lq;
+        const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
+        const uint32_t tG = tmem + wg * 256;
+        const uint32_t tOl = tG + lane_off;
         float *qr_t = sQR + wg * P.nb * 128 + t;
-        int it_w = 0, s_cnt = 0;
+        float *xch = sXch + wg * 256;  // [2 halves][128 rows]
+        uint32_t u = 0;  // this group's unit counter
+        int it_w = 0, gw = 0;
         for (int item = blockIdx.x; item < P.items; item += gridDim.x) {
             const Item I = decode_item(P, item);
             if (wg == 1 && !I.has_b) continue;
             const int qt = I.qt0 + wg;
             const int i = qt * 128 + t;
-            const bool warp_active = qt * 128 + lw * 32 < P.N;
+            const bool warp_active = qt * 128 + lq * 32 < P.N;
             const int ic = i < P.N ? i : P.N - 1;
             const int base_i = (ic / W) * G::COLS + (ic % W) + (P.H - 1) * G::COLS + (W - 1);
             if (HK) {
-                bool ok = __all_sync(~0u, mbar_wait(&bars.qr_full[wg], it_w & 1, wc,
+                const uint32_t slot = u % kSlots;
+                bool ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
                                                     kStatusTimeoutMma, &abort_flag));
-                if (!wg_red_and(wg, ok)) break;
+                if (!group_red_and(wg, ok)) break;
                 tc_fence_after();
                 if (warp_active) {
-                    uint32_t r0[32], r1[32];
-                    tmem_ld32(tQR + lane_off, r0);
-                    tmem_ld32(tQR + lane_off + 32, r1);
+                    // half 0 copies buckets 0-31, half 1 buckets 32-63
+                    uint32_t r[32];
+                    tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off + 32 * h, r);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int b = 0; b < 64; ++b)
-                        if (b < P.nb)
-                            qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
+                    for (int b = 0; b < 32; ++b)
+                        if (32 * h + b < P.nb) qr_t[(32 * h + b) * 128] = __uint_as_float(r[b]) * P.c;
                 }
                 tc_fence_before();
-                mbar_arrive(&bars.qr_empty[wg]);
+                mbar_arrive(&bars.slot_done[wg][slot]);
+                named_bar_sync(pair_bar, 64);  // both halves of the row's QR' are in place
+                ++u;
             }
             float m = -INFINITY, l = 0.f;
             bool aborted = false;
-            for (int kt = 0; kt < P.nkt; ++kt) {
-                bool ok = __all_sync(~0u, mbar_wait(&bars.s_full[wg], s_cnt & 1, wc,
+            for (int kt = 0; kt < P.nkt; ++kt, ++gw, ++u) {
+                const uint32_t slot = u % kSlots;
+                bool ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
                                                     kStatusTimeoutMma, &abort_flag));
-                ++s_cnt;
-                if (!wg_red_and(wg, ok)) {
+                if (!group_red_and(wg, ok)) {
                     aborted = true;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t tSl = tG + kColSlot0 + slot * kSlotCols + lane_off;
+                const uint8_t *lut_t = sLut + (base_i - kt * G::R * G::COLS);
+                float mh = -INFINITY;
+                if (warp_active)
+                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lut_t, qr_t, P.c)
+                                : HalfTile<W, HK, 1>::logits(tSl, lut_t, qr_t, P.c);
+                // agree on the tile max with the other half of the row
+                xch[h * 128 + t] = mh;
+                named_bar_sync(pair_bar, 64);
+                const float mt = fmaxf(mh, xch[(h ^ 1) * 128 + t]);
+                named_bar_sync(pair_bar, 64);  // the exchange slots may be reused
                 if (warp_active) {
-                    const int rj0 = kt * G::R;
-                    const int nvalid = min(G::R, P.H - rj0) * W;
-                    const uint8_t *lut_t = sLut + (base_i - rj0 * G::COLS);
-                    const uint32_t tSl = tS + lane_off, tOl = tO + lane_off;
-                    softmax_chunk<W, HK, 0>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
-                    softmax_chunk<W, HK, 1>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
-                    softmax_chunk<W, HK, 2>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
-                    softmax_chunk<W, HK, 3>(tSl, tOl, lut_t, qr_t, P.c, nvalid, kt > 0, m, l);
+                    // lazy rescale: the reference max moves only when it grows by > 2^8
+                    float alpha = 1.f;
+                    if (mt > m + kRescaleLog2) {
+                        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - mt);
+                        m = mt;
+                        l *= alpha;
+                    }
+                    if (h == 0 && kt > 0 && __any_sync(~0u, alpha < 1.f))
+                        rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
+                    l += h == 0 ? HalfTile<W, HK, 0>::probs(tSl, m) : HalfTile<W, HK, 1>::probs(tSl, m);
                     tmem_st_wait();
                 }
                 tc_fence_before();
-                mbar_arrive(&bars.p_full[wg]);
+                mbar_arrive(&bars.slot_done[wg][slot]);
             }
-            if (!wg_red_and(wg, !aborted)) break;
+            if (!group_red_and(wg, !aborted)) break;
             bool ok = __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc, kStatusTimeoutMma,
                                                 &abort_flag));
-            if (!wg_red_and(wg, ok)) break;
+            if (!group_red_and(wg, ok)) break;
             tc_fence_after();
-            uint32_t o0[32], o1[32];
+            // each half normalises and stores 32 of the row's 64 output columns
+            xch[h * 128 + t] = l;
+            named_bar_sync(pair_bar, 64);
+            const float inv = 1.f / (l + xch[(h ^ 1) * 128 + t]);
+            named_bar_sync(pair_bar, 64);
+            uint32_t o[32];
             if (warp_active) {
-                tmem_ld32(tO + lane_off, o0);
-                tmem_ld32(tO + lane_off + 32, o1);
+                tmem_ld32(tOl + 32 * h, o);
                 tmem_ld_wait();
             }
             tc_fence_before();
             mbar_arrive(&bars.o_empty[wg]);
             if (i < P.N) {
-                const float inv = 1.f / l;
-                uint4 *dst = reinterpret_cast<uint4 *>(P.out + (static_cast<size_t>(I.slice) * P.N + i) * kD);
+                uint4 *dst = reinterpret_cast<uint4 *>(P.out + (static_cast<size_t>(I.slice) * P.N + i) * kD + 32 * h);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t *src = c < 4 ? o0 + 8 * c : o1 + 8 * (c - 4);
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t *src = o + 8 * c;
                     uint4 v;
                     v.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
                     v.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
@@ -535,15 +672,20 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.items = p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
     p.lut_pad = static_cast<int>(align_up(G::R * G::COLS, 16));
+    p.nvalid_last = N - (p.nkt - 1) * G::KT;
     p.lut = a.lut;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
     const uint32_t cap = 227 * 1024 - 1024;
     uint32_t total = 0;
-    for (int nst = kMaxStages; nst >= 2; --nst) {
+    // prefer three K/V stages, then a double-buffered Q
+    const int choices[4][2] = {{3, 2}, {3, 1}, {2, 2}, {2, 1}};
+    for (const auto &ch : choices) {
+        const int nst = ch[0];
+        p.nq = ch[1];
         uint32_t off = 0;
         p.off_q = off;
-        off += 2 * kTileBytes;
+        off += p.nq * 2 * kTileBytes;
         p.off_kv = off;
         off += nst * 2 * kTileBytes;
         p.off_rk = off;
@@ -552,6 +694,11 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         if (HK) off += align_up(2 * p.nb * 512, 1024);
         p.off_lut = off;
         if (HK) off += p.lut_pad + align_up(p.lut_len, 16);
+        off = align_up(off, 1024);
+        p.off_mask = off;
+        off += 2 * 4096;
+        p.off_xch = off;
+        off += 2 * 2 * 128 * 4;
         total = 1024 + off;
         p.nst = nst;
         if (total <= cap) break;
@@ -586,7 +733,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
 }  // namespace
 
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
-    if (a.d != kD || (a.terms & ~1u) != 0) return false;
+    if (a.d != kD || (a.terms & ~1u) != 0 || a.num_buckets > 64) return false;
     const bool hk = (a.terms & 1u) != 0;
     if (a.W == 14)
         *err = hk ? launch_pp<14, true>(a, stream) : launch_pp<14, false>(a, stream);
