@@ -78,11 +78,10 @@ struct Geo {
 
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
-    uint32_t off_q, off_kv, off_rk, off_qr, off_lut, off_mask, off_xch;
+    uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask, off_xch;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
     const int32_t *lut;
-    __nv_bfloat16 *out;
     float c;  // log2(e) / sqrt(d)
     WaitCtl wc;
 };
@@ -93,7 +92,7 @@ struct PPBars {
     uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
     uint64_t slot_full[2][kSlots], slot_done[2][kSlots];
     uint64_t o_full[2], o_empty[2], pv_done[2];
-    uint64_t fin[2];  // drain of each issuer
+    uint64_t fin[2];   // drain of each issuer
 };
 
 struct Item {
@@ -117,26 +116,26 @@ __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
     return r;
 }
 
-// AND-reduction over the 256 threads of softmax group wg (named barrier 1 + wg).
-__device__ __forceinline__ bool group_red_and(int wg, bool v) {
+// AND-reduction of v over the nthreads threads that use named barrier id.
+__device__ __forceinline__ bool red_and(int id, int nthreads, bool v) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, 256, p;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}"
         : "=r"(r)
-        : "r"(v ? 1u : 0u), "r"(1 + wg)
+        : "r"(v ? 1u : 0u), "r"(id), "r"(nthreads)
         : "memory");
     return r != 0;
 }
 
 // Multiply this row's O (64 columns) by alpha once the group's previous P V
 // has completed. Out of line: it runs only when a row's reference max moves.
-__device__ __noinline__ void rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
+__device__ __noinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
                                        uint32_t pv_parity, const WaitCtl &wc,
                                        volatile int *abort) {
-    if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort))) return;
+    if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort))) return false;
     tc_fence_after();
 #pragma unroll 1
     for (int r = 0; r < 4; ++r) {
@@ -148,6 +147,7 @@ __device__ __noinline__ void rescale_o(float alpha, uint32_t tO, uint64_t *pv_ba
         tmem_st16(tO + r * 16, o);
     }
     tmem_st_wait();
+    return true;
 }
 
 // One half (H2 = 0: keys [0, HS) of the tile, 1: keys [HS, 2 HS)) of one row's tile.
@@ -158,10 +158,27 @@ struct HalfTile {
     static constexpr int NK = (G::KT - J0 < G::HS) ? G::KT - J0 : G::HS;  // keys of the half
     static constexpr int NQ = (NK + 15) / 16;                   // 16-key chunks holding them
 
+    // Grid rows of the tile that the half's keys lie on, and the key columns
+    // [c_lo, c_hi) of each. The offset-table bytes of one grid row of keys are
+    // contiguous (column c at byte c_hi - 1 - c from the lowest), so each run is
+    // read as aligned words, realigned with a funnel shift, and each id taken
+    // out with a byte permute: about one shared-memory wavefront per four ids.
+    static constexpr int ROW_LO = J0 / W;
+    static constexpr int ROW_HI = (J0 + NK - 1) / W;
+    static constexpr int NROWS = ROW_HI - ROW_LO + 1;
+    static constexpr int c_lo(int r) { return (J0 > r * W ? J0 : r * W) - r * W; }
+    static constexpr int c_hi(int r) { return (J0 + NK < (r + 1) * W ? J0 + NK : (r + 1) * W) - r * W; }
+    static constexpr int run_words(int r) { return (c_hi(r) - c_lo(r) + 3) / 4; }
+    static constexpr int NA = (W < NK ? W : NK) / 4 + 1;  // >= run_words of any row
+    static constexpr int first_chunk(int r) { return ((J0 > r * W ? J0 : r * W) - J0) / 16; }
+
     // Pass 1: x = S c + QR'[id] over the half's keys, stored back over the
-    // scores, 16 keys at a time; returns the half's max.
-    static __device__ __forceinline__ float logits(uint32_t tS, const uint8_t *lut_t,
-                                                   const float *qr_t, float c) {
+    // scores, 16 keys at a time; returns the half's max. lut_a: shared address
+    // of the offset-table byte of the tile's key 0 for this row; qr_a: shared
+    // address of this row's QR' for bucket 0 (buckets 512 bytes apart).
+    static __device__ __forceinline__ float logits(uint32_t tS, uint32_t lut_a, uint32_t qr_a,
+                                                   float c) {
+        uint32_t ida[NROWS][NA];
         float mx = -INFINITY;
         const float2 c2 = make_float2(c, c);
 #pragma unroll
@@ -169,15 +186,33 @@ struct HalfTile {
             const int jc = J0 + 16 * q;
             float qv[16];
             if constexpr (HK) {
-                int id[16];
+                // the id words of each grid row, read at the first chunk that needs them
+#pragma unroll
+                for (int rr = 0; rr < NROWS; ++rr) {
+                    const int r = ROW_LO + rr;
+                    if (first_chunk(r) != q) continue;
+                    const uint32_t lo = lut_a - static_cast<uint32_t>(r * G::COLS + c_hi(r) - 1);
+                    const uint32_t sh = (lo & 3u) * 8u;
+                    const uint32_t wa = lo & ~3u;
+                    uint32_t wv[NA + 1];
+#pragma unroll
+                    for (int m = 0; m <= NA; ++m)
+                        if (m <= run_words(r)) wv[m] = ld_shared_u32(wa + 4 * m);
+#pragma unroll
+                    for (int m = 0; m < NA; ++m)
+                        if (m < run_words(r)) ida[rr][m] = __funnelshift_r(wv[m], wv[m + 1], sh);
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int jj = jc + j;
-                    const int C = (jj / W) * G::COLS + (jj % W);
-                    id[j] = (jj < G::KT) ? lut_t[-C] : 0;
+                    if (jj < J0 + NK) {
+                        const int r = jj / W, k = c_hi(r) - 1 - jj % W;
+                        const uint32_t id = __byte_perm(ida[r - ROW_LO][k / 4], 0u, 0x4440u | (k % 4));
+                        qv[j] = ld_shared_f32(qr_a + id * 512u);
+                    } else {
+                        qv[j] = 0.f;
+                    }
                 }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) qv[j] = qr_t[id[j] * 128];
             } else {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qv[j] = 0.f;
@@ -251,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
-                        const __grid_constant__ CUtensorMap tm_rk, const PPParams P) {
+                        const __grid_constant__ CUtensorMap tm_rk,
+                        const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     using G = Geo<W>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -269,9 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sQ = smem + P.off_q;    // nq buffers of two query tiles
     uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s tiles, V at 2s + 1
     uint8_t *sRK = smem + P.off_rk;
-    float *sQR = reinterpret_cast<float *>(smem + P.off_qr);  // [2][nb][128]
     uint8_t *sLut = smem + P.off_lut + P.lut_pad;
-    float *sXch = reinterpret_cast<float *>(smem + P.off_xch);  // [2 groups][2 halves][128]
+    float *sXch = reinterpret_cast<float *>(smem + P.off_xch);  // [2 groups][3][2 halves][128]
 
     if (tid == 0) {
         mbar_init(&bars.tab_full, 1);
@@ -324,7 +359,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-    const int units_qr = HK ? 1 : 0;  // QR units per group and item
 
     if (warp >= 16) {
         regs_dealloc<kRegsControl>();
@@ -381,12 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else if (warp == 17 || warp == 18) {
             // -------------------------------------------- MMA issuer of group w
-            // An event loop: each pass consumes the oldest pending unit if the
-            // group has released it (issuing its P V at once) and issues the next
-            // unit if its inputs have landed and a slot is free. For items the
-            // group sits out, it still releases the item's Q buffer and K/V
-            // stages, each after the matching load has landed. A pass that makes
-            // no progress for the wait bound aborts the kernel.
+            // With two slots the order is fixed: unit u is issued once unit u - 2
+            // has been consumed (and, for a tile's scores, its P V issued), so
+            // the issuer is a straight sequence of bounded blocking waits. For
+            // items the group sits out it still releases the item's Q buffer and
+            // K/V stages, each after the matching load has landed.
             const int w = warp - 17;
             if (lane == 0) {
                 constexpr uint32_t kIdS = idesc_bf16(128, G::NS, false, false);
@@ -396,137 +429,101 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tG = tmem + w * 256;
                 const uint32_t aQ = smem_u32(sQ + w * kTileBytes);
                 const uint32_t aKV = smem_u32(sKV);
-                // pending units, oldest first: bits 0-3 stage, 4 QR unit, 5 first
+                // outstanding units, oldest first: bits 0-3 stage, 4 QR unit, 5 first
                 // tile of the item, 6 last tile of the item
                 uint32_t pend0 = 0, pend1 = 0;
                 int np = 0;
                 uint32_t u = 0;  // units issued
-                int ci_cons = 0;
+                int ci = 0;      // items whose last P V was issued
                 bool ok = true;
                 if (HK) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
-                // generator state: ph 0 = QR unit, 1 = tile units, 2 = sit-out
-                int it = 0, item = blockIdx.x, g = 0, qb = 0, ph = 0, kt = 0;
-                bool q_ready = false;
-                auto enter_item = [&]() {
-                    const Item I = decode_item(P, item);
-                    qb = it % P.nq;
-                    ph = (w == 1 && !I.has_b) ? 2 : (HK ? 0 : 1);
-                    kt = 0;
-                    q_ready = false;
+                // consume the oldest outstanding unit: wait until the group has
+                // released it, then issue its P V
+                auto consume = [&]() {
+                    const uint32_t x = pend0;
+                    const uint32_t cu = u - np;
+                    pend0 = pend1;
+                    --np;
+                    ok = ok && mbar_wait(&bars.slot_done[w][cu % kSlots], (cu / kSlots) & 1, wc,
+                                         kStatusTimeoutSync, &abort_flag);
+                    if (!ok || (x & 0x10u)) return;
+                    if (x & 0x20u)
+                        ok = mbar_wait(&bars.o_empty[w], (ci & 1) ^ 1, wc, kStatusTimeoutSync, &abort_flag);
+                    if (!ok) return;
+                    tc_fence_after();
+                    const int st = x & 0xF;
+                    const uint64_t dV = hi128 | ((aKV + (st * 2 + 1) * kTileBytes) >> 4);
+                    const uint32_t aP = tG + kColSlot0 + (cu % kSlots) * kSlotCols;
+                    const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
+#pragma unroll
+                    for (int kk = 0; kk < G::NS / 16; ++kk)
+                        mma_bf16_ts(tG, aP + p_col<W>(kk), dV + kk * (2048 >> 4), kIdO,
+                                    kk > 0 ? 1u : acc0);
+                    mma_commit(&bars.pv_done[w]);
+                    mma_commit(&bars.kv_empty[st]);
+                    if (x & 0x40u) {
+                        mma_commit(&bars.o_full[w]);
+                        ++ci;
+                    }
                 };
-                if (item < P.items) enter_item();
-                unsigned long long idle_since = 0;
-                while (ok) {
-                    bool progress = false;
-                    // 1. consume the oldest pending unit if the group has released it
-                    if (np > 0) {
-                        const uint32_t x = pend0;
-                        const uint32_t cu = u - np;  // its unit index
-                        bool ready = mbar_test(&bars.slot_done[w][cu % kSlots], (cu / kSlots) & 1);
-                        if (ready && (x & 0x30u) == 0x20u)
-                            ready = mbar_test(&bars.o_empty[w], (ci_cons & 1) ^ 1);
-                        if (ready) {
-                            pend0 = pend1;
-                            --np;
-                            progress = true;
-                            if (!(x & 0x10u)) {
-                                tc_fence_after();
-                                const int st = x & 0xF;
-                                const uint64_t dV = smem_desc(aKV + (st * 2 + 1) * kTileBytes, 16, 1024, kSwizzle128B);
-                                const uint32_t aP = tG + kColSlot0 + (cu % kSlots) * kSlotCols;
-                                const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
-#pragma unroll
-                                for (int kk = 0; kk < G::NS / 16; ++kk)
-                                    mma_bf16_ts(tG, aP + p_col<W>(kk), dV + kk * (2048 >> 4), kIdO,
-                                                kk > 0 ? 1u : acc0);
-                                mma_commit(&bars.pv_done[w]);
-                                mma_commit(&bars.kv_empty[st]);
-                                if (x & 0x40u) {
-                                    mma_commit(&bars.o_full[w]);
-                                    ++ci_cons;
-                                }
-                            }
+                int g = 0, it = 0;
+                for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++it) {
+                    const Item I = decode_item(P, item);
+                    const int qb = it % P.nq;
+                    ok = mbar_wait(&bars.q_full[qb], (it / P.nq) & 1, wc, kStatusTimeoutLoad, &abort_flag);
+                    if (w == 1 && !I.has_b) {
+                        // the outstanding units' P V release K/V stages that the
+                        // loads below may be waiting for: issue them first
+                        while (ok && np > 0) consume();
+                        for (int kt = 0; ok && kt < P.nkt; ++kt, ++g) {
+                            const int st = g % P.nst;
+                            ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc, kStatusTimeoutLoad,
+                                           &abort_flag);
+                            if (ok) mbar_arrive(&bars.kv_empty[st]);
                         }
+                        if (ok) mbar_arrive(&bars.q_empty[qb]);
+                        continue;
                     }
-                    // 2. next unit (or sit-out release) once its inputs have landed
-                    const bool has_next = item < P.items;
-                    if (has_next && (ph == 2 || np < kSlots)) {
-                        bool ready = q_ready;
-                        if (!ready && mbar_test(&bars.q_full[qb], (it / P.nq) & 1)) ready = q_ready = true;
-                        const int st = g % P.nst;
-                        if (ready && ph >= 1) ready = mbar_test(&bars.kv_full[st], (g / P.nst) & 1);
-                        if (ready) {
-                            progress = true;
-                            bool item_done = false;
-                            if (ph == 2) {
-                                // sit-out: release this tile's stage (and, at the end, Q)
-                                mbar_arrive(&bars.kv_empty[st]);
-                                ++g;
-                                if (kt == P.nkt - 1) {
-                                    mbar_arrive(&bars.q_empty[qb]);
-                                    item_done = true;
-                                } else {
-                                    ++kt;
-                                }
-                            } else {
-                                tc_fence_after();
-                                const uint32_t slot = u % kSlots;
-                                const uint64_t dQ = hi128 | ((aQ + qb * 2 * kTileBytes) >> 4);
-                                const uint32_t dS = tG + kColSlot0 + slot * kSlotCols;
-                                uint32_t code;
-                                if (ph == 0) {
-                                    const uint64_t dRK = hi128 | (smem_u32(sRK) >> 4);
+                    const uint64_t dQ = hi128 | ((aQ + qb * 2 * kTileBytes) >> 4);
+                    for (int kt = HK ? -1 : 0; ok && kt < P.nkt; ++kt) {
+                        if (np == kSlots) consume();
+                        if (!ok) break;
+                        const uint32_t slot = u % kSlots;
+                        const uint32_t dS = tG + kColSlot0 + slot * kSlotCols;
+                        uint32_t code;
+                        if (kt < 0) {
+                            tc_fence_after();
+                            const uint64_t dRK = hi128 | (smem_u32(sRK) >> 4);
 #pragma unroll
-                                    for (int kk = 0; kk < 4; ++kk)
-                                        mma_bf16_ss(dS, dQ + kk * 2, dRK + kk * 2, kIdQR, kk > 0);
-                                    code = 0x10u;
-                                    ph = 1;
-                                } else {
-                                    const uint64_t dK = hi128 | ((aKV + st * 2 * kTileBytes) >> 4);
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss(dS, dQ + kk * 2, dRK + kk * 2, kIdQR, kk > 0);
+                            code = 0x10u;
+                        } else {
+                            const int st = g % P.nst;
+                            ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc, kStatusTimeoutLoad,
+                                           &abort_flag);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const uint64_t dK = hi128 | ((aKV + st * 2 * kTileBytes) >> 4);
 #pragma unroll
-                                    for (int kk = 0; kk < 4; ++kk)
-                                        mma_bf16_ss(dS, dQ + kk * 2, dK + kk * 2, kIdS, kk > 0);
-                                    const bool last = kt == P.nkt - 1;
-                                    if (last && P.nvalid_last < G::KT) {
-                                        const uint64_t dMA = smem_desc(smem_u32(smem + P.off_mask), 16, 256, kSwizzle32B);
-                                        mma_bf16_ss(dS, dMA, dMA + (4096 >> 4), kIdS, 1u);
-                                    }
-                                    code = static_cast<uint32_t>(st) | (kt == 0 ? 0x20u : 0u) | (last ? 0x40u : 0u);
-                                    ++g;
-                                    if (last) {
-                                        item_done = true;
-                                    } else {
-                                        ++kt;
-                                    }
-                                }
-                                mma_commit(&bars.slot_full[w][slot]);
-                                if (item_done) mma_commit(&bars.q_empty[qb]);
-                                if (np == 0) pend0 = code; else pend1 = code;
-                                ++np;
-                                ++u;
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss(dS, dQ + kk * 2, dK + kk * 2, kIdS, kk > 0);
+                            const bool last = kt == P.nkt - 1;
+                            if (last && P.nvalid_last < G::KT) {
+                                const uint64_t dMA = smem_desc(smem_u32(smem + P.off_mask), 16, 256, kSwizzle32B);
+                                mma_bf16_ss(dS, dMA, dMA + (4096 >> 4), kIdS, 1u);
                             }
-                            if (item_done) {
-                                ++it;
-                                item += gridDim.x;
-                                if (item < P.items) enter_item();
-                            }
+                            code = static_cast<uint32_t>(st) | (kt == 0 ? 0x20u : 0u) | (last ? 0x40u : 0u);
+                            ++g;
                         }
-                    }
-                    if (!has_next && np == 0) break;
-                    if (progress) {
-                        idle_since = 0;
-                    } else {
-                        if (abort_flag) break;
-                        const unsigned long long now = global_ns();
-                        if (idle_since == 0) {
-                            idle_since = now;
-                        } else if (now - idle_since > wc.limit_ns) {
-                            atomicOr(wc.status, kStatusTimeoutSync);
-                            abort_flag = 1;
-                            ok = false;
-                        }
+                        mma_commit(&bars.slot_full[w][slot]);
+                        if (kt == P.nkt - 1) mma_commit(&bars.q_empty[qb]);
+                        if (np == 0) pend0 = code; else pend1 = code;
+                        ++np;
+                        ++u;
                     }
                 }
+                while (ok && np > 0) consume();
                 // drain: a last commit completes after every product this thread issued
                 mma_commit(&bars.fin[w]);
                 mbar_wait(&bars.fin[w], 0, drain, kStatusTimeoutDrain, nullptr);
@@ -536,16 +533,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         regs_alloc<kRegsSoftmax>();
         // ------------------------------------------------ softmax groups
+        // Decisions to go on or stop are uniform over the two warps of a lane
+        // quarter within a tile (one bar.red per tile, which also publishes the
+        // half maxima) and over the whole group twice per item (at its start and
+        // before the epilogue); a pair that stops mid-item goes straight to the
+        // second group vote, so every group barrier is reached by all its warps.
         const int wg = warp >> 3;        // query tile of the pair
         const int h = (warp >> 2) & 1;  // half of each row's keys
         const int lq = warp & 3;         // tensor-memory lane quarter
         const int t = lq * 32 + lane;    // row within the query tile
         const int pair_bar = kBarPair0 + wg * 4 + lq;
+        const int group_bar = 1 + wg;
+        const bool leader = (warp & 7) == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
         const uint32_t tG = tmem + wg * 256;
         const uint32_t tOl = tG + lane_off;
-        float *qr_t = sQR + wg * P.nb * 128 + t;
-        float *xch = sXch + wg * 256;  // [2 halves][128 rows]
+        // The group's QR' table [bucket][128 rows] fp32; during the epilogue it
+        // holds the output tile (128 rows x 128 bytes, 128-byte swizzle) for the
+        // TMA store.
+        uint8_t *qr_base = smem + P.off_qr + wg * P.qr_stride;
+        float *qr_t = reinterpret_cast<float *>(qr_base) + t;
+        const uint32_t qr_a = smem_u32(qr_t);
+        const uint32_t stage_row = smem_u32(qr_base) + t * 128;
+        const uint32_t lut_a0 = smem_u32(sLut);
+        float *xch = sXch + wg * 768;  // [max, even tiles | max, odd tiles | sum][2 halves][128 rows]
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
         for (int item = blockIdx.x; item < P.items; item += gridDim.x) {
@@ -556,11 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool warp_active = qt * 128 + lq * 32 < P.N;
             const int ic = i < P.N ? i : P.N - 1;
             const int base_i = (ic / W) * G::COLS + (ic % W) + (P.H - 1) * G::COLS + (W - 1);
+            // the previous item's TMA store has read the staging area (the QR' table)
+            if (leader && it_w > 0) bulk_wait_read_all();
+            bool ok = true;
+            uint32_t slot = u % kSlots;
+            if (HK)
+                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
+                                               kStatusTimeoutMma, &abort_flag));
+            if (!red_and(group_bar, 256, ok)) break;
             if (HK) {
-                const uint32_t slot = u % kSlots;
-                bool ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
-                                                    kStatusTimeoutMma, &abort_flag));
-                if (!group_red_and(wg, ok)) break;
                 tc_fence_after();
                 if (warp_active) {
                     // half 0 copies buckets 0-31, half 1 buckets 32-63
@@ -577,27 +592,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ++u;
             }
             float m = -INFINITY, l = 0.f;
-            bool aborted = false;
             for (int kt = 0; kt < P.nkt; ++kt, ++gw, ++u) {
-                const uint32_t slot = u % kSlots;
-                bool ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
-                                                    kStatusTimeoutMma, &abort_flag));
-                if (!group_red_and(wg, ok)) {
-                    aborted = true;
-                    break;
-                }
+                slot = u % kSlots;
+                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
+                                               kStatusTimeoutMma, &abort_flag)) && ok;
                 tc_fence_after();
                 const uint32_t tSl = tG + kColSlot0 + slot * kSlotCols + lane_off;
-                const uint8_t *lut_t = sLut + (base_i - kt * G::R * G::COLS);
+                const uint32_t lut_a = lut_a0 + static_cast<uint32_t>(base_i - kt * G::R * G::COLS);
                 float mh = -INFINITY;
-                if (warp_active)
-                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lut_t, qr_t, P.c)
-                                : HalfTile<W, HK, 1>::logits(tSl, lut_t, qr_t, P.c);
-                // agree on the tile max with the other half of the row
-                xch[h * 128 + t] = mh;
-                named_bar_sync(pair_bar, 64);
-                const float mt = fmaxf(mh, xch[(h ^ 1) * 128 + t]);
-                named_bar_sync(pair_bar, 64);  // the exchange slots may be reused
+                if (ok && warp_active)
+                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lut_a, qr_a, P.c)
+                                : HalfTile<W, HK, 1>::logits(tSl, lut_a, qr_a, P.c);
+                // agree on the tile max (and on going on) with the other half of the row
+                float *xb = xch + (gw & 1) * 256;
+                xb[h * 128 + t] = mh;
+                ok = red_and(pair_bar, 64, ok);
+                if (!ok) break;
+                const float mt = fmaxf(mh, xb[(h ^ 1) * 128 + t]);
                 if (warp_active) {
                     // lazy rescale: the reference max moves only when it grows by > 2^8
                     float alpha = 1.f;
@@ -607,45 +618,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                         l *= alpha;
                     }
                     if (h == 0 && kt > 0 && __any_sync(~0u, alpha < 1.f))
-                        rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
+                        ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
                     l += h == 0 ? HalfTile<W, HK, 0>::probs(tSl, m) : HalfTile<W, HK, 1>::probs(tSl, m);
                     tmem_st_wait();
                 }
                 tc_fence_before();
                 mbar_arrive(&bars.slot_done[wg][slot]);
             }
-            if (!group_red_and(wg, !aborted)) break;
-            bool ok = __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc, kStatusTimeoutMma,
-                                                &abort_flag));
-            if (!group_red_and(wg, ok)) break;
+            if (ok)
+                ok = __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc, kStatusTimeoutMma,
+                                               &abort_flag));
+            if (!red_and(group_bar, 256, ok)) break;
             tc_fence_after();
-            // each half normalises and stores 32 of the row's 64 output columns
-            xch[h * 128 + t] = l;
+            // each half normalises 32 of the row's 64 output columns into the
+            // staging tile, 16 at a time
+            float *xs = xch + 512;
+            xs[h * 128 + t] = l;
             named_bar_sync(pair_bar, 64);
-            const float inv = 1.f / (l + xch[(h ^ 1) * 128 + t]);
-            named_bar_sync(pair_bar, 64);
-            uint32_t o[32];
-            if (warp_active) {
-                tmem_ld32(tOl + 32 * h, o);
-                tmem_ld_wait();
+            const float inv = 1.f / (l + xs[(h ^ 1) * 128 + t]);
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t o[16];
+                if (warp_active) {
+                    tmem_ld16(tOl + 32 * h + 16 * c2, o);
+                    tmem_ld_wait();
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t *src = o + 8 * c;
+                    const int chunk = 4 * h + 2 * c2 + c;
+                    st_shared_v4(stage_row + ((chunk ^ (t & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv));
+                }
             }
             tc_fence_before();
             mbar_arrive(&bars.o_empty[wg]);
-            if (i < P.N) {
-                uint4 *dst = reinterpret_cast<uint4 *>(P.out + (static_cast<size_t>(I.slice) * P.N + i) * kD + 32 * h);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const uint32_t *src = o + 8 * c;
-                    uint4 v;
-                    v.x = pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv);
-                    v.y = pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv);
-                    v.z = pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv);
-                    v.w = pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv);
-                    dst[c] = v;
-                }
+            fence_proxy_async_smem();
+            named_bar_sync(group_bar, 256);
+            if (leader) {
+                // rows past the grid fall outside the tensor map and are not written
+                tma_store_3d(&tm_o, qr_base, 0, qt * 128, I.slice);
+                bulk_commit_group();
             }
             ++it_w;
         }
+        if (leader) bulk_wait_all();
     }
     tc_fence_before();
     asm volatile("barrier.sync 0;" ::: "memory");
@@ -671,10 +691,9 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.slices = a.B * a.heads;
     p.items = p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
-    p.lut_pad = static_cast<int>(align_up(G::R * G::COLS, 16));
+    p.lut_pad = static_cast<int>(align_up(G::R * G::COLS + 4, 16));
     p.nvalid_last = N - (p.nkt - 1) * G::KT;
     p.lut = a.lut;
-    p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
     const uint32_t cap = 227 * 1024 - 1024;
     uint32_t total = 0;
@@ -691,14 +710,16 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_rk = off;
         if (HK) off += kTileBytes / 2;
         p.off_qr = off;
-        if (HK) off += align_up(2 * p.nb * 512, 1024);
+        // each group's QR' table doubles as its 16 KB output staging tile
+        p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, 128 * 128), 1024);
+        off += 2 * p.qr_stride;
         p.off_lut = off;
-        if (HK) off += p.lut_pad + align_up(p.lut_len, 16);
+        if (HK) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
         off = align_up(off, 1024);
         p.off_mask = off;
         off += 2 * 4096;
         p.off_xch = off;
-        off += 2 * 2 * 128 * 4;
+        off += 2 * 3 * 2 * 128 * 4;
         total = 1024 + off;
         p.nst = nst;
         if (total <= cap) break;
@@ -715,8 +736,9 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const uint32_t tbox[2] = {kD, 64};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-    CUtensorMap tq, tk, tv, trk;
+    CUtensorMap tq, tk, tv, trk, to;
     if (!encode_tensor_map(&tq, bf, 3, a.q, dims, strides, box, sw) ||
+        !encode_tensor_map(&to, bf, 3, a.out, dims, strides, box, sw) ||
         !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box, sw) ||
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box, sw) ||
         !encode_tensor_map(&trk, bf, 2, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
@@ -726,7 +748,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count());
-    rpe_pingpong_kernel<W, HK><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, p);
+    rpe_pingpong_kernel<W, HK><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, to, p);
     return cudaGetLastError();
 }
 
