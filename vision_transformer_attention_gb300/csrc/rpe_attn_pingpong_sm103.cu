@@ -141,7 +141,7 @@ __device__ __noinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_ba
     for (int r = 0; r < 4; ++r) {
         uint32_t o[16];
         tmem_ld16(tO + r * 16, o);
-        tmem_ld_wait();
+        tmem_ld_wait(o);
 #pragma unroll
         for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
         tmem_st16(tO + r * 16, o);
@@ -173,11 +173,11 @@ struct HalfTile {
     static constexpr int first_chunk(int r) { return ((J0 > r * W ? J0 : r * W) - J0) / 16; }
 
     // Pass 1: x = S c + QR'[id] over the half's keys, stored back over the
-    // scores, 16 keys at a time; returns the half's max. lut_a: shared address
-    // of the offset-table byte of the tile's key 0 for this row; qr_a: shared
-    // address of this row's QR' for bucket 0 (buckets 512 bytes apart).
-    static __device__ __forceinline__ float logits(uint32_t tS, uint32_t lut_a, uint32_t qr_a,
-                                                   float c) {
+    // scores, 16 keys at a time; returns the half's max. lutw: the offset
+    // table as words; e0: byte index in it of the tile's key 0 for this row;
+    // qr_t: this row's QR' for bucket 0 (buckets 128 floats apart).
+    static __device__ __forceinline__ float logits(uint32_t tS, const uint32_t *lutw, int e0,
+                                                   const float *qr_t, float c) {
         uint32_t ida[NROWS][NA];
         float mx = -INFINITY;
         const float2 c2 = make_float2(c, c);
@@ -191,13 +191,13 @@ struct HalfTile {
                 for (int rr = 0; rr < NROWS; ++rr) {
                     const int r = ROW_LO + rr;
                     if (first_chunk(r) != q) continue;
-                    const uint32_t lo = lut_a - static_cast<uint32_t>(r * G::COLS + c_hi(r) - 1);
-                    const uint32_t sh = (lo & 3u) * 8u;
-                    const uint32_t wa = lo & ~3u;
+                    const int lo = e0 - (r * G::COLS + c_hi(r) - 1);  // may be negative (padding)
+                    const uint32_t sh = static_cast<uint32_t>(lo & 3) * 8u;
+                    const uint32_t *wp = lutw + (lo >> 2);
                     uint32_t wv[NA + 1];
 #pragma unroll
                     for (int m = 0; m <= NA; ++m)
-                        if (m <= run_words(r)) wv[m] = ld_shared_u32(wa + 4 * m);
+                        if (m <= run_words(r)) wv[m] = wp[m];
 #pragma unroll
                     for (int m = 0; m < NA; ++m)
                         if (m < run_words(r)) ida[rr][m] = __funnelshift_r(wv[m], wv[m + 1], sh);
@@ -208,7 +208,7 @@ struct HalfTile {
                     if (jj < J0 + NK) {
                         const int r = jj / W, k = c_hi(r) - 1 - jj % W;
                         const uint32_t id = __byte_perm(ida[r - ROW_LO][k / 4], 0u, 0x4440u | (k % 4));
-                        qv[j] = ld_shared_f32(qr_a + id * 512u);
+                        qv[j] = qr_t[id * 128];
                     } else {
                         qv[j] = 0.f;
                     }
@@ -219,7 +219,7 @@ struct HalfTile {
             }
             uint32_t s[16];
             tmem_ld16(tS + jc, s);
-            tmem_ld_wait();
+            tmem_ld_wait(s);
             float x[16];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
@@ -251,7 +251,7 @@ struct HalfTile {
             const int jc = J0 + 16 * q;
             uint32_t xs[16];
             tmem_ld16(tS + jc, xs);
-            tmem_ld_wait();
+            tmem_ld_wait(xs);
             float2 p[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
@@ -290,8 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     using G = Geo<W>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned by pointer arithmetic, so the compiler keeps the shared address space
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ PPBars bars;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
@@ -553,9 +553,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // TMA store.
         uint8_t *qr_base = smem + P.off_qr + wg * P.qr_stride;
         float *qr_t = reinterpret_cast<float *>(qr_base) + t;
-        const uint32_t qr_a = smem_u32(qr_t);
         const uint32_t stage_row = smem_u32(qr_base) + t * 128;
-        const uint32_t lut_a0 = smem_u32(sLut);
+        const uint32_t *lutw = reinterpret_cast<const uint32_t *>(sLut);
         float *xch = sXch + wg * 768;  // [max, even tiles | max, odd tiles | sum][2 halves][128 rows]
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
@@ -581,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // half 0 copies buckets 0-31, half 1 buckets 32-63
                     uint32_t r[32];
                     tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off + 32 * h, r);
-                    tmem_ld_wait();
+                    tmem_ld_wait(r);
 #pragma unroll
                     for (int b = 0; b < 32; ++b)
                         if (32 * h + b < P.nb) qr_t[(32 * h + b) * 128] = __uint_as_float(r[b]) * P.c;
@@ -598,11 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                kStatusTimeoutMma, &abort_flag)) && ok;
                 tc_fence_after();
                 const uint32_t tSl = tG + kColSlot0 + slot * kSlotCols + lane_off;
-                const uint32_t lut_a = lut_a0 + static_cast<uint32_t>(base_i - kt * G::R * G::COLS);
+                const int e0 = base_i - kt * G::R * G::COLS;
                 float mh = -INFINITY;
                 if (ok && warp_active)
-                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lut_a, qr_a, P.c)
-                                : HalfTile<W, HK, 1>::logits(tSl, lut_a, qr_a, P.c);
+                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lutw, e0, qr_t, P.c)
+                                : HalfTile<W, HK, 1>::logits(tSl, lutw, e0, qr_t, P.c);
                 // agree on the tile max (and on going on) with the other half of the row
                 float *xb = xch + (gw & 1) * 256;
                 xb[h * 128 + t] = mh;
@@ -641,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t o[16];
                 if (warp_active) {
                     tmem_ld16(tOl + 32 * h + 16 * c2, o);
-                    tmem_ld_wait();
+                    tmem_ld_wait(o);
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {

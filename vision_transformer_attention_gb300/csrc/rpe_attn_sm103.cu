@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(tmem + lane_off + kColQR, r0);
                 tmem_ld32(tmem + lane_off + kColQR + 32, r1);
                 tmem_ld_wait();
+                tmem_ready(r0);
+                tmem_ready(r1);
 #pragma unroll
                 for (int b = 0; b < 64; ++b)
                     if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
@@ -349,6 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_off + kColKR + b * 64, r0);
                     tmem_ld32(tmem + lane_off + kColKR + b * 64 + 32, r1);
                     tmem_ld_wait();
+                    tmem_ready(r0);
+                    tmem_ready(r1);
                     float *kr = sKR + t * kKRStride;
 #pragma unroll
                     for (int bb = 0; bb < 64; ++bb)
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_off + kColS + b * 128 + 32, *reinterpret_cast<uint32_t(*)[32]>(s1));
                     tmem_ld32(tmem + lane_off + kColS + b * 128 + 64, *reinterpret_cast<uint32_t(*)[32]>(s2));
                     tmem_ld32(tmem + lane_off + kColS + b * 128 + 96, *reinterpret_cast<uint32_t(*)[32]>(s3));
-                    tmem_ld_wait();
+                    tmem_ld_wait(s);
                 }
                 tc_fence_before();
                 mbar_arrive(&bars.s_empty[b]);  // S[b] and KR[b] are read
@@ -412,6 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ld32(tmem + lane_off + kColO, o0);
                     tmem_ld32(tmem + lane_off + kColO + 32, o1);
                     tmem_ld_wait();
+                    tmem_ready(o0);
+                    tmem_ready(o1);
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
                         o0[c] = __float_as_uint(__uint_as_float(o0[c]) * alpha);
@@ -480,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tmem + lane_off + kColO, o0);
             tmem_ld32(tmem + lane_off + kColO + 32, o1);
             tmem_ld_wait();
+            tmem_ready(o0);
+            tmem_ready(o1);
             tc_fence_before();
             mbar_arrive(&bars.o_empty);
             if (i < P.N) {

@@ -177,6 +177,8 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             tmem_ld32(taddr, s0);
             tmem_ld32(taddr + 32, s1);
             tmem_ld_wait();
+            tmem_ready(s0);
+            tmem_ready(s1);
             const int h = (unit < units ? unit : 0) % heads;
             const float *bp = bias_s + h * T::kNBPad + bias_base;
             float x[T::kN];
@@ -241,7 +243,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             for (int half = 0; half < D / 32; ++half) {
                 uint32_t o[32];
                 tmem_ld32(tmem + lane_off + half * 32, o);
-                tmem_ld_wait();
+                tmem_ld_wait(o);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int chunk = half * 4 + c;
