@@ -14,32 +14,35 @@
 //     warps: the two warps that share a tensor-memory lane quarter split each
 //     row's keys in halves, so four warps per SM sub-partition hide one
 //     another's latencies.
-//   * Each group has its own MMA-issuing warp (one thread issuing tcgen05.mma
-//     back to back is limited to roughly one instruction per 100 cycles; two
-//     issuers nearly double the tensor core's intake) and its own ring of two
-//     tensor-memory slots. A "unit" is either QR = Q R^K^T (once per item) or
-//     one tile's scores; unit u goes into slot u mod 2 once unit u-2 has been
-//     consumed (its QR copied out, or its P V issued). Each issuer is an event
-//     loop: it issues a P V the moment its probabilities are ready and the next
-//     unit the moment its inputs have landed.
+//   * Each group has its own MMA-issuing warp (a single thread pushing small
+//     tcgen05.mma instructions manages about one per 60-130 cycles; two
+//     issuers nearly double the tensor core's intake) and its own ring of
+//     SLOTS tensor-memory slots. A "unit" is either QR = Q R^K^T (once per
+//     item) or one tile's scores; unit u goes into slot u mod SLOTS once unit
+//     u - SLOTS has been consumed (its QR copied out, or its P V issued). The
+//     issuer is a straight sequence of bounded blocking waits.
 //   * Per tile, each half computes its logits x = S c + QR'[id] (log2 units),
 //     writes them back over its scores, and reports its maximum; the two
-//     halves agree on the tile maximum through shared memory. The reference
-//     max m of a row moves only when a tile's max exceeds it by more than 2^8,
-//     in which case O (earlier tiles) is rescaled. Then each half writes its
-//     probabilities as bf16 pairs over its own logits, where the P V product
-//     reads its A operand.
-//   * Key tiles hold whole grid rows (84 keys for W = 14, 56 for W = 56, so
-//     that two score slots and O fit each group's 256 tensor-memory columns);
-//     the offset-table position of key jj of a tile is then a compile-time
-//     constant and each score's bucket id is one shared-memory byte load at an
-//     immediate offset. Keys past the grid (last tile only) get -9984 added by
-//     one extra K = 16 product, so the softmax never tests for them.
+//     halves agree on the tile maximum (and on going on) with one bar.red per
+//     lane quarter. The reference max m of a row moves only when a tile's max
+//     exceeds it by more than 2^8, in which case O (earlier tiles) is
+//     rescaled. Then each half writes its probabilities as bf16 pairs over its
+//     own logits, where the P V product reads its A operand.
+//   * Key tiles hold whole grid rows: 84 keys (NS = 96 columns) for W = 14,
+//     56 keys (NS = 64) for W = 56. The offset-table
+//     bytes of one grid row of keys are contiguous, so a row's bucket ids are
+//     read as a few aligned words and taken out with byte permutes. Keys past
+//     the grid (last tile only) get -9984 added by one extra K = 16 product,
+//     so the softmax never tests for them. K/V are loaded as KT-row boxes into
+//     NS-row buffers whose last NS - KT rows stay zero.
+//   * The epilogue stages the bf16 output tile in the group's QR' table (not
+//     needed until the next item) with a 128-byte swizzle and writes it with
+//     one TMA store; rows past the grid fall outside the tensor map.
 //
 // Warps 0-7: group 0 (warp 4h + q: half h, lane quarter q); 8-15: group 1;
 // warpgroup 4 (warps 16-19): 16 TMA producer, 17 and 18 MMA issuers of groups
 // 0 and 1, 19 idle. Tensor memory (512 columns): group w owns [256w, 256w+256):
-// O at +0 (64 columns), slots at +64 and +160 (NS <= 96 columns each).
+// O at +0 (64 columns), slot s at +64 + s NS.
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -60,10 +63,9 @@ constexpr int kRegsControl = 64;
 constexpr int kRegsSoftmax = 104;
 static_assert(128 * kRegsControl + 512 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kMaxStages = 3;
-constexpr int kSlots = 2;          // score slots per group
+constexpr int kMaxStages = 8;
+constexpr int kMaxSlots = 3;       // score slots per group (see Geo::SLOTS)
 constexpr uint32_t kColSlot0 = 64;  // within the group's 256 columns
-constexpr uint32_t kSlotCols = 96;
 constexpr int kBarPair0 = 3;  // named barriers 3..10: the two warps of a lane quarter
 
 template <int W>
@@ -73,6 +75,14 @@ struct Geo {
     static constexpr int NS = (KT + 15) / 16 * 16;  // N of QK^T, K of PV
     static constexpr int HS = NS / 2 / 16 * 16 + ((NS / 2) % 16 ? 16 : 0);  // keys per half
     static constexpr int COLS = 2 * W - 1;          // offset-table row length
+    // one K or V buffer: the tile's KT rows (loaded) and NS - KT rows that stay
+    // zero (the products read NS rows)
+    static constexpr int KV_BYTES = NS * 128;
+    // score slots of NS columns after O's 64 in the group's 256 (a third slot
+    // where it fits, W = 56, measured slower: the tensor core, not the
+    // prefetch depth, limits there)
+    static constexpr int SLOTS = 2;
+    static_assert(SLOTS >= 2 && SLOTS <= kMaxSlots, "slots");
     static_assert(NS <= 96 && HS % 16 == 0 && 2 * HS >= NS, "tile geometry");
 };
 
@@ -90,7 +100,7 @@ struct PPBars {
     uint64_t tab_full;
     uint64_t q_full[2], q_empty[2];
     uint64_t kv_full[kMaxStages], kv_empty[kMaxStages];
-    uint64_t slot_full[2][kSlots], slot_done[2][kSlots];
+    uint64_t slot_full[2][kMaxSlots], slot_done[2][kMaxSlots];
     uint64_t o_full[2], o_empty[2], pv_done[2];
     uint64_t fin[2];   // drain of each issuer
 };
@@ -100,7 +110,10 @@ struct Item {
     bool has_b;
 };
 
-// Full pairs of query tiles first (slice-major), then the odd last tiles.
+// Items: full pairs of query tiles (slice-major), then the odd last tiles,
+// dealt round-robin over the CTAs (an odd tile takes about as long as a pair:
+// the two groups of a pair run side by side). item_at(P, k) is the k-th item
+// of this CTA, -1 past its last; every role walks the same sequence.
 __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
     Item r;
     const int nfull = P.slices * P.pairs_full;
@@ -114,6 +127,11 @@ __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
         r.has_b = false;
     }
     return r;
+}
+
+__device__ __forceinline__ int item_at(const PPParams &P, int k) {
+    const int item = blockIdx.x + k * gridDim.x;
+    return item < P.items ? item : -1;
 }
 
 // AND-reduction of v over the nthreads threads that use named barrier id.
@@ -303,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const WaitCtl drain{wc.status, kDefaultWaitNs};
 
     uint8_t *sQ = smem + P.off_q;    // nq buffers of two query tiles
-    uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s tiles, V at 2s + 1
+    uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s buffers, V at 2s + 1
     uint8_t *sRK = smem + P.off_rk;
     uint8_t *sLut = smem + P.off_lut + P.lut_pad;
     float *sXch = reinterpret_cast<float *>(smem + P.off_xch);  // [2 groups][3][2 halves][128]
@@ -317,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.o_empty[i], 256);
             mbar_init(&bars.pv_done[i], 1);
             mbar_init(&bars.fin[i], 1);
-            for (int s = 0; s < kSlots; ++s) {
+            for (int s = 0; s < kMaxSlots; ++s) {
                 mbar_init(&bars.slot_full[i][s], 1);
                 mbar_init(&bars.slot_done[i][s], 256);
             }
@@ -340,6 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
         }
     }
+    // K/V buffers: rows KT..NS-1 are never loaded and must hold finite values
+    for (int e = tid; e < P.nst * 2 * G::KV_BYTES / 16; e += kThreads)
+        st_shared_v4(smem_u32(sKV) + e * 16, 0u, 0u, 0u, 0u);
     // Masking operands for the last key tile (128 rows x 16 bf16, K-major, 32-byte
     // swizzle): A has -9984 in column 0 of every row, B has 1 in column 0 of
     // every key row past the grid, so A B^T adds -9984 to exactly those scores.
@@ -374,9 +395,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 int g = 0, it = 0;
                 int last_q[2] = {-1, -1};
-                int last_use[kMaxStages] = {-1, -1, -1};
+                int last_use[kMaxStages];
+                for (int st = 0; st < kMaxStages; ++st) last_use[st] = -1;
                 bool ok = true;
-                for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++it) {
+                for (int item = item_at(P, 0); ok && item >= 0; item = item_at(P, ++it)) {
                     const Item I = decode_item(P, item);
                     const int qb = it % P.nq, quse = it / P.nq;
                     if (!(ok = mbar_wait(&bars.q_empty[qb], (quse & 1) ^ 1, wc, kStatusTimeoutSync,
@@ -394,10 +416,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (!(ok = mbar_wait(&bars.kv_empty[st], (use & 1) ^ 1, wc,
                                              kStatusTimeoutSync, &abort_flag)))
                             break;
-                        uint8_t *kb = sKV + st * 2 * kTileBytes;
-                        mbar_arrive_expect_tx(&bars.kv_full[st], 2 * kTileBytes);
+                        uint8_t *kb = sKV + st * 2 * G::KV_BYTES;
+                        mbar_arrive_expect_tx(&bars.kv_full[st], 2 * G::KT * 128);
                         tma_load_3d(kb, &tm_k, &bars.kv_full[st], 0, kt * G::KT, I.slice);
-                        tma_load_3d(kb + kTileBytes, &tm_v, &bars.kv_full[st], 0, kt * G::KT,
+                        tma_load_3d(kb + G::KV_BYTES, &tm_v, &bars.kv_full[st], 0, kt * G::KT,
                                     I.slice);
                         last_use[st] = use;
                     }
@@ -415,8 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         } else if (warp == 17 || warp == 18) {
             // -------------------------------------------- MMA issuer of group w
-            // With two slots the order is fixed: unit u is issued once unit u - 2
-            // has been consumed (and, for a tile's scores, its P V issued), so
+            // The order is fixed: unit u is issued once unit u - SLOTS has been
+            // consumed (and, for a tile's scores, its P V issued), so
             // the issuer is a straight sequence of bounded blocking waits. For
             // items the group sits out it still releases the item's Q buffer and
             // K/V stages, each after the matching load has landed.
@@ -431,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t aKV = smem_u32(sKV);
                 // outstanding units, oldest first: bits 0-3 stage, 4 QR unit, 5 first
                 // tile of the item, 6 last tile of the item
-                uint32_t pend0 = 0, pend1 = 0;
+                uint32_t pend0 = 0, pend1 = 0, pend2 = 0;
                 int np = 0;
                 uint32_t u = 0;  // units issued
                 int ci = 0;      // items whose last P V was issued
@@ -443,8 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t x = pend0;
                     const uint32_t cu = u - np;
                     pend0 = pend1;
+                    pend1 = pend2;
                     --np;
-                    ok = ok && mbar_wait(&bars.slot_done[w][cu % kSlots], (cu / kSlots) & 1, wc,
+                    ok = ok && mbar_wait(&bars.slot_done[w][cu % G::SLOTS], (cu / G::SLOTS) & 1, wc,
                                          kStatusTimeoutSync, &abort_flag);
                     if (!ok || (x & 0x10u)) return;
                     if (x & 0x20u)
@@ -452,8 +475,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!ok) return;
                     tc_fence_after();
                     const int st = x & 0xF;
-                    const uint64_t dV = hi128 | ((aKV + (st * 2 + 1) * kTileBytes) >> 4);
-                    const uint32_t aP = tG + kColSlot0 + (cu % kSlots) * kSlotCols;
+                    const uint64_t dV = hi128 | ((aKV + (st * 2 + 1) * G::KV_BYTES) >> 4);
+                    const uint32_t aP = tG + kColSlot0 + (cu % G::SLOTS) * G::NS;
                     const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
 #pragma unroll
                     for (int kk = 0; kk < G::NS / 16; ++kk)
@@ -467,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 };
                 int g = 0, it = 0;
-                for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++it) {
+                for (int item = item_at(P, 0); ok && item >= 0; item = item_at(P, ++it)) {
                     const Item I = decode_item(P, item);
                     const int qb = it % P.nq;
                     ok = mbar_wait(&bars.q_full[qb], (it / P.nq) & 1, wc, kStatusTimeoutLoad, &abort_flag);
@@ -486,10 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint64_t dQ = hi128 | ((aQ + qb * 2 * kTileBytes) >> 4);
                     for (int kt = HK ? -1 : 0; ok && kt < P.nkt; ++kt) {
-                        if (np == kSlots) consume();
+                        if (np == G::SLOTS) consume();
                         if (!ok) break;
-                        const uint32_t slot = u % kSlots;
-                        const uint32_t dS = tG + kColSlot0 + slot * kSlotCols;
+                        const uint32_t slot = u % G::SLOTS;
+                        const uint32_t dS = tG + kColSlot0 + slot * G::NS;
                         uint32_t code;
                         if (kt < 0) {
                             tc_fence_after();
@@ -504,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            &abort_flag);
                             if (!ok) break;
                             tc_fence_after();
-                            const uint64_t dK = hi128 | ((aKV + st * 2 * kTileBytes) >> 4);
+                            const uint64_t dK = hi128 | ((aKV + st * 2 * G::KV_BYTES) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 mma_bf16_ss(dS, dQ + kk * 2, dK + kk * 2, kIdS, kk > 0);
@@ -518,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         mma_commit(&bars.slot_full[w][slot]);
                         if (kt == P.nkt - 1) mma_commit(&bars.q_empty[qb]);
-                        if (np == 0) pend0 = code; else pend1 = code;
+                        if (np == 0) pend0 = code; else if (np == 1) pend1 = code; else pend2 = code;
                         ++np;
                         ++u;
                     }
@@ -558,7 +581,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *xch = sXch + wg * 768;  // [max, even tiles | max, odd tiles | sum][2 halves][128 rows]
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
-        for (int item = blockIdx.x; item < P.items; item += gridDim.x) {
+        int k_item = 0;
+        for (int item = item_at(P, 0); item >= 0; item = item_at(P, ++k_item)) {
             const Item I = decode_item(P, item);
             if (wg == 1 && !I.has_b) continue;
             const int qt = I.qt0 + wg;
@@ -569,9 +593,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the previous item's TMA store has read the staging area (the QR' table)
             if (leader && it_w > 0) bulk_wait_read_all();
             bool ok = true;
-            uint32_t slot = u % kSlots;
+            uint32_t slot = u % G::SLOTS;
             if (HK)
-                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
+                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag));
             if (!red_and(group_bar, 256, ok)) break;
             if (HK) {
@@ -579,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (warp_active) {
                     // half 0 copies buckets 0-31, half 1 buckets 32-63
                     uint32_t r[32];
-                    tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off + 32 * h, r);
+                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32 * h, r);
                     tmem_ld_wait(r);
 #pragma unroll
                     for (int b = 0; b < 32; ++b)
@@ -592,11 +616,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             float m = -INFINITY, l = 0.f;
             for (int kt = 0; kt < P.nkt; ++kt, ++gw, ++u) {
-                slot = u % kSlots;
-                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / kSlots) & 1, wc,
+                slot = u % G::SLOTS;
+                ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag)) && ok;
                 tc_fence_after();
-                const uint32_t tSl = tG + kColSlot0 + slot * kSlotCols + lane_off;
+                const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
                 float mh = -INFINITY;
                 if (ok && warp_active)
@@ -696,33 +720,34 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
     const uint32_t cap = 227 * 1024 - 1024;
     uint32_t total = 0;
-    // prefer three K/V stages, then a double-buffered Q
-    const int choices[4][2] = {{3, 2}, {3, 1}, {2, 2}, {2, 1}};
-    for (const auto &ch : choices) {
-        const int nst = ch[0];
-        p.nq = ch[1];
+    // as many K/V stages as fit (up to kMaxStages) next to a double-buffered Q;
+    // a single Q buffer only when that leaves fewer than three stages
+    for (int nq = 2; nq >= 1; --nq) {
+        p.nq = nq;
         uint32_t off = 0;
         p.off_q = off;
-        off += p.nq * 2 * kTileBytes;
-        p.off_kv = off;
-        off += nst * 2 * kTileBytes;
+        off += nq * 2 * kTileBytes;
         p.off_rk = off;
         if (HK) off += kTileBytes / 2;
         p.off_qr = off;
         // each group's QR' table doubles as its 16 KB output staging tile
         p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, 128 * 128), 1024);
         off += 2 * p.qr_stride;
-        p.off_lut = off;
-        if (HK) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
-        off = align_up(off, 1024);
         p.off_mask = off;
         off += 2 * 4096;
         p.off_xch = off;
         off += 2 * 3 * 2 * 128 * 4;
-        total = 1024 + off;
-        p.nst = nst;
-        if (total <= cap) break;
+        p.off_lut = off;
+        if (HK) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
+        off = align_up(off, 1024);
+        p.off_kv = off;
+        const int room = static_cast<int>((cap - std::min(cap, 1024 + off)) / (2 * G::KV_BYTES));
+        p.nst = std::min(room, kMaxStages);
+        total = 1024 + off + p.nst * 2 * G::KV_BYTES;
+        if (p.nst >= 3 || (nq == 1 && p.nst >= 2)) break;
     }
+    // an issuer waiting for tile t's K/V holds up to SLOTS - 1 earlier tiles
+    if (p.nst < G::SLOTS) return cudaErrorInvalidValue;
     if (total > cap) return cudaErrorInvalidValue;
     unsigned *status = device_status_word();
     if (status == nullptr) return cudaErrorMemoryAllocation;
@@ -730,6 +755,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const uint64_t dims[3] = {kD, static_cast<uint64_t>(N), static_cast<uint64_t>(p.slices)};
     const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(N) * kD * 2};
     const uint32_t box[3] = {kD, 128, 1};
+    const uint32_t box_kv[3] = {kD, static_cast<uint32_t>(G::KT), 1};  // one key tile
     const uint64_t tdims[2] = {kD, static_cast<uint64_t>(a.num_buckets)};
     const uint64_t tstrides[1] = {kD * 2};
     const uint32_t tbox[2] = {kD, 64};
@@ -738,8 +764,8 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     CUtensorMap tq, tk, tv, trk, to;
     if (!encode_tensor_map(&tq, bf, 3, a.q, dims, strides, box, sw) ||
         !encode_tensor_map(&to, bf, 3, a.out, dims, strides, box, sw) ||
-        !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box, sw) ||
-        !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box, sw) ||
+        !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box_kv, sw) ||
+        !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 2, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK>,
