@@ -16,14 +16,17 @@
 // thread per row reads its half from TMEM, adds the bias from a shared-memory
 // copy of the table (the per-key offset is a compile-time immediate because
 // M is a template parameter), takes the softmax in base 2 and writes bf16
-// probabilities into the K-major P operand; the cross-unit half of P stays
-// zero, so a single M=128, N=d, K=128 MMA gives P V. The epilogue scales by
-// 1/rowsum, converts to bf16 and leaves through a TMA store that drops the
-// padding rows. No n x n bias is ever formed in global memory.
+// probabilities back into tensor memory over the scores, as the A operand of
+// P V: columns [32 s, 32 s + 32) hold slot s's keys in pairs, the other 32
+// columns of the row are zero, so a single M=128, N=d, K=128 MMA gives P V,
+// written to columns [64, 64 + d) (scores no longer needed). The epilogue
+// scales by 1/rowsum, converts to bf16 and leaves through a TMA store that
+// drops the padding rows. No n x n bias is ever formed in global memory.
 //
 // The kernel is persistent (grid = a multiple of the SM count), double-
-// buffers Q/K/V so the next tile's loads overlap this tile's work, and runs
-// two CTAs per SM at d = 32 so one CTA's softmax overlaps the other's copies.
+// buffers Q/K/V so the next tile's loads overlap this tile's work, and uses
+// 128 tensor-memory columns and about 60 KB of shared memory per CTA, so
+// three CTAs share an SM at d = 32 and overlap one another's latencies.
 #include "rpe_attn.h"
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
@@ -44,14 +47,13 @@ struct SwinTile {
     static constexpr int kSbo = 8 * kRowBytes;  // stride between 8-row groups
     static constexpr int kOperBytes = 128 * kRowBytes;
     static constexpr int kStageBytes = 3 * kOperBytes;
-    static constexpr int kPBlockBytes = 128 * 128;  // [128 rows][64 keys] bf16
-    static constexpr int kPBytes = 2 * kPBlockBytes;
     static constexpr int kNB = (2 * M - 1) * (2 * M - 1);
     static constexpr int kNBPad = (kNB + 3) & ~3;
     static constexpr int kMaxHeads = 32;
-    static constexpr int kSmemFixed = 1024 + 2 * kStageBytes + kPBytes + kOperBytes;
+    static constexpr int kSmemFixed = 1024 + 2 * kStageBytes + kOperBytes;
     static int smem_bytes(int heads) { return kSmemFixed + heads * kNBPad * 4; }
-    static constexpr int kCtasPerSm = (D == 32) ? 2 : 1;
+    static constexpr int kCtasPerSm = (D == 32) ? 3 : 1;
+    static constexpr uint32_t kColO = 64;  // O after P V (scores dead by then)
     static_assert(kN <= 64, "a window must fit one 64-row slot");
 };
 
@@ -67,8 +69,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stage_base = smem;
-    uint8_t *p_base = smem + 2 * T::kStageBytes;
-    uint8_t *o_stage = p_base + T::kPBytes;
+    uint8_t *o_stage = smem + 2 * T::kStageBytes;
     float *bias_s = reinterpret_cast<float *>(o_stage + T::kOperBytes);
 
     __shared__ __align__(8) uint64_t bar_load[2];
@@ -99,11 +100,6 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         const int h = e / T::kNB, b = e % T::kNB;
         bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * heads + h) * kLog2e;
     }
-    // P starts all zero; each thread later rewrites only its own unit's half,
-    // so the cross-unit half stays zero for the whole kernel.
-    for (int e = tid; e < T::kPBytes / 16; e += blockDim.x)
-        st_shared_v4(smem_u32(p_base) + e * 16, 0u, 0u, 0u, 0u);
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -136,7 +132,6 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     const int rr = (r < T::kN) ? r : 0;
     const int bias_base = (rr / M) * (2 * M - 1) + (rr % M) + (M - 1) * (2 * M - 1) + (M - 1);
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t prow = smem_u32(p_base) + slot * T::kPBlockBytes + tid * 128;
 
     int it = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++it) {
@@ -198,18 +193,20 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
                 sum += x[j];
             }
             l = sum;
+            // P over the scores: this slot's 32 columns, then 32 zero columns
+            // for the other slot's keys (read above, not needed any more)
+            uint32_t w[32], z[32];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j0 = c * 8 + 2 * e;
-                    const float a = (row_ok && j0 < T::kN) ? x[j0 < T::kN ? j0 : 0] : 0.f;
-                    const float b = (row_ok && j0 + 1 < T::kN) ? x[j0 + 1 < T::kN ? j0 + 1 : 0] : 0.f;
-                    w[e] = pack_bf16x2(a, b);
-                }
-                st_shared_v4(prow + ((c ^ (tid & 7)) << 4), w[0], w[1], w[2], w[3]);
+            for (int c = 0; c < 32; ++c) {
+                const int j0 = 2 * c;
+                const float a = (row_ok && j0 < T::kN) ? x[j0 < T::kN ? j0 : 0] : 0.f;
+                const float b = (row_ok && j0 + 1 < T::kN) ? x[j0 + 1 < T::kN ? j0 + 1 : 0] : 0.f;
+                w[c] = pack_bf16x2(a, b);
+                z[c] = 0u;
             }
+            tmem_st32(tmem + lane_off + slot * 32, w);
+            tmem_st32(tmem + lane_off + (slot ^ 1) * 32, z);
+            tmem_st_wait();
         }
         if (tid == 0) bulk_wait_read_all();  // the staging buffer is free again
         fence_proxy_async_smem();
@@ -221,12 +218,9 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t a = smem_desc(
-                    smem_u32(p_base) + (kk >> 2) * T::kPBlockBytes + (kk & 3) * 32, 16, 1024,
-                    kSwizzle128B);
                 const uint64_t b = smem_desc(
                     smem_u32(sb + 2 * T::kOperBytes) + kk * 16 * T::kRowBytes, 16, T::kSbo, T::kSwz);
-                mma_bf16_ss(tmem, a, b, kIdescO, kk > 0 ? 1u : 0u);
+                mma_bf16_ts(tmem + T::kColO, tmem + kk * 8, b, kIdescO, kk > 0 ? 1u : 0u);
             }
             mma_commit(&bar_o);
             mma_bar_pending = &bar_o;
@@ -242,7 +236,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
 #pragma unroll
             for (int half = 0; half < D / 32; ++half) {
                 uint32_t o[32];
-                tmem_ld32(tmem + lane_off + half * 32, o);
+                tmem_ld32(tmem + lane_off + T::kColO + half * 32, o);
                 tmem_ld_wait(o);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
