@@ -24,9 +24,10 @@
 // drops the padding rows. No n x n bias is ever formed in global memory.
 //
 // The kernel is persistent (grid = a multiple of the SM count), double-
-// buffers Q/K/V so the next tile's loads overlap this tile's work, and uses
-// 128 tensor-memory columns and about 60 KB of shared memory per CTA, so
-// three CTAs share an SM at d = 32 and overlap one another's latencies.
+// buffers Q/K/V so the next tile's loads overlap this tile's work, stages
+// the output tile in the Q buffer it no longer needs, and uses 128
+// tensor-memory columns and about 50 KB of shared memory per CTA at d = 32
+// (four CTAs per SM, overlapping one another's latencies; two at d = 64).
 #include "rpe_attn.h"
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
@@ -50,9 +51,9 @@ struct SwinTile {
     static constexpr int kNB = (2 * M - 1) * (2 * M - 1);
     static constexpr int kNBPad = (kNB + 3) & ~3;
     static constexpr int kMaxHeads = 32;
-    static constexpr int kSmemFixed = 1024 + 2 * kStageBytes + kOperBytes;
+    static constexpr int kSmemFixed = 1024 + 2 * kStageBytes;
     static int smem_bytes(int heads) { return kSmemFixed + heads * kNBPad * 4; }
-    static constexpr int kCtasPerSm = (D == 32) ? 3 : 1;
+    static constexpr int kCtasPerSm = (D == 32) ? 4 : 2;
     static constexpr uint32_t kColO = 64;  // O after P V (scores dead by then)
     static_assert(kN <= 64, "a window must fit one 64-row slot");
 };
@@ -69,8 +70,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stage_base = smem;
-    uint8_t *o_stage = smem + 2 * T::kStageBytes;
-    float *bias_s = reinterpret_cast<float *>(o_stage + T::kOperBytes);
+    float *bias_s = reinterpret_cast<float *>(smem + 2 * T::kStageBytes);
 
     __shared__ __align__(8) uint64_t bar_load[2];
     __shared__ __align__(8) uint64_t bar_s;
@@ -141,7 +141,12 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         // ---- thread 0: prefetch the next tile, then S = Q K^T for this one
         if (tid == 0 && !abort_flag) {
             const int next = tile + gridDim.x;
-            if (next < tiles) issue_load(next, stage ^ 1);
+            // the other stage's Q buffer staged the previous tile's output:
+            // its TMA store must have read it before the next load lands there
+            if (next < tiles) {
+                bulk_wait_read_all();
+                issue_load(next, stage ^ 1);
+            }
             if (mbar_wait(&bar_load[stage], load_uses[stage] & 1, wc, kStatusTimeoutLoad,
                           &abort_flag)) {
                 loads_pending &= ~(1u << stage);
@@ -208,7 +213,6 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             tmem_st32(tmem + lane_off + (slot ^ 1) * 32, z);
             tmem_st_wait();
         }
-        if (tid == 0) bulk_wait_read_all();  // the staging buffer is free again
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -232,7 +236,9 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             if (tid == 0) mma_bar_pending = nullptr;
             tc_fence_after();
             const float inv = row_ok ? 1.f / l : 0.f;
-            const uint32_t orow = smem_u32(o_stage) + tid * T::kRowBytes;
+            // the output tile is staged in this stage's Q buffer (Q is dead
+            // once S is formed)
+            const uint32_t orow = smem_u32(sb) + tid * T::kRowBytes;
 #pragma unroll
             for (int half = 0; half < D / 32; ++half) {
                 uint32_t o[32];
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         const int aborted = __syncthreads_or(abort_flag);
         if (aborted) break;
         if (tid == 0) {
-            tma_store_3d(&tm_o, o_stage, 0, 0, 2 * tile);
+            tma_store_3d(&tm_o, sb, 0, 0, 2 * tile);
             bulk_commit_group();
         }
     }
