@@ -55,25 +55,24 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kD = 64;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-column bf16 tile
-constexpr int kThreads = 640;
-// Register split (launch: 640 threads x 96 = 61,440): control warpgroup 64,
-// softmax warps 104 -> 128 x 64 + 512 x 104 = 61,440.
-constexpr int kRegsLaunch = 96;
+constexpr int kThreads = 384;
+// Register split (launch: 384 threads x 168 = 64,512): control warpgroup 64,
+// softmax warps 216 -> 128 x 64 + 256 x 216 = 63,488.
+constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 64;
-constexpr int kRegsSoftmax = 104;
-static_assert(128 * kRegsControl + 512 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 3;       // score slots per group (see Geo::SLOTS)
 constexpr uint32_t kColSlot0 = 64;  // within the group's 256 columns
-constexpr int kBarPair0 = 3;  // named barriers 3..10: the two warps of a lane quarter
 
 template <int W>
 struct Geo {
     static constexpr int R = 96 / W;                // grid rows per key tile
     static constexpr int KT = R * W;                // keys per tile
     static constexpr int NS = (KT + 15) / 16 * 16;  // N of QK^T, K of PV
-    static constexpr int HS = NS / 2 / 16 * 16 + ((NS / 2) % 16 ? 16 : 0);  // keys per half
+    static constexpr int HS = NS;  // keys per thread and tile (one thread owns a row)
     static constexpr int COLS = 2 * W - 1;          // offset-table row length
     // one K or V buffer: the tile's KT rows (loaded) and NS - KT rows that stay
     // zero (the products read NS rows)
@@ -88,7 +87,7 @@ struct Geo {
 
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
-    uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask, off_xch;
+    uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
     const int32_t *lut;
@@ -324,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *sKV = smem + P.off_kv;  // stage s: K at 2s buffers, V at 2s + 1
     uint8_t *sRK = smem + P.off_rk;
     uint8_t *sLut = smem + P.off_lut + P.lut_pad;
-    float *sXch = reinterpret_cast<float *>(smem + P.off_xch);  // [2 groups][3][2 halves][128]
 
     if (tid == 0) {
         mbar_init(&bars.tab_full, 1);
@@ -332,12 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars.q_full[i], 1);
             mbar_init(&bars.q_empty[i], 2);  // one arrival per group issuer
             mbar_init(&bars.o_full[i], 1);
-            mbar_init(&bars.o_empty[i], 256);
+            mbar_init(&bars.o_empty[i], 128);
             mbar_init(&bars.pv_done[i], 1);
             mbar_init(&bars.fin[i], 1);
             for (int s = 0; s < kMaxSlots; ++s) {
                 mbar_init(&bars.slot_full[i][s], 1);
-                mbar_init(&bars.slot_done[i][s], 256);
+                mbar_init(&bars.slot_done[i][s], 128);
             }
         }
         for (int i = 0; i < kMaxStages; ++i) {
@@ -381,9 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp >= 16) {
+    if (warp >= 8) {
         regs_dealloc<kRegsControl>();
-        if (warp == 16) {
+        if (warp == 8) {
             // -------------------------------------------- TMA producer
             if (lane == 0) {
                 prefetch_tmap(&tm_q);
@@ -435,14 +433,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   nullptr);
             }
             __syncwarp();
-        } else if (warp == 17 || warp == 18) {
+        } else if (warp == 9 || warp == 10) {
             // -------------------------------------------- MMA issuer of group w
             // The order is fixed: unit u is issued once unit u - SLOTS has been
             // consumed (and, for a tile's scores, its P V issued), so
             // the issuer is a straight sequence of bounded blocking waits. For
             // items the group sits out it still releases the item's Q buffer and
             // K/V stages, each after the matching load has landed.
-            const int w = warp - 17;
+            const int w = warp - 9;
             if (lane == 0) {
                 constexpr uint32_t kIdS = idesc_bf16(128, G::NS, false, false);
                 constexpr uint32_t kIdQR = idesc_bf16(128, 64, false, false);
@@ -556,33 +554,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         regs_alloc<kRegsSoftmax>();
         // ------------------------------------------------ softmax groups
-        // Decisions to go on or stop are uniform over the two warps of a lane
-        // quarter within a tile (one bar.red per tile, which also publishes the
-        // half maxima) and over the whole group twice per item (at its start and
-        // before the epilogue); a pair that stops mid-item goes straight to the
-        // second group vote, so every group barrier is reached by all its warps.
-        const int wg = warp >> 3;        // query tile of the pair
-        const int h = (warp >> 2) & 1;  // half of each row's keys
+        // One thread per query row. Decisions to go on or stop are uniform per
+        // warp within an item and over the whole group twice per item (at its
+        // start and before the epilogue); a warp that stops mid-item goes
+        // straight to the second group vote, so every group barrier is reached
+        // by all of the group's warps.
+        const int wg = warp >> 2;        // query tile of the pair
         const int lq = warp & 3;         // tensor-memory lane quarter
         const int t = lq * 32 + lane;    // row within the query tile
-        const int pair_bar = kBarPair0 + wg * 4 + lq;
         const int group_bar = 1 + wg;
-        const bool leader = (warp & 7) == 0 && lane == 0;
+        const bool leader = lq == 0 && lane == 0;
         const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
         const uint32_t tG = tmem + wg * 256;
         const uint32_t tOl = tG + lane_off;
         // The group's QR' table [bucket][128 rows] fp32; during the epilogue it
         // holds the output tile (128 rows x 128 bytes, 128-byte swizzle) for the
-        // TMA store.
+        // TMA store. A thread reads and writes only its own row of it.
         uint8_t *qr_base = smem + P.off_qr + wg * P.qr_stride;
         float *qr_t = reinterpret_cast<float *>(qr_base) + t;
         const uint32_t stage_row = smem_u32(qr_base) + t * 128;
         const uint32_t *lutw = reinterpret_cast<const uint32_t *>(sLut);
-        float *xch = sXch + wg * 768;  // [max, even tiles | max, odd tiles | sum][2 halves][128 rows]
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
-        int k_item = 0;
-        for (int item = item_at(P, 0); item >= 0; item = item_at(P, ++k_item)) {
+        for (int item = item_at(P, 0), k_item = 0; item >= 0; item = item_at(P, ++k_item)) {
             const Item I = decode_item(P, item);
             if (wg == 1 && !I.has_b) continue;
             const int qt = I.qt0 + wg;
@@ -597,21 +591,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (HK)
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag));
-            if (!red_and(group_bar, 256, ok)) break;
+            if (!red_and(group_bar, 128, ok)) break;
             if (HK) {
                 tc_fence_after();
                 if (warp_active) {
-                    // half 0 copies buckets 0-31, half 1 buckets 32-63
-                    uint32_t r[32];
-                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32 * h, r);
-                    tmem_ld_wait(r);
+                    uint32_t r0[32], r1[32];
+                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off, r0);
+                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32, r1);
+                    tmem_ld_wait();
+                    tmem_ready(r0);
+                    tmem_ready(r1);
 #pragma unroll
-                    for (int b = 0; b < 32; ++b)
-                        if (32 * h + b < P.nb) qr_t[(32 * h + b) * 128] = __uint_as_float(r[b]) * P.c;
+                    for (int b = 0; b < 64; ++b)
+                        if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b] : r1[b - 32]) * P.c;
                 }
                 tc_fence_before();
                 mbar_arrive(&bars.slot_done[wg][slot]);
-                named_bar_sync(pair_bar, 64);  // both halves of the row's QR' are in place
                 ++u;
             }
             float m = -INFINITY, l = 0.f;
@@ -619,20 +614,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 slot = u % G::SLOTS;
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag)) && ok;
+                if (!ok) break;
                 tc_fence_after();
                 const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
-                float mh = -INFINITY;
-                if (ok && warp_active)
-                    mh = h == 0 ? HalfTile<W, HK, 0>::logits(tSl, lutw, e0, qr_t, P.c)
-                                : HalfTile<W, HK, 1>::logits(tSl, lutw, e0, qr_t, P.c);
-                // agree on the tile max (and on going on) with the other half of the row
-                float *xb = xch + (gw & 1) * 256;
-                xb[h * 128 + t] = mh;
-                ok = red_and(pair_bar, 64, ok);
-                if (!ok) break;
-                const float mt = fmaxf(mh, xb[(h ^ 1) * 128 + t]);
                 if (warp_active) {
+                    const float mt = HalfTile<W, HK, 0>::logits(tSl, lutw, e0, qr_t, P.c);
                     // lazy rescale: the reference max moves only when it grows by > 2^8
                     float alpha = 1.f;
                     if (mt > m + kRescaleLog2) {
@@ -640,9 +627,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         m = mt;
                         l *= alpha;
                     }
-                    if (h == 0 && kt > 0 && __any_sync(~0u, alpha < 1.f))
+                    if (kt > 0 && __any_sync(~0u, alpha < 1.f))
                         ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
-                    l += h == 0 ? HalfTile<W, HK, 0>::probs(tSl, m) : HalfTile<W, HK, 1>::probs(tSl, m);
+                    l += HalfTile<W, HK, 0>::probs(tSl, m);
                     tmem_st_wait();
                 }
                 tc_fence_before();
@@ -651,25 +638,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok)
                 ok = __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc, kStatusTimeoutMma,
                                                &abort_flag));
-            if (!red_and(group_bar, 256, ok)) break;
+            if (!red_and(group_bar, 128, ok)) break;
             tc_fence_after();
-            // each half normalises 32 of the row's 64 output columns into the
-            // staging tile, 16 at a time
-            float *xs = xch + 512;
-            xs[h * 128 + t] = l;
-            named_bar_sync(pair_bar, 64);
-            const float inv = 1.f / (l + xs[(h ^ 1) * 128 + t]);
+            // normalise the row's 64 output columns into the staging tile, 16 at a time
+            const float inv = 1.f / l;
 #pragma unroll
-            for (int c2 = 0; c2 < 2; ++c2) {
+            for (int c2 = 0; c2 < 4; ++c2) {
                 uint32_t o[16];
                 if (warp_active) {
-                    tmem_ld16(tOl + 32 * h + 16 * c2, o);
+                    tmem_ld16(tOl + 16 * c2, o);
                     tmem_ld_wait(o);
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     const uint32_t *src = o + 8 * c;
-                    const int chunk = 4 * h + 2 * c2 + c;
+                    const int chunk = 2 * c2 + c;
                     st_shared_v4(stage_row + ((chunk ^ (t & 7)) << 4),
                                  pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
                                  pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
@@ -680,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars.o_empty[wg]);
             fence_proxy_async_smem();
-            named_bar_sync(group_bar, 256);
+            named_bar_sync(group_bar, 128);
             if (leader) {
                 // rows past the grid fall outside the tensor map and are not written
                 tma_store_3d(&tm_o, qr_base, 0, qt * 128, I.slice);
@@ -735,8 +718,6 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         off += 2 * p.qr_stride;
         p.off_mask = off;
         off += 2 * 4096;
-        p.off_xch = off;
-        off += 2 * 3 * 2 * 128 * 4;
         p.off_lut = off;
         if (HK) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
         off = align_up(off, 1024);
