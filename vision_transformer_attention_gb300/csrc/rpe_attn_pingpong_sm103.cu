@@ -55,13 +55,25 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kD = 64;
 constexpr int kTileBytes = 128 * 128;  // one 128-row x 64-column bf16 tile
-constexpr int kThreads = 384;
-// Register split (launch: 384 threads x 168 = 64,512): control warpgroup 64,
-// softmax warps 216 -> 128 x 64 + 256 x 216 = 63,488.
-constexpr int kRegsLaunch = 168;
-constexpr int kRegsControl = 64;
-constexpr int kRegsSoftmax = 216;
-static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+// NG softmax groups (query tiles) per CTA: warps 0..4NG-1 are the groups'
+// warpgroups, warpgroup NG the control warps. Register split per CTA: control
+// warpgroup 64 registers, softmax warps the rest of the launch allocation.
+// NG = 2 (a pair of query tiles sharing every K/V tile, one CTA per SM) is
+// used; NG = 1 (one query tile per CTA, two CTAs per SM, independent
+// pipelines but twice the K/V traffic from L2) measured slower at both grid
+// widths.
+constexpr int kGroupsPerCta = 2;
+
+template <int NG>
+struct Layout {
+    static constexpr int kThreads = 128 * (NG + 1);
+    static constexpr int kCtasPerSm = NG == 1 ? 2 : 1;
+    static constexpr int kRegsLaunch = NG == 2 ? 168 : 128;
+    static constexpr int kRegsControl = 64;
+    static constexpr int kRegsSoftmax = NG == 2 ? 216 : 192;
+    static_assert(128 * kRegsControl + 128 * NG * kRegsSoftmax <= kThreads * kRegsLaunch,
+                  "register split");
+};
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 3;       // score slots per group (see Geo::SLOTS)
@@ -87,6 +99,7 @@ struct Geo {
 
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
+    int single;  // 1: an item is one query tile (one group per CTA)
     uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
@@ -115,6 +128,12 @@ struct Item {
 // of this CTA, -1 past its last; every role walks the same sequence.
 __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
     Item r;
+    if (P.single) {
+        r.slice = item / P.qtiles;
+        r.qt0 = item % P.qtiles;
+        r.has_b = false;
+        return r;
+    }
     const int nfull = P.slices * P.pairs_full;
     if (item < nfull) {
         r.slice = item / P.pairs_full;
@@ -198,6 +217,11 @@ struct HalfTile {
         uint32_t ida[NROWS][NA];
         float mx = -INFINITY;
         const float2 c2 = make_float2(c, c);
+        // all of the row's scores in one tensor-memory round trip; its latency
+        // overlaps the first chunk's gathers
+        uint32_t s[NQ][16];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) tmem_ld16(tS + J0 + 16 * q, s[q]);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             const int jc = J0 + 16 * q;
@@ -234,13 +258,15 @@ struct HalfTile {
 #pragma unroll
                 for (int j = 0; j < 16; ++j) qv[j] = 0.f;
             }
-            uint32_t s[16];
-            tmem_ld16(tS + jc, s);
-            tmem_ld_wait(s);
+            if (q == 0) {
+                tmem_ld_wait();
+#pragma unroll
+                for (int qq = 0; qq < NQ; ++qq) tmem_ready(s[qq]);
+            }
             float x[16];
 #pragma unroll
             for (int j = 0; j < 16; j += 2) {
-                const float2 r = ffma2(make_float2(__uint_as_float(s[j]), __uint_as_float(s[j + 1])),
+                const float2 r = ffma2(make_float2(__uint_as_float(s[q][j]), __uint_as_float(s[q][j + 1])),
                                        c2, make_float2(qv[j], qv[j + 1]));
                 x[j] = (jc + j < G::KT) ? r.x : -INFINITY;
                 x[j + 1] = (jc + j + 1 < G::KT) ? r.y : -INFINITY;
@@ -263,16 +289,21 @@ struct HalfTile {
         tmem_st_wait();
         float sum = 0.f;
         const float2 nm = make_float2(-m, -m);
+        // all of the row's logits in one round trip (so no chunk's P overwrites
+        // logits still to be read)
+        uint32_t xs[NQ][16];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) tmem_ld16(tS + J0 + 16 * q, xs[q]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) tmem_ready(xs[q]);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             const int jc = J0 + 16 * q;
-            uint32_t xs[16];
-            tmem_ld16(tS + jc, xs);
-            tmem_ld_wait(xs);
             float2 p[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const float2 d = fadd2(make_float2(__uint_as_float(xs[2 * e]), __uint_as_float(xs[2 * e + 1])), nm);
+                const float2 d = fadd2(make_float2(__uint_as_float(xs[q][2 * e]), __uint_as_float(xs[q][2 * e + 1])), nm);
                 p[e] = make_float2(jc + 2 * e < G::KT ? ex2_approx(d.x) : 0.f,
                                    jc + 2 * e + 1 < G::KT ? ex2_approx(d.y) : 0.f);
             }
@@ -298,14 +329,16 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
     return static_cast<uint32_t>((16 * kk / G::HS) * G::HS + ((16 * kk) % G::HS) / 2);
 }
 
-template <int W, bool HK>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int W, bool HK, int NG>
+__global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_rk,
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     using G = Geo<W>;
+    using L = Layout<NG>;
+    constexpr int kThreads = L::kThreads;
     extern __shared__ uint8_t smem_raw[];
     // aligned by pointer arithmetic, so the compiler keeps the shared address space
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -328,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars.tab_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.q_full[i], 1);
-            mbar_init(&bars.q_empty[i], 2);  // one arrival per group issuer
+            mbar_init(&bars.q_empty[i], NG);  // one arrival per group issuer
             mbar_init(&bars.o_full[i], 1);
             mbar_init(&bars.o_empty[i], 128);
             mbar_init(&bars.pv_done[i], 1);
@@ -340,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kMaxStages; ++i) {
             mbar_init(&bars.kv_full[i], 1);
-            mbar_init(&bars.kv_empty[i], 2);  // one arrival per group issuer
+            mbar_init(&bars.kv_empty[i], NG);  // one arrival per group issuer
         }
         abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 0) tmem_alloc(&tmem_base_s, 512);
+    if (warp == 0) tmem_alloc(&tmem_base_s, 256 * NG);
     if (HK) {
         // offset table as bytes, ids clamped into [0, nb). Keys past the last
         // grid row index up to lut_pad bytes before the table; those bytes hold
@@ -379,9 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    if (warp >= 8) {
-        regs_dealloc<kRegsControl>();
-        if (warp == 8) {
+    if (warp >= 4 * NG) {
+        regs_dealloc<L::kRegsControl>();
+        if (warp == 4 * NG) {
             // -------------------------------------------- TMA producer
             if (lane == 0) {
                 prefetch_tmap(&tm_q);
@@ -402,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!(ok = mbar_wait(&bars.q_empty[qb], (quse & 1) ^ 1, wc, kStatusTimeoutSync,
                                          &abort_flag)))
                         break;
-                    uint8_t *qd = sQ + qb * 2 * kTileBytes;
+                    uint8_t *qd = sQ + qb * NG * kTileBytes;
                     mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes);
                     tma_load_3d(qd, &tm_q, &bars.q_full[qb], 0, I.qt0 * 128, I.slice);
                     if (I.has_b)
@@ -433,14 +466,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   nullptr);
             }
             __syncwarp();
-        } else if (warp == 9 || warp == 10) {
+        } else if (warp > 4 * NG && warp <= 5 * NG) {
             // -------------------------------------------- MMA issuer of group w
             // The order is fixed: unit u is issued once unit u - SLOTS has been
             // consumed (and, for a tile's scores, its P V issued), so
             // the issuer is a straight sequence of bounded blocking waits. For
             // items the group sits out it still releases the item's Q buffer and
             // K/V stages, each after the matching load has landed.
-            const int w = warp - 9;
+            const int w = warp - (4 * NG + 1);
             if (lane == 0) {
                 constexpr uint32_t kIdS = idesc_bf16(128, G::NS, false, false);
                 constexpr uint32_t kIdQR = idesc_bf16(128, 64, false, false);
@@ -505,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (ok) mbar_arrive(&bars.q_empty[qb]);
                         continue;
                     }
-                    const uint64_t dQ = hi128 | ((aQ + qb * 2 * kTileBytes) >> 4);
+                    const uint64_t dQ = hi128 | ((aQ + qb * NG * kTileBytes) >> 4);
                     for (int kt = HK ? -1 : 0; ok && kt < P.nkt; ++kt) {
                         if (np == G::SLOTS) consume();
                         if (!ok) break;
@@ -552,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
         }
     } else {
-        regs_alloc<kRegsSoftmax>();
+        regs_alloc<L::kRegsSoftmax>();
         // ------------------------------------------------ softmax groups
         // One thread per query row. Decisions to go on or stop are uniform per
         // warp within an item and over the whole group twice per item (at its
@@ -677,15 +710,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("barrier.sync 0;" ::: "memory");
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, 256 * NG);
     }
 }
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int W, bool HK>
+template <int W, bool HK, int NG>
 cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     using G = Geo<W>;
+    using L = Layout<NG>;
     PPParams p{};
     const int N = a.H * a.W;
     p.N = N;
@@ -695,13 +729,16 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.qtiles = (N + 127) / 128;
     p.pairs_full = p.qtiles / 2;
     p.slices = a.B * a.heads;
-    p.items = p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
+    p.single = NG == 1;
+    p.items = NG == 1 ? p.slices * p.qtiles
+                      : p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
     p.lut_pad = static_cast<int>(align_up(G::R * G::COLS + 4, 16));
     p.nvalid_last = N - (p.nkt - 1) * G::KT;
     p.lut = a.lut;
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
-    const uint32_t cap = 227 * 1024 - 1024;
+    // per CTA: the SM's 228 KB less 1 KB reserved per CTA
+    const uint32_t cap = (228 / L::kCtasPerSm - 1) * 1024;
     uint32_t total = 0;
     // as many K/V stages as fit (up to kMaxStages) next to a double-buffered Q;
     // a single Q buffer only when that leaves fewer than three stages
@@ -709,13 +746,13 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.nq = nq;
         uint32_t off = 0;
         p.off_q = off;
-        off += nq * 2 * kTileBytes;
+        off += nq * NG * kTileBytes;
         p.off_rk = off;
         if (HK) off += kTileBytes / 2;
         p.off_qr = off;
         // each group's QR' table doubles as its 16 KB output staging tile
         p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, 128 * 128), 1024);
-        off += 2 * p.qr_stride;
+        off += NG * p.qr_stride;
         p.off_mask = off;
         off += 2 * 4096;
         p.off_lut = off;
@@ -725,7 +762,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         const int room = static_cast<int>((cap - std::min(cap, 1024 + off)) / (2 * G::KV_BYTES));
         p.nst = std::min(room, kMaxStages);
         total = 1024 + off + p.nst * 2 * G::KV_BYTES;
-        if (p.nst >= 3 || (nq == 1 && p.nst >= 2)) break;
+        if (p.nst >= 3 || (nq == 1 && p.nst >= G::SLOTS)) break;
     }
     // an issuer waiting for tile t's K/V holds up to SLOTS - 1 earlier tiles
     if (p.nst < G::SLOTS) return cudaErrorInvalidValue;
@@ -749,12 +786,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 2, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK>,
+    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
-    const int grid = std::min(p.items, sm_count());
-    rpe_pingpong_kernel<W, HK><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, to, p);
+    const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
+    rpe_pingpong_kernel<W, HK, NG><<<grid, L::kThreads, total, stream>>>(tq, tk, tv, trk, to, p);
     return cudaGetLastError();
 }
 
@@ -763,10 +800,11 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
     if (a.d != kD || (a.terms & ~1u) != 0 || a.num_buckets > 64) return false;
     const bool hk = (a.terms & 1u) != 0;
+    constexpr int NG = kGroupsPerCta;
     if (a.W == 14)
-        *err = hk ? launch_pp<14, true>(a, stream) : launch_pp<14, false>(a, stream);
+        *err = hk ? launch_pp<14, true, NG>(a, stream) : launch_pp<14, false, NG>(a, stream);
     else if (a.W == 56)
-        *err = hk ? launch_pp<56, true>(a, stream) : launch_pp<56, false>(a, stream);
+        *err = hk ? launch_pp<56, true, NG>(a, stream) : launch_pp<56, false, NG>(a, stream);
     else
         return false;
     return true;
