@@ -346,6 +346,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
+    griddep_launch_dependents();
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
@@ -379,16 +380,6 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 256 * NG);
-    if (HK) {
-        // offset table as bytes, ids clamped into [0, nb). Keys past the last
-        // grid row index up to lut_pad bytes before the table; those bytes hold
-        // bucket 0 so every read stays in bounds (those scores are masked).
-        for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
-        for (int e = tid; e < P.lut_len; e += kThreads) {
-            const int id = __ldg(P.lut + e);
-            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
-        }
-    }
     // K/V buffers: rows KT..NS-1 are never loaded and must hold finite values
     for (int e = tid; e < P.nst * 2 * G::KV_BYTES / 16; e += kThreads)
         st_shared_v4(smem_u32(sKV) + e * 16, 0u, 0u, 0u, 0u);
@@ -406,6 +397,18 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             if (r >= P.nvalid_last) *reinterpret_cast<uint16_t *>(mk + 4096 + off) = 0x3F80u;  // bf16 1
         }
         fence_proxy_async_smem();
+    }
+    // everything above touches no input: it may overlap the previous kernel
+    griddep_wait();
+    if (HK) {
+        // offset table as bytes, ids clamped into [0, nb). Keys past the last
+        // grid row index up to lut_pad bytes before the table; those bytes hold
+        // bucket 0 so every read stays in bounds (those scores are masked).
+        for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
+        for (int e = tid; e < P.lut_len; e += kThreads) {
+            const int id = __ldg(P.lut + e);
+            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -791,8 +794,8 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
-    rpe_pingpong_kernel<W, HK, NG><<<grid, L::kThreads, total, stream>>>(tq, tk, tv, trk, to, p);
-    return cudaGetLastError();
+    return launch_pdl(rpe_pingpong_kernel<W, HK, NG>, dim3(grid), dim3(L::kThreads), total, stream,
+                      tq, tk, tv, trk, to, p);
 }
 
 }  // namespace

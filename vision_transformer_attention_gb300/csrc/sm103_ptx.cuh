@@ -106,6 +106,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const 
 
 // ------------------------------------------------------------------ fences
 
+// Programmatic dependent launch. launch_dependents lets the next grid in the
+// stream (launched with programmatic stream serialization) be scheduled once
+// every CTA of this grid has issued it or exited; wait blocks until the grids
+// this one depends on have completed and their memory operations are visible
+// (it returns at once for a grid launched without that attribute). A kernel
+// launched with the attribute must wait before it reads any input.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

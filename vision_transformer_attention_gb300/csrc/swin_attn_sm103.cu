@@ -78,6 +78,7 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
 
+    griddep_launch_dependents();
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
 
@@ -94,6 +95,8 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         prefetch_tmap(&tm_o);
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 128);
+    // nothing above reads an input: it may overlap the previous kernel
+    griddep_wait();
 
     // Bias table -> shared memory, head-major, pre-multiplied by log2(e).
     for (int e = tid; e < heads * T::kNB; e += blockDim.x) {
@@ -315,10 +318,9 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
     if (status == nullptr) return cudaErrorMemoryAllocation;
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
-    swin_bf16_kernel<M, D><<<grid, 128, smem, stream>>>(
-        tq, tk, tv, to, a.bias_table, a.heads, units, tiles, scale_log2e,
-        WaitCtl{status, kDefaultWaitNs});
-    return cudaGetLastError();
+    return launch_pdl(swin_bf16_kernel<M, D>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
+                      a.bias_table, a.heads, units, tiles, scale_log2e,
+                      WaitCtl{status, kDefaultWaitNs});
 }
 
 }  // namespace
@@ -408,10 +410,9 @@ cudaError_t launch_swin_noalloc_tmpl(const SwinBf16Args &a, unsigned *status,
     if (err != cudaSuccess) return err;
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
-    swin_bf16_kernel<M, D><<<grid, 128, smem, stream>>>(tq, tk, tv, to, a.bias_table, a.heads,
-                                                        units, tiles, scale_log2e,
-                                                        WaitCtl{status, kDefaultWaitNs});
-    return cudaGetLastError();
+    return launch_pdl(swin_bf16_kernel<M, D>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
+                      a.bias_table, a.heads, units, tiles, scale_log2e,
+                      WaitCtl{status, kDefaultWaitNs});
 }
 
 }  // namespace

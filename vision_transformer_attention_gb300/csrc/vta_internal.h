@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <utility>
 #include <cstdint>
 
 namespace vta {
@@ -17,6 +18,25 @@ unsigned *device_status_word();
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // Number of SMs of the current device (cached per device).
+// Launches kernel with programmatic stream serialization: its prologue may
+// overlap the tail of the previous kernel in the stream. Only for kernels that
+// call griddep_wait() before reading any input.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int sm_count();
 
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point.
