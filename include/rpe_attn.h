@@ -161,6 +161,29 @@ int swin_window_attn_fwd_noalloc(const void *q, const void *k, const void *v,
                                  int M, int d, void *out, void *stream);
 
 /*
+ * swin_window_attn_fwd_fmap -- swin_window_attn_fwd with the window partition
+ * (and its reverse) fused into the kernel (SWIN 3.2: self-attention inside
+ * non-overlapping M x M windows that tile the feature map).
+ *
+ * q, k, v, out : device bf16 feature maps [batch, img_h, img_w, heads * d],
+ *                channels-last (head h of pixel (y, x) at channels
+ *                [h * d, (h + 1) * d)). Window (wy, wx) of an image covers rows
+ *                [wy M, wy M + M) and columns [wx M, wx M + M); its token i is
+ *                pixel (wy M + i / M, wx M + i % M). Every window and head is
+ *                attended exactly as swin_window_attn_fwd does for the same
+ *                window cut out of the map, and out receives the result at the
+ *                same pixels and channels.
+ * bias_table   : device float32 [(2M-1)^2, heads], as for swin_window_attn_fwd.
+ * Requires img_h and img_w to be multiples of M (else RPE_ERR_INVALID_ARG),
+ * M == 7, d in {32, 64}, heads <= 32 (else RPE_ERR_UNSUPPORTED); pointers
+ * 16-byte aligned. The library owns nothing the caller passes; the call is
+ * asynchronous on `stream`.
+ */
+int swin_window_attn_fwd_fmap(const void *q, const void *k, const void *v,
+                              const float *bias_table, int batch, int img_h, int img_w,
+                              int heads, int M, int d, void *out, void *stream);
+
+/*
  * rpe_device_status -- synchronises the current device and returns, through
  * *status, the word the kernels set when a bounded wait ran out (0 = none).
  * Clears the word when `clear` is non-zero. Returns RPE_ERR_TIMEOUT if any

@@ -27,6 +27,7 @@ SIGNATURES = {
     "rpe_attn_fwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _u, _i, _p, _p]),
     "swin_window_attn_fwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
     "swin_window_attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p]),
+    "swin_window_attn_fwd_fmap": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),
     "rpe_device_status": (_i, [ctypes.POINTER(_u), _i]),
     "rpe_wait_probe": (_i, [_u64, _p]),
     "rpe_status_string": (ctypes.c_char_p, [_i]),

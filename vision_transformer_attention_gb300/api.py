@@ -101,6 +101,37 @@ def swin_window_attn_fwd(q, k, v, bias_table, M, out=None):
     return out
 
 
+def swin_window_attn_fwd_fmap(q, k, v, bias_table, M, out=None):
+    """Swin window attention on channels-last bf16 feature maps q, k, v
+    [batch, img_h, img_w, heads * d]: every M x M window of every head is
+    attended as swin_window_attn_fwd does, with the window partition and its
+    reverse done by the kernel's loads and stores."""
+    _need(q, "q")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bfloat16")
+    if q.dim() != 4:
+        raise ValueError("q must be [batch, img_h, img_w, heads * d]")
+    batch, img_h, img_w, channels = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    if bias_table.dim() != 2 or bias_table.shape[0] != (2 * M - 1) ** 2:
+        raise ValueError("bias_table must be [(2M-1)^2, heads]")
+    heads = bias_table.shape[1]
+    _need(bias_table, "bias_table", torch.float32, ((2 * M - 1) ** 2, heads), q.device)
+    if channels % heads:
+        raise ValueError("channels must be heads * d")
+    d = channels // heads
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", q.dtype, q.shape, q.device)
+    with torch.cuda.device(q.device):
+        check("swin_window_attn_fwd_fmap", _lib.lib().swin_window_attn_fwd_fmap(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), batch, img_h, img_w, heads, M, d,
+            _ptr(out), _stream(q)))
+    return out
+
+
 def rpe_device_status(clear=True):
     """Synchronises the device; returns the in-kernel timeout status word (0 = none)."""
     st = ctypes.c_uint(0)

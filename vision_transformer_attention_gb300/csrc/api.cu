@@ -237,6 +237,26 @@ int swin_window_attn_fwd(const void *q, const void *k, const void *v, const floa
     return status_of(launch_swin_bf16(a, st));
 }
 
+int swin_window_attn_fwd_fmap(const void *q, const void *k, const void *v,
+                              const float *bias_table, int batch, int img_h, int img_w,
+                              int heads, int M, int d, void *out, void *stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bias_table == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (batch < 1 || img_h < 1 || img_w < 1 || heads < 1 || M < 1 || d < 1)
+        return RPE_ERR_INVALID_ARG;
+    if (img_h % M != 0 || img_w % M != 0) return RPE_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, out, bias_table};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
+    const long long units =
+        static_cast<long long>(batch) * (img_h / M) * (img_w / M) * static_cast<long long>(heads);
+    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30) ||
+        img_h >= (1 << 24) || img_w >= (1 << 24))
+        return RPE_ERR_UNSUPPORTED;
+    SwinFmapArgs a{q, k, v, out, bias_table, batch, img_h, img_w, heads, M, d};
+    return status_of(launch_swin_bf16_fmap(a, static_cast<cudaStream_t>(stream)));
+}
+
 int rpe_device_status(unsigned *status, int clear) {
     if (status == nullptr) return RPE_ERR_INVALID_ARG;
     if (cudaDeviceSynchronize() != cudaSuccess) return RPE_ERR_CUDA;

@@ -58,13 +58,20 @@ struct SwinTile {
     static_assert(kN <= 64, "a window must fit one 64-row slot");
 };
 
-template <int M, int D>
+// FM = false: q/k/v/out are [units][n][d] (windows already partitioned), one
+// 3D box per operand and tile. FM = true: they are channels-last feature maps
+// [batch][img_h][img_w][heads][d] and a unit is (image, window row, window
+// column, head) in that order; one 5D box [1][M][M][1][d] per unit and operand
+// reads the window straight from the map (and writes it back), so no
+// partition or reverse copy exists.
+template <int M, int D, bool FM>
 __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     swin_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ bias_table,
-                     int heads, int units, int tiles, float scale_log2e, WaitCtl wc) {
+                     int heads, int units, int tiles, int wins_y, int wins_x, float scale_log2e,
+                     WaitCtl wc) {
     using T = SwinTile<M, D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -95,6 +102,13 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         prefetch_tmap(&tm_o);
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 128);
+    if constexpr (FM) {
+        // a window's box fills rows 0..n-1 of its 64-row slot; the rest must
+        // hold finite values (zero) for the products
+        for (int e = tid; e < 2 * T::kStageBytes / 16; e += blockDim.x)
+            st_shared_v4(smem_u32(stage_base) + e * 16, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     // nothing above reads an input: it may overlap the previous kernel
     griddep_wait();
 
@@ -118,12 +132,33 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     uint64_t *mma_bar_pending = nullptr;
     uint32_t mma_parity_pending = 0;
 
+    // feature-map coordinates (head, first column, first row, image) of a unit
+    auto unit_coords = [&](int u, int &h, int &x0, int &y0, int &b) {
+        h = u % heads;
+        const int win = u / heads;
+        x0 = (win % wins_x) * M;
+        y0 = ((win / wins_x) % wins_y) * M;
+        b = win / (wins_x * wins_y);
+    };
     auto issue_load = [&](int tile, int stage) {
         uint8_t *sb = stage_base + stage * T::kStageBytes;
-        mbar_arrive_expect_tx(&bar_load[stage], 3 * T::kOperBytes);
-        tma_load_3d(sb, &tm_q, &bar_load[stage], 0, 0, 2 * tile);
-        tma_load_3d(sb + T::kOperBytes, &tm_k, &bar_load[stage], 0, 0, 2 * tile);
-        tma_load_3d(sb + 2 * T::kOperBytes, &tm_v, &bar_load[stage], 0, 0, 2 * tile);
+        if constexpr (FM) {
+            const int nu = 2 * tile + 1 < units ? 2 : 1;
+            mbar_arrive_expect_tx(&bar_load[stage], 3 * nu * T::kN * T::kRowBytes);
+            for (int s2 = 0; s2 < nu; ++s2) {
+                int h, x0, y0, b;
+                unit_coords(2 * tile + s2, h, x0, y0, b);
+                uint8_t *dst = sb + s2 * 64 * T::kRowBytes;
+                tma_load_5d(dst, &tm_q, &bar_load[stage], 0, h, x0, y0, b);
+                tma_load_5d(dst + T::kOperBytes, &tm_k, &bar_load[stage], 0, h, x0, y0, b);
+                tma_load_5d(dst + 2 * T::kOperBytes, &tm_v, &bar_load[stage], 0, h, x0, y0, b);
+            }
+        } else {
+            mbar_arrive_expect_tx(&bar_load[stage], 3 * T::kOperBytes);
+            tma_load_3d(sb, &tm_q, &bar_load[stage], 0, 0, 2 * tile);
+            tma_load_3d(sb + T::kOperBytes, &tm_k, &bar_load[stage], 0, 0, 2 * tile);
+            tma_load_3d(sb + 2 * T::kOperBytes, &tm_v, &bar_load[stage], 0, 0, 2 * tile);
+        }
         loads_pending |= 1u << stage;
     };
 
@@ -268,7 +303,16 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         const int aborted = __syncthreads_or(abort_flag);
         if (aborted) break;
         if (tid == 0) {
-            tma_store_3d(&tm_o, sb, 0, 0, 2 * tile);
+            if constexpr (FM) {
+                const int nu = 2 * tile + 1 < units ? 2 : 1;
+                for (int s2 = 0; s2 < nu; ++s2) {
+                    int h, x0, y0, b;
+                    unit_coords(2 * tile + s2, h, x0, y0, b);
+                    tma_store_5d(&tm_o, sb + s2 * 64 * T::kRowBytes, 0, h, x0, y0, b);
+                }
+            } else {
+                tma_store_3d(&tm_o, sb, 0, 0, 2 * tile);
+            }
             bulk_commit_group();
         }
     }
@@ -310,7 +354,7 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, swz))
         return cudaErrorInvalidValue;
     const int smem = T::smem_bytes(a.heads);
-    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D>,
+    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D, false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            T::smem_bytes(T::kMaxHeads));
     if (err != cudaSuccess) return err;
@@ -318,8 +362,45 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
     if (status == nullptr) return cudaErrorMemoryAllocation;
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
-    return launch_pdl(swin_bf16_kernel<M, D>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
-                      a.bias_table, a.heads, units, tiles, scale_log2e,
+    return launch_pdl(swin_bf16_kernel<M, D, false>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
+                      a.bias_table, a.heads, units, tiles, 1, 1, scale_log2e,
+                      WaitCtl{status, kDefaultWaitNs});
+}
+
+template <int M, int D>
+cudaError_t launch_swin_fmap_tmpl(const SwinFmapArgs &a, cudaStream_t stream) {
+    using T = SwinTile<M, D>;
+    if (a.heads > T::kMaxHeads) return cudaErrorInvalidValue;
+    const int wins_y = a.img_h / M, wins_x = a.img_w / M;
+    const int units = a.batch * wins_y * wins_x * a.heads;
+    const int tiles = (units + 1) / 2;
+    const uint64_t row = static_cast<uint64_t>(a.heads) * D * 2;  // bytes per pixel
+    const uint64_t dims[5] = {static_cast<uint64_t>(D), static_cast<uint64_t>(a.heads),
+                              static_cast<uint64_t>(a.img_w), static_cast<uint64_t>(a.img_h),
+                              static_cast<uint64_t>(a.batch)};
+    const uint64_t strides[4] = {static_cast<uint64_t>(D) * 2, row, row * a.img_w,
+                                 row * a.img_w * a.img_h};
+    const uint32_t box[5] = {static_cast<uint32_t>(D), 1, M, M, 1};
+    const CUtensorMapSwizzle swz =
+        (D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+    const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUtensorMap tq, tk, tv, to;
+    if (!encode_tensor_map(&tq, bf, 5, a.q, dims, strides, box, swz) ||
+        !encode_tensor_map(&tk, bf, 5, a.k, dims, strides, box, swz) ||
+        !encode_tensor_map(&tv, bf, 5, a.v, dims, strides, box, swz) ||
+        !encode_tensor_map(&to, bf, 5, a.out, dims, strides, box, swz))
+        return cudaErrorInvalidValue;
+    const int smem = T::smem_bytes(a.heads);
+    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D, true>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           T::smem_bytes(T::kMaxHeads));
+    if (err != cudaSuccess) return err;
+    unsigned *status = device_status_word();
+    if (status == nullptr) return cudaErrorMemoryAllocation;
+    const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
+    const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
+    return launch_pdl(swin_bf16_kernel<M, D, true>, dim3(grid), dim3(128), smem, stream, tq, tk,
+                      tv, to, a.bias_table, a.heads, units, tiles, wins_y, wins_x, scale_log2e,
                       WaitCtl{status, kDefaultWaitNs});
 }
 
@@ -328,6 +409,12 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
 cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream) {
     if (a.M == 7 && a.d == 32) return launch_swin_tmpl<7, 32>(a, stream);
     if (a.M == 7 && a.d == 64) return launch_swin_tmpl<7, 64>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_swin_bf16_fmap(const SwinFmapArgs &a, cudaStream_t stream) {
+    if (a.M == 7 && a.d == 32) return launch_swin_fmap_tmpl<7, 32>(a, stream);
+    if (a.M == 7 && a.d == 64) return launch_swin_fmap_tmpl<7, 64>(a, stream);
     return cudaErrorInvalidValue;
 }
 
@@ -401,7 +488,7 @@ cudaError_t launch_swin_noalloc_tmpl(const SwinBf16Args &a, unsigned *status,
         !encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, swz))
         return cudaErrorInvalidValue;
     const int smem = T::smem_bytes(a.heads);
-    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D>,
+    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D, false>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            T::smem_bytes(T::kMaxHeads));
     if (err != cudaSuccess) return err;
@@ -410,8 +497,8 @@ cudaError_t launch_swin_noalloc_tmpl(const SwinBf16Args &a, unsigned *status,
     if (err != cudaSuccess) return err;
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
-    return launch_pdl(swin_bf16_kernel<M, D>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
-                      a.bias_table, a.heads, units, tiles, scale_log2e,
+    return launch_pdl(swin_bf16_kernel<M, D, false>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
+                      a.bias_table, a.heads, units, tiles, 1, 1, scale_log2e,
                       WaitCtl{status, kDefaultWaitNs});
 }
 

@@ -69,6 +69,15 @@ struct SwinBf16Args {
     int num_windows, heads, M, d;
 };
 cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream);
+// Swin window attention on channels-last feature maps [batch][img_h][img_w][heads][d]:
+// windows are read from and written back to the maps by the kernel's TMA boxes.
+struct SwinFmapArgs {
+    const void *q, *k, *v;
+    void *out;
+    const float *bias_table;
+    int batch, img_h, img_w, heads, M, d;
+};
+cudaError_t launch_swin_bf16_fmap(const SwinFmapArgs &a, cudaStream_t stream);
 
 struct RpeBf16Args {
     const void *q, *k, *v, *tab_q, *tab_k, *tab_v;

@@ -117,6 +117,33 @@ def swin_inputs(num_windows, heads, M, d, dtype="bf16", table_std=0.02, seed=0):
     return {"q": q, "k": k, "v": v, "table": table}
 
 
+def swin_fmap_inputs(batch, img_h, img_w, heads, M, d, table_std=0.02, seed=0):
+    """Channels-last bf16 feature maps q, k, v [batch, img_h, img_w, heads * d]
+    and the bias table [(2M-1)^2, heads] fp32 (same draws as swin_inputs)."""
+    shape = (batch, img_h, img_w, heads * d)
+    q = _normal(shape, seed + 0).to(torch.bfloat16)
+    k = _normal(shape, seed + 1).to(torch.bfloat16)
+    v = _normal(shape, seed + 2).to(torch.bfloat16)
+    table = _normal(((2 * M - 1) ** 2, heads), seed + 3, table_std)
+    return {"q": q, "k": k, "v": v, "table": table}
+
+
+def window_partition(x, M, heads):
+    """[batch, img_h, img_w, heads * d] -> [windows, heads, M*M, d]: windows in
+    (image, window row, window column) order, token i of a window at (i / M, i % M)."""
+    b, h, w, c = x.shape
+    d = c // heads
+    x = x.reshape(b, h // M, M, w // M, M, heads, d)
+    return x.permute(0, 1, 3, 5, 2, 4, 6).reshape(b * (h // M) * (w // M), heads, M * M, d)
+
+
+def window_reverse(x, M, batch, img_h, img_w):
+    """Inverse of window_partition."""
+    nw, heads, n, d = x.shape
+    x = x.reshape(batch, img_h // M, img_w // M, heads, M, M, d)
+    return x.permute(0, 1, 4, 2, 5, 3, 6).reshape(batch, img_h, img_w, heads * d)
+
+
 def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02, seed=0):
     """q, k, v [B, heads, N, d] and head-shared tables [num_buckets, d] for the
     enabled terms (None for a disabled one)."""
