@@ -62,8 +62,11 @@ def work_of(cfg):
 def workload_config(cfg):
     from vision_transformer_attention_gb300.workloads import SwinConfig
     if isinstance(cfg, SwinConfig):
-        return {"workload": cfg.name, "num_windows": cfg.num_windows, "heads": cfg.heads,
-                "window": cfg.M, "n": cfg.n, "d": cfg.d}
+        out = {"workload": cfg.name, "num_windows": cfg.num_windows, "heads": cfg.heads,
+               "window": cfg.M, "n": cfg.n, "d": cfg.d}
+        if cfg.fmap:
+            out["feature_map"] = list(cfg.fmap) + [cfg.heads * cfg.d]
+        return out
     terms = "".join(t for t, f in (("Q", 2), ("K", 1), ("V", 4)) if cfg.flags & f)
     return {"workload": cfg.name, "B": cfg.B, "heads": cfg.heads, "grid": [cfg.H, cfg.W],
             "N": cfg.N, "d": cfg.d, "terms": terms or "none", "num_buckets": cfg.num_buckets,
@@ -74,10 +77,11 @@ def workload_config(cfg):
 # and its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from an ncu capture of the kernel as it stands; None when not measured).
 DOMINANT = {
-    "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", 57842432 + 1343232),
-    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,K>", "hbm", 28999168 + 0),
-    "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29064704 + 1536),
-    "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", 58135296 + 1886464),
+    "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", 57840640 + 1616128),
+    "swin_t_stage1_fmap": ("swin_bf16_kernel<7,32,fmap>", "hbm", 57851136 + 1450752),
+    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,K>", "hbm", 29001472 + 0),
+    "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29064960 + 2816),
+    "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", 58131200 + 2073856),
 }
 
 
@@ -160,7 +164,12 @@ def make_step(cfg, sets):
     """Returns step(i) running the hot path on input set i % len(sets)."""
     from vision_transformer_attention_gb300 import api
     from vision_transformer_attention_gb300.workloads import SwinConfig
-    if isinstance(cfg, SwinConfig):
+    if isinstance(cfg, SwinConfig) and cfg.fmap:
+        def step(i):
+            s = sets[i % len(sets)]
+            api.swin_window_attn_fwd_fmap(s["q"], s["k"], s["v"], s["table"], cfg.M,
+                                          out=s["out"])
+    elif isinstance(cfg, SwinConfig):
         def step(i):
             s = sets[i % len(sets)]
             api.swin_window_attn_fwd(s["q"], s["k"], s["v"], s["table"], cfg.M, out=s["out"])
@@ -261,7 +270,11 @@ def e2e_run(cfg, dev, steps, barrier):
                              cfg.flags, table_q=tabs["tab_q"], table_k=tabs["tab_k"],
                              table_v=tabs["tab_v"], out=out)
         else:
-            api.swin_window_attn_fwd(dq["q"], dq["k"], dq["v"], tabs["table"], cfg.M, out=out)
+            if cfg.fmap:
+                api.swin_window_attn_fwd_fmap(dq["q"], dq["k"], dq["v"], tabs["table"], cfg.M,
+                                              out=out)
+            else:
+                api.swin_window_attn_fwd(dq["q"], dq["k"], dq["v"], tabs["table"], cfg.M, out=out)
         out_host.copy_(out, non_blocking=True)
 
     for _ in range(3):
@@ -359,7 +372,7 @@ def gpu_arm(args):
 
     extra_cfgs = {}
     if not args.headline_only:
-        for name in ("swin_t_stage1", "irpe_qkv_deit_s", "irpe_k_56x56"):
+        for name in ("swin_t_stage1", "swin_t_stage1_fmap", "irpe_qkv_deit_s", "irpe_k_56x56"):
             if name == args.workload:
                 continue
             c = workloads.CONFIGS[name]

@@ -42,6 +42,9 @@ class SwinConfig:
     M: int
     d: int
     dtype: str  # "bf16" or "f32"
+    # (batch, img_h, img_w) when q/k/v/out are channels-last feature maps that
+    # the kernel partitions itself; () for pre-partitioned windows
+    fmap: tuple = ()
 
     @property
     def n(self) -> int:
@@ -83,6 +86,9 @@ CONFIGS = {
     "swin_w7_small_fp32": SwinConfig("swin_w7_small_fp32", 4, 3, 7, 32, "f32"),
     # Swin-T stage 1: 56x56 map = 64 windows, batch 32 -> 2048 windows
     "swin_t_stage1": SwinConfig("swin_t_stage1", 2048, 3, 7, 32, "bf16"),
+    # the same, read from and written to the [32, 56, 56, 96] feature maps
+    "swin_t_stage1_fmap": SwinConfig("swin_t_stage1_fmap", 2048, 3, 7, 32, "bf16",
+                                     fmap=(32, 56, 56)),
     # iRPE-K at the DeiT-S shape, 14x14 grid, no class token
     "irpe_k_deit_s": IrpeConfig("irpe_k_deit_s", 64, 6, 14, 14, 64, FLAG_K, "bf16"),
     # iRPE on queries, keys and values, same shape
@@ -161,6 +167,9 @@ def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02
 
 
 def config_inputs(cfg, table_std=0.02, seed=0):
+    if isinstance(cfg, SwinConfig) and cfg.fmap:
+        b, h, w = cfg.fmap
+        return swin_fmap_inputs(b, h, w, cfg.heads, cfg.M, cfg.d, table_std, seed)
     if isinstance(cfg, SwinConfig):
         return swin_inputs(cfg.num_windows, cfg.heads, cfg.M, cfg.d, cfg.dtype,
                            table_std, seed)
