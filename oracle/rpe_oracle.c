@@ -85,6 +85,30 @@ int orc_product_bucket_ids(int H, int W, double alpha, double beta, double gamma
     return span * span;
 }
 
+/* iRPE section 3.2, Euclidean mapping (undirected): the bucket comes from the
+ * Euclidean length of the 2D offset through the same index function. The
+ * distance is rounded before the index (the Paper-vs-code list: the code
+ * rounds first; round half to even, as Python does). The table has
+ * 2*int(beta)+1 entries (section 3.2: 2 beta + 1 buckets); the index, in
+ * [0, int(beta)] for a distance, is stored shifted by int(beta), the same
+ * shift as one axis of a directed mapping. Writes ids[i*N + j]; returns the
+ * number of buckets. */
+int orc_euclidean_bucket_ids(int H, int W, double alpha, double beta, double gamma,
+                             int32_t *ids)
+{
+    int half = (int)beta;
+    int N = H * W;
+    for (int i = 0; i < N; ++i) {
+        int ri = i / W, ci = i % W;
+        for (int j = 0; j < N; ++j) {
+            int dr = ri - j / W, dc = ci - j % W;
+            double dist = nearbyint(sqrt((double)dr * dr + (double)dc * dc));
+            ids[(int64_t)i * N + j] = orc_piecewise_index(dist, alpha, beta, gamma) + half;
+        }
+    }
+    return 2 * half + 1;
+}
+
 /* SWIN2D sections 3.1-3.2: inside an M x M window the offsets lie in
  * [-(M-1), M-1]; shifting by M-1 moves them to [0, 2M-2]; the compact
  * (2M-1) x (2M-1) table is read at (dr', dc') and, flattened to 1D, at
@@ -134,20 +158,23 @@ static double dot(const double *a, const double *b, int d)
  *
  *   e_ij = ( q_i.k_j                      content term       (iRPE eq. 13)
  *          + [tab_k] q_i . tab_k[id_ij]   contextual key     (iRPE eq. 15)
- *          + [tab_q] k_j . tab_q[id_ij] ) contextual query   (iRPE eq. 16)
+ *          + [tab_q] k_j . tab_q[id_ij]   contextual query   (iRPE eq. 16)
+ *          + [bias_in] bias_in[id_ij] )   bias mode: a scalar per bucket,
+ *                                         inside the scaling  (iRPE eqs. 13-14)
  *          * scale
  *          + [bias] bias[id_ij]           Swin bias, after the scaling (SWIN)
  *   a_ij = exp(e_ij - max_j e_ij) / sum_j exp(e_ij - max_j e_ij)
  *   z_i  = sum_j a_ij v_j + [tab_v] sum_j a_ij tab_v[id_ij]   (iRPE eq. 17)
  *
- * ids is n x n (query-major); tables are [num_buckets x d]; bias has one
- * scalar per bucket. Any of tab_k, tab_q, tab_v, bias may be NULL (term off).
+ * ids is n x n (query-major); tables are [num_buckets x d]; bias and bias_in
+ * have one scalar per bucket. Any of tab_k, tab_q, tab_v, bias, bias_in may be
+ * NULL (term off).
  * rows lists the query rows to compute (NULL: all n); out and attn are
  * written only at those rows. attn may be NULL. Returns 0, or -1 on a bad id. */
 int orc_attention(int n, int d, const double *q, const double *k, const double *v,
                   const int32_t *ids, int num_buckets,
                   const double *tab_k, const double *tab_q, const double *tab_v,
-                  const double *bias, double scale,
+                  const double *bias, const double *bias_in, double scale,
                   int nrows, const int32_t *rows, double *out, double *attn)
 {
     double *e = (double *)malloc(sizeof(double) * (size_t)n);
@@ -164,6 +191,7 @@ int orc_attention(int n, int d, const double *q, const double *k, const double *
             double logit = dot(qi, kj, d);
             if (tab_k) logit += dot(qi, tab_k + (int64_t)id * d, d);
             if (tab_q) logit += dot(kj, tab_q + (int64_t)id * d, d);
+            if (bias_in) logit += bias_in[id];
             logit *= scale;
             if (bias) logit += bias[id];
             e[j] = logit;
@@ -274,9 +302,48 @@ int orc_irpe_attention(int B, int heads, int H, int W, int d,
                                (flags & ORC_K) ? tab_k : NULL,
                                (flags & ORC_Q) ? tab_q : NULL,
                                (flags & ORC_V) ? tab_v : NULL,
-                               NULL, scale, nrows, rows, out + off, NULL);
+                               NULL, NULL, scale, nrows, rows, out + off, NULL);
     }
     free(ids);
+    return status;
+}
+
+/* iRPE attention over q, k, v [B, heads, N, d] with a caller-given id map
+ * ids [N, N] of num_buckets buckets (any mapping: Product, Euclidean, ...),
+ * head-shared contextual tables selected by flags, and an optional bias-mode
+ * table bias_in [num_buckets, bias_heads] (iRPE eq. 14; bias_heads is 1 for
+ * one table shared by every head, else heads; column h serves head h).
+ * slice_list / rows as for orc_irpe_attention. */
+int orc_irpe_attention_ids(int B, int heads, int N, int d, const int32_t *ids,
+                           int num_buckets, unsigned flags,
+                           const double *q, const double *k, const double *v,
+                           const double *tab_q, const double *tab_k, const double *tab_v,
+                           const double *bias_in, int bias_heads,
+                           int nslices, const int32_t *slice_list,
+                           int nrows, const int32_t *rows, double *out)
+{
+    double *bias = NULL;
+    if (bias_in) {
+        bias = (double *)malloc(sizeof(double) * (size_t)num_buckets);
+        if (!bias) return -2;
+    }
+    double scale = 1.0 / sqrt((double)d);
+    int count = slice_list ? nslices : B * heads;
+    int status = 0;
+    for (int s = 0; s < count && status == 0; ++s) {
+        int64_t bh = slice_list ? slice_list[s] : s;
+        if (bias_in) {
+            int h = bias_heads == 1 ? 0 : (int)(bh % heads);
+            for (int b = 0; b < num_buckets; ++b) bias[b] = bias_in[(int64_t)b * bias_heads + h];
+        }
+        int64_t off = bh * (int64_t)N * d;
+        status = orc_attention(N, d, q + off, k + off, v + off, ids, num_buckets,
+                               (flags & ORC_K) ? tab_k : NULL,
+                               (flags & ORC_Q) ? tab_q : NULL,
+                               (flags & ORC_V) ? tab_v : NULL,
+                               NULL, bias, scale, nrows, rows, out + off, NULL);
+    }
+    free(bias);
     return status;
 }
 
@@ -303,7 +370,7 @@ int orc_swin_attention(int num_windows, int heads, int M, int d,
         for (int b = 0; b < nb; ++b) bias[b] = table[(int64_t)b * heads + h];
         int64_t off = wh * (int64_t)n * d;
         status = orc_attention(n, d, q + off, k + off, v + off, idx, nb,
-                               NULL, NULL, NULL, bias, scale, 0, NULL, out + off, NULL);
+                               NULL, NULL, NULL, bias, NULL, scale, 0, NULL, out + off, NULL);
     }
     free(idx); free(bias);
     return status;

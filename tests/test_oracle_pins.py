@@ -333,3 +333,105 @@ def test_stress_tables_move_output_beyond_tolerance():
     t = 2.0 * _rand((169, 3), 45)
     assert np.max(np.abs(oracle.swin_attention(qs, ks, vs, t, M)
                          - oracle.swin_attention(qs, ks, vs, 0 * t, M))) > 0.2
+
+
+# ------------------------------------------------------------ Euclidean mapping
+
+def test_euclidean_axis_offsets_follow_the_1d_index():
+    # on one axis the distance is the offset's length, so the Euclidean index is
+    # the printed piecewise index of |offset| (shifted by int(beta))
+    rows = read_golden("piecewise_r1p9.txt")
+    alpha, beta, gamma = rows[0]
+    half = int(beta)
+    for H, W in ((1, 56), (56, 1)):
+        ids, K = oracle.euclidean_bucket_ids(H, W, alpha, beta, gamma)
+        assert K == 2 * half + 1
+        for off, idx in rows[1:]:
+            off = int(off)
+            if off < max(H, W):
+                assert ids[0, off] - half == int(idx), (H, W, off)
+                assert ids[off, 0] - half == int(idx), (H, W, off)
+
+
+def test_euclidean_ids_are_undirected_and_axis_symmetric():
+    H, W = 6, 9
+    ids, K = oracle.euclidean_bucket_ids(H, W, *R19)
+    assert np.array_equal(ids, ids.T)          # offset and its negation share a bucket
+    tr, _ = oracle.euclidean_bucket_ids(W, H, *R19)
+    for i in range(H * W):
+        for j in range(H * W):
+            ri, ci, rj, cj = i // W, i % W, j // W, j % W
+            # the same pair with rows and columns swapped
+            assert tr[ci * H + ri, cj * H + rj] == ids[i, j]
+    assert ids.min() >= int(R19[1]) and ids.max() < K   # indices of distances are >= 0
+
+
+def test_euclidean_pythagorean_offsets_hit_exact_distances():
+    rows = dict((int(o), int(i)) for o, i in read_golden("piecewise_r1p9.txt")[1:])
+    H, W = 9, 9
+    ids, _ = oracle.euclidean_bucket_ids(H, W, *R19)
+    half = int(R19[1])
+    for dr, dc, dist in ((3, 4, 5), (4, 3, 5), (6, 8, 10), (8, 6, 10), (0, 7, 7)):
+        i, j = dr * W + dc, 0  # query at (dr, dc), key at (0, 0)
+        assert ids[i, j] - half == rows[dist]
+
+
+# ------------------------------------------------------------ bias mode (eq. 14)
+
+def test_constant_bias_mode_table_is_a_softmax_shift():
+    H, W, d = 4, 5, 8
+    n = H * W
+    q, k, v = _rand((n, d), 40), _rand((n, d), 41), _rand((n, d), 42)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    out = oracle.attention(q, k, v, ids, K, bias_in=np.full(K, 3.7))
+    assert np.max(np.abs(out - _sdpa(q, k, v))) < 1e-12
+
+
+def test_bias_mode_is_added_inside_the_scaling():
+    # b inside the 1/sqrt(d) scaling equals b / sqrt(d) added after it (the
+    # pinned Swin placement); b added after would differ by the factor sqrt(d)
+    H, W, d = 4, 5, 16
+    n = H * W
+    q, k, v = _rand((n, d), 43), _rand((n, d), 44), _rand((n, d), 45)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    b = 3.0 * _rand((K,), 46)
+    inside = oracle.attention(q, k, v, ids, K, bias_in=b)
+    after = oracle.attention(q, k, v, ids, K, bias=b / np.sqrt(d))
+    assert np.max(np.abs(inside - after)) < 1e-12
+    wrong = oracle.attention(q, k, v, ids, K, bias=b)
+    assert np.max(np.abs(inside - wrong)) > 1e-3
+
+
+def test_hard_bias_mode_picks_the_keys_of_one_bucket():
+    # q = k = 0: the logits are the bias alone, so with a large bias on bucket b0
+    # (zero elsewhere) each query averages v over the keys in that bucket
+    H, W, d = 5, 5, 4
+    n = H * W
+    z = np.zeros((n, d))
+    v = _rand((n, d), 47)
+    ids, K = oracle.euclidean_bucket_ids(H, W, *R19)
+    b0 = int(R19[1]) + 1  # distance 1: the four axis neighbours
+    bias = np.zeros(K)
+    bias[b0] = 60.0 * np.sqrt(d)  # 60 after the scaling: other keys weigh ~e^-60
+    out = oracle.attention(z, z, v, ids, K, bias_in=bias)
+    for i in range(n):
+        sel = ids[i] == b0
+        assert sel.sum() >= 2
+        assert np.allclose(out[i], v[sel].mean(axis=0), atol=1e-12)
+
+
+def test_irpe_attention_ids_matches_per_slice_calls():
+    B, heads, H, W, d = 2, 3, 4, 5, 8
+    n = H * W
+    q, k, v = (_rand((B, heads, n, d), s) for s in (50, 51, 52))
+    ids, K = oracle.euclidean_bucket_ids(H, W, *R19)
+    tk = _rand((K, d), 53)
+    bias = _rand((K, heads), 54)
+    out = oracle.irpe_attention_ids(q, k, v, ids, K, 1, tab_k=tk, bias_in=bias)
+    for b in range(B):
+        for h in range(heads):
+            ref = oracle.attention(q[b, h], k[b, h], v[b, h], ids, K, tab_k=tk, bias_in=bias[:, h])
+            assert np.max(np.abs(out[b, h] - ref)) < 1e-12
+    shared = oracle.irpe_attention_ids(q, k, v, ids, K, 0, bias_in=bias[:, 1])
+    ref = oracle.attention(q[1, 2], k[1, 2], v[1, 2], ids, K, bias_in=bias[:, 1])
+    assert np.max(np.abs(shared[1, 2] - ref)) < 1e-12
