@@ -48,8 +48,9 @@ enum {
     RPE_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (device status) */
 };
 
-/* Offset-to-bucket mappings (iRPE section 3.2). Only Product is built. */
-enum { RPE_MAP_PRODUCT = 0 };
+/* Offset-to-bucket mappings (iRPE section 3.2): Product (directed) and
+ * Euclidean (undirected). Cross and Quantization are not built. */
+enum { RPE_MAP_PRODUCT = 0, RPE_MAP_EUCLIDEAN = 1 };
 
 /* Which contextual terms rpe_attn_fwd adds (iRPE eqs. 15-17). */
 enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4 };
@@ -58,14 +59,20 @@ enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4 };
 enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
 
 /*
- * rpe_build_bucket_ids -- iRPE eq. 18 and eq. 25, evaluated on the GPU in
- * double precision.
+ * rpe_build_bucket_ids -- iRPE eq. 18 with the eq. 25 (Product) or the
+ * Euclidean mapping (section 3.2), evaluated on the GPU in double precision.
  *
  * For an H x W grid and index-function constants 0 < alpha <= beta <= gamma
- * (the code's ratio r gives alpha = r, beta = 2r, gamma = 8r), computes the
- * piecewise index g of every axis offset and pairs the row and column
- * indices into the Product bucket
- *     id = (g(dr) + h) * (2h + 1) + (g(dc) + h),   h = int(beta).
+ * (the code's ratio r gives alpha = r, beta = 2r, gamma = 8r), with
+ * h = int(beta):
+ *   RPE_MAP_PRODUCT:   the piecewise index g of every axis offset, the row and
+ *                      column indices paired into one bucket
+ *                        id = (g(dr) + h) * (2h + 1) + (g(dc) + h),
+ *                      (2h + 1)^2 buckets;
+ *   RPE_MAP_EUCLIDEAN: g of the offset's Euclidean length, rounded (half to
+ *                      even) before the index as the original code does,
+ *                        id = g(rint(sqrt(dr^2 + dc^2))) + h,
+ *                      2h + 1 buckets (ids h..2h occur).
  * Outputs (device, int32, written on `stream`):
  *   bucket_lut [(2H-1) * (2W-1)]  id of offset (dr, dc) at
  *                                 (dr + H - 1) * (2W - 1) + (dc + W - 1).
@@ -75,10 +82,10 @@ enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
  *                                 read at each pair's offset.
  *   ids        [N * N] or NULL    the expanded map (query i, key j at i*N + j),
  *                                 N = H * W, read from the same table.
- *   num_buckets (host int*)       set to (2h + 1)^2.
+ *   num_buckets (host int*)       set to the mapping's bucket count.
  * Errors (RPE_ERR_INVALID_ARG): H or W < 1, N*N >= 2^31, alpha <= 0,
- * alpha > beta or beta > gamma or a non-finite constant, mode other than
- * RPE_MAP_PRODUCT, a NULL bucket_lut or num_buckets, (2h+1)^2 > 256.
+ * alpha > beta or beta > gamma or a non-finite constant, an unknown mode, a
+ * NULL bucket_lut or num_buckets, more than 256 buckets.
  */
 int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
                          double gamma, int32_t *bucket_lut, int32_t *ids,
@@ -109,6 +116,25 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
                  const int32_t *bucket_lut, int num_buckets,
                  int B, int heads, int H, int W, int d,
                  unsigned terms, int dtype, void *out, void *stream);
+
+/*
+ * rpe_attn_bias_fwd -- iRPE bias mode on an H x W grid (eqs. 13-14): a learned
+ * scalar per bucket, added to the content logit before the scaling,
+ *
+ *   e_ij  = ( q_i.k_j + b[id(i, j)][h] ) / sqrt(d)
+ *   out_i = sum_j softmax_j(e_ij) v_j
+ *
+ * q, k, v, out : device [B, heads, N, d], N = H * W, element type `dtype`.
+ * bias_table   : device float32 [num_buckets, bias_heads] (bucket-major);
+ *                bias_heads = heads (column h for head h) or 1 (one table
+ *                shared by every head).
+ * bucket_lut, num_buckets: as for rpe_attn_fwd (any mapping).
+ * Supported: RPE_DTYPE_F32 on any grid with d <= 64; RPE_DTYPE_BF16 with
+ * d == 64 and W in {14, 56}; num_buckets <= 64. Errors as for rpe_attn_fwd.
+ */
+int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,
+                      int bias_heads, const int32_t *bucket_lut, int num_buckets, int B,
+                      int heads, int H, int W, int d, int dtype, void *out, void *stream);
 
 /*
  * swin_window_attn_fwd -- Swin window attention with the relative bias

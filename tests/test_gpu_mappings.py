@@ -1,0 +1,131 @@
+"""The Euclidean mapping and iRPE bias mode ("Rethinking and Improving Relative
+Position Encoding for Vision Transformer", Method, section 3.2 and eqs. 13-14)
+on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from vision_transformer_attention_gb300 import api, workloads
+from vision_transformer_attention_gb300._lib import RPE_MAP_EUCLIDEAN, RPE_MAP_PRODUCT, RpeError
+from vision_transformer_attention_gb300.workloads import FLAG_K, FLAG_Q, FLAG_V
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+R19 = workloads.index_constants(1.9)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    yield
+    assert api.rpe_device_status(clear=True) == 0
+
+
+def _maxerr(gpu, ref):
+    return float(np.max(np.abs(gpu.detach().float().cpu().numpy().astype(np.float64) - ref)))
+
+
+def _ids(H, W, mode, consts=R19):
+    if mode == RPE_MAP_EUCLIDEAN:
+        return oracle.euclidean_bucket_ids(H, W, *consts)
+    return oracle.product_bucket_ids(H, W, *consts)
+
+
+@pytest.mark.parametrize("H,W,ratio", [(14, 14, 1.9), (56, 56, 1.9), (5, 9, 1.9), (1, 7, 1.9),
+                                       (14, 14, 2.0), (9, 4, 3.5), (1, 1, 1.9)])
+def test_euclidean_ids_bit_exact(H, W, ratio):
+    consts = workloads.index_constants(ratio)
+    lut, ids, nb = api.rpe_build_bucket_ids(H, W, *consts, with_ids=True, mode=RPE_MAP_EUCLIDEAN)
+    ref, nb_ref = oracle.euclidean_bucket_ids(H, W, *consts)
+    assert nb == nb_ref == 2 * int(consts[1]) + 1
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+# With only 7 Euclidean buckets the value term gathers a row's probability mass
+# on few table rows, and at table_std 1 outputs reach 4, where half a bf16 ulp
+# alone is 2^-6; the value-term case therefore uses table_std 0.5.
+@pytest.mark.parametrize("B,heads,H,W,flags,dtype,table_std", [
+    (2, 3, 14, 14, FLAG_K, "bf16", 1.0),                    # two-warpgroup kernel, W = 14
+    (1, 2, 9, 12, FLAG_K | FLAG_Q | FLAG_V, "bf16", 0.5),   # general kernel
+    (1, 2, 5, 9, FLAG_K | FLAG_V, "f32", 1.0),              # fp32 path
+])
+def test_euclidean_attention_matches_oracle(B, heads, H, W, flags, dtype, table_std):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_EUCLIDEAN)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64 if dtype == "bf16" else 32, nb, flags, dtype,
+                                table_std=table_std, seed=H + W)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = _ids(H, W, RPE_MAP_EUCLIDEAN)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
+                                    tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+def test_euclidean_attention_56x56_sampled():
+    B, heads, H, W = 2, 3, 56, 56
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_EUCLIDEAN)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64, nb, FLAG_K, "bf16", table_std=1.0, seed=7)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, FLAG_K, table_k=g["tab_k"])
+    ids, K = _ids(H, W, RPE_MAP_EUCLIDEAN)
+    rows = np.unique(np.concatenate([np.arange(0, 24), np.arange(1500, 1520), np.arange(3110, 3136)]))
+    sl = np.array([0, 5])
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K,
+                                    tab_k=inp["tab_k"], slices=sl, rows=rows)
+    S = B * heads
+    got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
+
+
+def _bias_case(B, heads, H, W, mode, shared, dtype, table_std, seed):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=mode)
+    d = 64 if dtype == "bf16" else 32
+    inp = workloads.irpe_inputs(B, heads, H * W, d, nb, 0, dtype, seed=seed)
+    bias = workloads.bias_table(nb, 1 if shared else heads, table_std, seed + 100)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], bias.cuda(), lut, nb, H, W)
+    ids, K = _ids(H, W, mode)
+    return inp, bias, ids, K, out
+
+
+@pytest.mark.parametrize("H,W,mode,shared,dtype", [
+    (14, 14, RPE_MAP_PRODUCT, False, "bf16"),
+    (14, 14, RPE_MAP_PRODUCT, True, "bf16"),
+    (14, 14, RPE_MAP_EUCLIDEAN, False, "bf16"),
+    (9, 14, RPE_MAP_PRODUCT, False, "bf16"),     # 126 rows: one query tile per item
+    (5, 9, RPE_MAP_PRODUCT, False, "f32"),
+    (5, 9, RPE_MAP_EUCLIDEAN, True, "f32"),
+])
+def test_bias_mode_matches_oracle(H, W, mode, shared, dtype):
+    inp, bias, ids, K, out = _bias_case(2, 3, H, W, mode, shared, dtype, 2.0, seed=H * W)
+    b = bias.numpy()[:, 0] if shared else bias.numpy()
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=b)
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+    # negative control: at this size the bias moves the output well beyond the tolerance
+    plain = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0)
+    assert np.max(np.abs(plain - ref)) > 3 * TOL_BF16
+
+
+def test_bias_mode_56x56_sampled():
+    B, heads, H, W = 2, 3, 56, 56
+    inp, bias, ids, K, out = _bias_case(B, heads, H, W, RPE_MAP_PRODUCT, False, "bf16", 2.0, seed=9)
+    rows = np.unique(np.concatenate([np.arange(0, 24), np.arange(3110, 3136)]))
+    sl = np.array([1, 4])
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=bias.numpy(),
+                                    slices=sl, rows=rows)
+    S = B * heads
+    got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
+
+
+def test_bias_mode_bf16_unsupported_width_is_an_error():
+    lut, _, nb = api.rpe_build_bucket_ids(6, 9, *R19)
+    inp = workloads.irpe_inputs(1, 2, 54, 64, nb, 0, "bf16")
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    with pytest.raises(RpeError):
+        api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], workloads.bias_table(nb, 2).cuda(), lut, nb, 6, 9)

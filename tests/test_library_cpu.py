@@ -45,7 +45,7 @@ def test_host_argument_checks_reject_before_any_launch():
     nb = ctypes.c_int(0)
     fake = ctypes.c_void_p(1 << 20)
     assert lib.rpe_build_bucket_ids(0, 14, 0, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
-    assert lib.rpe_build_bucket_ids(14, 14, 1, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
+    assert lib.rpe_build_bucket_ids(14, 14, 2, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     assert lib.rpe_build_bucket_ids(14, 14, 0, 3.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     # misaligned pointer
     bad = ctypes.c_void_p((1 << 20) + 4)

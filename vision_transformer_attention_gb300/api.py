@@ -81,6 +81,31 @@ def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, ta
     return out
 
 
+def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=None):
+    """iRPE bias mode (eqs. 13-14) on q, k, v [B, heads, H*W, d]: bias_table is fp32
+    [num_buckets, heads] (per head) or [num_buckets] / [num_buckets, 1] (shared)."""
+    _need(q, "q")
+    B, heads, N, d = q.shape
+    if q.dtype not in _DTYPES:
+        raise TypeError("q must be bfloat16 or float32")
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    if bias_table.dim() == 1:
+        bias_table = bias_table.reshape(-1, 1)
+    bias_heads = bias_table.shape[1]
+    _need(bias_table, "bias_table", torch.float32, (num_buckets, bias_heads), q.device)
+    _need(bucket_lut, "bucket_lut", torch.int32, None, q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", q.dtype, q.shape, q.device)
+    with torch.cuda.device(q.device):
+        check("rpe_attn_bias_fwd", _lib.lib().rpe_attn_bias_fwd(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), bias_heads, _ptr(bucket_lut),
+            num_buckets, B, heads, H, W, d, _DTYPES[q.dtype], _ptr(out), _stream(q)))
+    return out
+
+
 def swin_window_attn_fwd(q, k, v, bias_table, M, out=None):
     """Swin window attention SoftMax(QK^T/sqrt(d) + B)V on [windows, heads, M*M, d]."""
     _need(q, "q")

@@ -118,8 +118,8 @@ extern "C" {
 
 int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, double gamma,
                          int32_t *bucket_lut, int32_t *ids, int *num_buckets, void *stream) {
-    if (H < 1 || W < 1 || mode != RPE_MAP_PRODUCT || bucket_lut == nullptr ||
-        num_buckets == nullptr)
+    if (H < 1 || W < 1 || (mode != RPE_MAP_PRODUCT && mode != RPE_MAP_EUCLIDEAN) ||
+        bucket_lut == nullptr || num_buckets == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (!std::isfinite(alpha) || !std::isfinite(beta) || !std::isfinite(gamma) || alpha <= 0.0 ||
         alpha > beta || beta > gamma || beta >= 127.0)
@@ -128,10 +128,11 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, doub
     if (n * n >= (1LL << 31) || H > 32768 || W > 32768) return RPE_ERR_INVALID_ARG;
     const int half = static_cast<int>(beta);
     const int span = 2 * half + 1;
-    if (span * span > 256) return RPE_ERR_INVALID_ARG;
+    const int nb = mode == RPE_MAP_PRODUCT ? span * span : span;
+    if (nb > 256) return RPE_ERR_INVALID_ARG;
     if (!aligned16(bucket_lut) || (ids != nullptr && !aligned16(ids))) return RPE_ERR_INVALID_ARG;
-    *num_buckets = span * span;
-    return status_of(launch_build_bucket_lut(H, W, alpha, beta, gamma, bucket_lut, ids,
+    *num_buckets = nb;
+    return status_of(launch_build_bucket_lut(H, W, mode, alpha, beta, gamma, bucket_lut, ids,
                                              static_cast<cudaStream_t>(stream)));
 }
 
@@ -177,6 +178,8 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         a.tab_q = (terms & RPE_TERM_Q) ? static_cast<const float *>(table_q) : nullptr;
         a.tab_v = (terms & RPE_TERM_V) ? static_cast<const float *>(table_v) : nullptr;
         a.bias = nullptr;
+        a.bias_heads = 1;
+        a.bias_inside = false;
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }
@@ -197,6 +200,64 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.W = W;
     a.d = d;
     a.terms = terms;
+    return status_of(launch_rpe_bf16(a, st));
+}
+
+int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,
+                      int bias_heads, const int32_t *bucket_lut, int num_buckets, int B,
+                      int heads, int H, int W, int d, int dtype, void *out, void *stream) {
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bias_table == nullptr ||
+        bucket_lut == nullptr)
+        return RPE_ERR_INVALID_ARG;
+    if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
+    if (bias_heads != 1 && bias_heads != heads) return RPE_ERR_INVALID_ARG;
+    if (dtype != RPE_DTYPE_BF16 && dtype != RPE_DTYPE_F32) return RPE_ERR_INVALID_ARG;
+    const void *ptrs[] = {q, k, v, out, bucket_lut, bias_table};
+    for (const void *p : ptrs)
+        if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
+    const long long N = static_cast<long long>(H) * W;
+    const long long slices = static_cast<long long>(B) * heads;
+    if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dtype == RPE_DTYPE_F32) {
+        if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
+        F32AttnArgs a{};
+        a.q = static_cast<const float *>(q);
+        a.k = static_cast<const float *>(k);
+        a.v = static_cast<const float *>(v);
+        a.out = static_cast<float *>(out);
+        a.slices = static_cast<int>(slices);
+        a.heads = heads;
+        a.N = static_cast<int>(N);
+        a.d = d;
+        a.H = H;
+        a.W = W;
+        a.lut = bucket_lut;
+        a.num_buckets = num_buckets;
+        a.bias = bias_table;
+        a.bias_heads = bias_heads;
+        a.bias_inside = true;
+        a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
+        return status_of(launch_attn_f32(a, st));
+    }
+    // bf16: the two-warpgroup kernel, which is specialised for these grid widths
+    if (d != 64 || (W != 14 && W != 56)) return RPE_ERR_UNSUPPORTED;
+    RpeBf16Args a{};
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.out = out;
+    a.lut = bucket_lut;
+    a.num_buckets = num_buckets;
+    a.B = B;
+    a.heads = heads;
+    a.H = H;
+    a.W = W;
+    a.d = d;
+    a.terms = 0;
+    a.bias = bias_table;
+    a.bias_heads = bias_heads;
     return status_of(launch_rpe_bf16(a, st));
 }
 
@@ -228,6 +289,8 @@ int swin_window_attn_fwd(const void *q, const void *k, const void *v, const floa
         a.lut = nullptr;  // the bucket of a pair is its shifted, flattened offset
         a.num_buckets = (2 * M - 1) * (2 * M - 1);
         a.bias = bias_table;
+        a.bias_heads = heads;
+        a.bias_inside = false;
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }

@@ -6,9 +6,9 @@
 //
 // One thread owns one query row. Logits follow the unified form of
 // "Rethinking and Improving Relative Position Encoding for Vision Transformer"
-// (eq. 13, with the contextual key / query terms of eqs. 15-16 inside the
-// 1/sqrt(d) scaling) and the Swin form of "Swin Transformer, section 3.2"
-// (bias added after the scaling). The value term is eq. 17. The softmax takes
+// (eq. 13, with the contextual key / query terms of eqs. 15-16 and the bias
+// mode scalar of eq. 14 inside the 1/sqrt(d) scaling) and the Swin form of
+// "Swin Transformer, section 3.2" (bias added after the scaling). The value term is eq. 17. The softmax takes
 // two passes over the keys, one for the row maximum and normaliser and one
 // for the weighted sum, so nothing needs rescaling.
 #include "vta_internal.h"
@@ -49,8 +49,15 @@ __device__ __forceinline__ float logit(const F32AttnArgs &a, const float (&qi)[k
         const float *r = a.tab_q + static_cast<size_t>(id) * a.d;
         for (int c = 0; c < a.d; ++c) s = fmaf(kj[c], __ldg(r + c), s);
     }
-    s *= a.scale;
-    if (a.bias) s += __ldg(a.bias + static_cast<size_t>(id) * a.heads + head);
+    if (a.bias) {
+        const float b = __ldg(a.bias + static_cast<size_t>(id) * a.bias_heads +
+                              (a.bias_heads == 1 ? 0 : head));
+        if (a.bias_inside) s += b;  // iRPE bias mode (eqs. 13-14)
+        s *= a.scale;
+        if (!a.bias_inside) s += b;  // Swin: after the scaling
+    } else {
+        s *= a.scale;
+    }
     return s;
 }
 

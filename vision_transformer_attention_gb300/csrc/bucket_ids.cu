@@ -1,5 +1,6 @@
-// bucket_ids.cu -- iRPE eq. 18 (piecewise index) and eq. 25 (Product mapping)
-// evaluated on the GPU in double precision.
+// bucket_ids.cu -- iRPE eq. 18 (piecewise index) with the eq. 25 Product
+// mapping or the Euclidean mapping (section 3.2), evaluated on the GPU in
+// double precision.
 //
 // "Rethinking and Improving Relative Position Encoding for Vision Transformer",
 // Method: an axis offset x keeps its own integer index while |x| <= alpha; past
@@ -9,8 +10,13 @@
 // entry of a (2h+1) x (2h+1) table with h = int(beta) (Pitfalls: the table is
 // sized from int(beta), not from beta).
 //
+// The Euclidean id is g of the offset's length, rounded first as the original
+// code does (half to even; a length sqrt(k) is never exactly a half), shifted
+// by int(beta): ids int(beta)..2 int(beta) of 2 int(beta) + 1.
+//
 // A pair's id depends only on its offset, so the attention kernels read ids
 // from a table indexed by offset: lut[(dr + H - 1) * (2W - 1) + dc + W - 1].
+#include "rpe_attn.h"
 #include "vta_internal.h"
 
 #include <algorithm>
@@ -19,8 +25,7 @@
 namespace vta {
 namespace {
 
-__device__ int piecewise_index(int offset, double alpha, double beta, double gamma) {
-    const double x = static_cast<double>(offset);
+__device__ int piecewise_index_real(double x, double alpha, double beta, double gamma) {
     const double ax = fabs(x);
     if (ax <= alpha) return static_cast<int>(rint(x));  // rint: round half to even
     const double share = log(ax / alpha) / log(gamma / alpha);
@@ -29,8 +34,12 @@ __device__ int piecewise_index(int offset, double alpha, double beta, double gam
     return static_cast<int>(x > 0.0 ? capped : -capped);  // the cast truncates toward zero
 }
 
-__global__ void build_lut_kernel(int H, int W, double alpha, double beta, double gamma,
-                                 int32_t *lut) {
+__device__ int piecewise_index(int offset, double alpha, double beta, double gamma) {
+    return piecewise_index_real(static_cast<double>(offset), alpha, beta, gamma);
+}
+
+__global__ void build_lut_kernel(int H, int W, int mode, double alpha, double beta,
+                                 double gamma, int32_t *lut) {
     const int cols = 2 * W - 1;
     const int total = (2 * H - 1) * cols;
     const int half = static_cast<int>(beta);
@@ -38,9 +47,14 @@ __global__ void build_lut_kernel(int H, int W, double alpha, double beta, double
     for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < total; e += gridDim.x * blockDim.x) {
         const int dr = e / cols - (H - 1);
         const int dc = e % cols - (W - 1);
-        const int gr = piecewise_index(dr, alpha, beta, gamma);
-        const int gc = piecewise_index(dc, alpha, beta, gamma);
-        lut[e] = (gr + half) * span + (gc + half);
+        if (mode == RPE_MAP_EUCLIDEAN) {
+            const double dist = rint(sqrt(static_cast<double>(dr) * dr + static_cast<double>(dc) * dc));
+            lut[e] = piecewise_index_real(dist, alpha, beta, gamma) + half;
+        } else {
+            const int gr = piecewise_index(dr, alpha, beta, gamma);
+            const int gc = piecewise_index(dc, alpha, beta, gamma);
+            lut[e] = (gr + half) * span + (gc + half);
+        }
     }
 }
 
@@ -59,10 +73,10 @@ __global__ void expand_ids_kernel(int H, int W, const int32_t *__restrict__ lut,
 
 }  // namespace
 
-cudaError_t launch_build_bucket_lut(int H, int W, double alpha, double beta, double gamma,
-                                    int32_t *lut, int32_t *ids, cudaStream_t stream) {
+cudaError_t launch_build_bucket_lut(int H, int W, int mode, double alpha, double beta,
+                                    double gamma, int32_t *lut, int32_t *ids, cudaStream_t stream) {
     const int total = (2 * H - 1) * (2 * W - 1);
-    build_lut_kernel<<<(total + 255) / 256, 256, 0, stream>>>(H, W, alpha, beta, gamma, lut);
+    build_lut_kernel<<<(total + 255) / 256, 256, 0, stream>>>(H, W, mode, alpha, beta, gamma, lut);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess || ids == nullptr) return err;
     const long long n2 = static_cast<long long>(H * W) * (H * W);

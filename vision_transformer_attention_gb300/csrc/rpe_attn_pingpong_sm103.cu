@@ -100,6 +100,8 @@ struct Geo {
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
     int single;  // 1: an item is one query tile (one group per CTA)
+    const float *bias;  // bias mode: [nb, bias_heads] fp32
+    int bias_heads, heads;
     uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
@@ -187,7 +189,9 @@ __device__ __noinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_ba
 }
 
 // One half (H2 = 0: keys [0, HS) of the tile, 1: keys [HS, 2 HS)) of one row's tile.
-template <int W, bool HK, int H2>
+// GATHER: the logits add a term read by bucket id from a shared-memory table
+// at stride QS floats per bucket (QR' rows: 128; a bias-mode row: 1).
+template <int W, bool GATHER, int H2, int QS = 128>
 struct HalfTile {
     using G = Geo<W>;
     static constexpr int J0 = G::HS * H2;                       // first key of the half
@@ -226,7 +230,7 @@ struct HalfTile {
         for (int q = 0; q < NQ; ++q) {
             const int jc = J0 + 16 * q;
             float qv[16];
-            if constexpr (HK) {
+            if constexpr (GATHER) {
                 // the id words of each grid row, read at the first chunk that needs them
 #pragma unroll
                 for (int rr = 0; rr < NROWS; ++rr) {
@@ -249,7 +253,7 @@ struct HalfTile {
                     if (jj < J0 + NK) {
                         const int r = jj / W, k = c_hi(r) - 1 - jj % W;
                         const uint32_t id = __byte_perm(ida[r - ROW_LO][k / 4], 0u, 0x4440u | (k % 4));
-                        qv[j] = qr_t[id * 128];
+                        qv[j] = qr_t[id * QS];
                     } else {
                         qv[j] = 0.f;
                     }
@@ -329,7 +333,9 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
     return static_cast<uint32_t>((16 * kk / G::HS) * G::HS + ((16 * kk) % G::HS) / 2);
 }
 
-template <int W, bool HK, int NG>
+// BM: iRPE bias mode (a scalar per bucket and head, inside the scaling) in
+// place of the contextual key term; HK and BM are not both set.
+template <int W, bool HK, int NG, bool BM>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -400,7 +406,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     }
     // everything above touches no input: it may overlap the previous kernel
     griddep_wait();
-    if (HK) {
+    if (HK || BM) {
         // offset table as bytes, ids clamped into [0, nb). Keys past the last
         // grid row index up to lut_pad bytes before the table; those bytes hold
         // bucket 0 so every read stays in bounds (those scores are masked).
@@ -608,6 +614,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         // TMA store. A thread reads and writes only its own row of it.
         uint8_t *qr_base = smem + P.off_qr + wg * P.qr_stride;
         float *qr_t = reinterpret_cast<float *>(qr_base) + t;
+        // bias mode: the item's head's bias row, scaled, in the same region
+        float *bias_row = reinterpret_cast<float *>(qr_base);
         const uint32_t stage_row = smem_u32(qr_base) + t * 128;
         const uint32_t *lutw = reinterpret_cast<const uint32_t *>(sLut);
         uint32_t u = 0;  // this group's unit counter
@@ -628,6 +636,13 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag));
             if (!red_and(group_bar, 128, ok)) break;
+            if (BM) {
+                // the item's bias row, pre-scaled like the logits (eq. 13: inside
+                // the 1/sqrt(d) scaling); visible to the group after the barrier
+                const int col = P.bias_heads == 1 ? 0 : I.slice % P.heads;
+                if (t < P.nb) bias_row[t] = __ldg(P.bias + t * P.bias_heads + col) * P.c;
+                named_bar_sync(group_bar, 128);
+            }
             if (HK) {
                 tc_fence_after();
                 if (warp_active) {
@@ -655,7 +670,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
                 if (warp_active) {
-                    const float mt = HalfTile<W, HK, 0>::logits(tSl, lutw, e0, qr_t, P.c);
+                    const float mt = HalfTile<W, HK || BM, 0, BM ? 1 : 128>::logits(
+                        tSl, lutw, e0, BM ? bias_row : qr_t, P.c);
                     // lazy rescale: the reference max moves only when it grows by > 2^8
                     float alpha = 1.f;
                     if (mt > m + kRescaleLog2) {
@@ -665,7 +681,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                     if (kt > 0 && __any_sync(~0u, alpha < 1.f))
                         ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
-                    l += HalfTile<W, HK, 0>::probs(tSl, m);
+                    l += HalfTile<W, HK || BM, 0, BM ? 1 : 128>::probs(tSl, m);
                     tmem_st_wait();
                 }
                 tc_fence_before();
@@ -719,7 +735,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int W, bool HK, int NG>
+template <int W, bool HK, int NG, bool BM>
 cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     using G = Geo<W>;
     using L = Layout<NG>;
@@ -740,6 +756,9 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.nvalid_last = N - (p.nkt - 1) * G::KT;
     p.lut = a.lut;
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
+    p.bias = a.bias;
+    p.bias_heads = a.bias_heads;
+    p.heads = a.heads;
     // per CTA: the SM's 228 KB less 1 KB reserved per CTA
     const uint32_t cap = (228 / L::kCtasPerSm - 1) * 1024;
     uint32_t total = 0;
@@ -759,7 +778,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_mask = off;
         off += 2 * 4096;
         p.off_lut = off;
-        if (HK) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
+        if (HK || BM) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
         off = align_up(off, 1024);
         p.off_kv = off;
         const int room = static_cast<int>((cap - std::min(cap, 1024 + off)) / (2 * G::KV_BYTES));
@@ -789,12 +808,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 2, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG>,
+    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG, BM>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
-    return launch_pdl(rpe_pingpong_kernel<W, HK, NG>, dim3(grid), dim3(L::kThreads), total, stream,
+    return launch_pdl(rpe_pingpong_kernel<W, HK, NG, BM>, dim3(grid), dim3(L::kThreads), total, stream,
                       tq, tk, tv, trk, to, p);
 }
 
@@ -803,11 +822,17 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
     if (a.d != kD || (a.terms & ~1u) != 0 || a.num_buckets > 64) return false;
     const bool hk = (a.terms & 1u) != 0;
+    const bool bm = a.bias != nullptr;
+    if (hk && bm) return false;
     constexpr int NG = kGroupsPerCta;
     if (a.W == 14)
-        *err = hk ? launch_pp<14, true, NG>(a, stream) : launch_pp<14, false, NG>(a, stream);
+        *err = bm ? launch_pp<14, false, NG, true>(a, stream)
+             : hk ? launch_pp<14, true, NG, false>(a, stream)
+                  : launch_pp<14, false, NG, false>(a, stream);
     else if (a.W == 56)
-        *err = hk ? launch_pp<56, true, NG>(a, stream) : launch_pp<56, false, NG>(a, stream);
+        *err = bm ? launch_pp<56, false, NG, true>(a, stream)
+             : hk ? launch_pp<56, true, NG, false>(a, stream)
+                  : launch_pp<56, false, NG, false>(a, stream);
     else
         return false;
     return true;

@@ -601,6 +601,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
     if (launch_rpe_bf16_pingpong(a, stream, &err)) return err;
+    if (a.bias != nullptr) return cudaErrorInvalidValue;  // bias mode: ping-pong kernel only
     const bool k = a.terms & 1u, q = a.terms & 2u, v = a.terms & 4u;
     if (!k && !q && !v) return launch_tmpl<false, false, false>(a, stream);
     if (k && !q && !v) return launch_tmpl<true, false, false>(a, stream);

@@ -47,7 +47,7 @@ bool encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, int rank, co
 
 // ---- launchers (each returns the cudaError_t of its launch) ----
 
-cudaError_t launch_build_bucket_lut(int H, int W, double alpha, double beta, double gamma,
+cudaError_t launch_build_bucket_lut(int H, int W, int mode, double alpha, double beta, double gamma,
                                     int32_t *lut, int32_t *ids, cudaStream_t stream);
 
 struct F32AttnArgs {
@@ -57,7 +57,9 @@ struct F32AttnArgs {
     const int32_t *lut;  // offset -> bucket; NULL: the bucket is the offset index
     int num_buckets;
     const float *tab_k, *tab_q, *tab_v;  // [num_buckets, d] or NULL
-    const float *bias;                   // [num_buckets, heads] or NULL
+    const float *bias;                   // [num_buckets, bias_heads] or NULL
+    int bias_heads;                      // columns of bias: 1 (shared by all heads) or heads
+    bool bias_inside;                    // added before the scaling (iRPE bias mode) or after (Swin)
     float scale;
 };
 cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
@@ -85,6 +87,8 @@ struct RpeBf16Args {
     const int32_t *lut;
     int num_buckets, B, heads, H, W, d;
     unsigned terms;
+    const float *bias = nullptr;  // bias mode: fp32 [num_buckets, bias_heads], inside the scaling
+    int bias_heads = 0;
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 

@@ -166,6 +166,11 @@ def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02
     return out
 
 
+def bias_table(num_buckets, heads, table_std=0.02, seed=6):
+    """iRPE bias-mode table [num_buckets, heads] fp32 (heads = 1: shared)."""
+    return _normal((num_buckets, heads), seed, table_std)
+
+
 def config_inputs(cfg, table_std=0.02, seed=0):
     if isinstance(cfg, SwinConfig) and cfg.fmap:
         b, h, w = cfg.fmap
