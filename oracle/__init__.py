@@ -66,12 +66,16 @@ def _load():
         lib.orc_clip_ids_1d.restype = None
         lib.orc_clip_ids_1d.argtypes = [i32, i32, p]
         lib.orc_attention.restype = i32
-        lib.orc_attention.argtypes = [i32, i32, p, p, p, p, i32, p, p, p, p, p, dbl,
+        lib.orc_attention.argtypes = [i32, i32, p, p, p, p, p, i32, p, p, p, p, p, dbl,
                                       i32, p, p, p]
+        lib.orc_cross_bucket_ids.restype = i32
+        lib.orc_cross_bucket_ids.argtypes = [i32, i32, dbl, dbl, dbl, p, p]
+        lib.orc_clip_product_bucket_ids.restype = i32
+        lib.orc_clip_product_bucket_ids.argtypes = [i32, i32, i32, p]
         lib.orc_euclidean_bucket_ids.restype = i32
         lib.orc_euclidean_bucket_ids.argtypes = [i32, i32, dbl, dbl, dbl, p]
         lib.orc_irpe_attention_ids.restype = i32
-        lib.orc_irpe_attention_ids.argtypes = [i32, i32, i32, i32, p, i32, u32, p, p, p,
+        lib.orc_irpe_attention_ids.argtypes = [i32, i32, i32, i32, p, p, i32, u32, p, p, p,
                                                p, p, p, p, i32, i32, p, i32, p, p]
         lib.orc_attention_efficient.restype = i32
         lib.orc_attention_efficient.argtypes = [i32, i32, p, p, p, p, i32, p, p, p,
@@ -130,21 +134,43 @@ def euclidean_bucket_ids(H: int, W: int, alpha: float, beta: float, gamma: float
     return ids, int(K)
 
 
+def cross_bucket_ids(H: int, W: int, alpha: float, beta: float, gamma: float):
+    """Cross-mapping ids (section 3.2, eqs. 22-24): (ids_row, ids_col, K), both
+    [N, N] int32, row buckets in [0, span), column buckets in [span, 2 span),
+    K = 2 span, span = 2*int(beta)+1."""
+    N = H * W
+    ids_row = np.zeros((N, N), dtype=np.int32)
+    ids_col = np.zeros((N, N), dtype=np.int32)
+    K = _load().orc_cross_bucket_ids(H, W, alpha, beta, gamma, _ptr(ids_row), _ptr(ids_col))
+    return ids_row, ids_col, int(K)
+
+
+def clip_product_bucket_ids(H: int, W: int, k: int):
+    """Product ids of the per-axis clipped offsets (table 3's clip index): (ids, (2k+1)^2)."""
+    N = H * W
+    ids = np.zeros((N, N), dtype=np.int32)
+    K = _load().orc_clip_product_bucket_ids(H, W, k, _ptr(ids))
+    return ids, int(K)
+
+
 def irpe_attention_ids(q, k, v, ids, num_buckets, flags=0, tab_q=None, tab_k=None,
-                       tab_v=None, bias_in=None, slices=None, rows=None):
+                       tab_v=None, bias_in=None, slices=None, rows=None, ids2=None):
     """iRPE attention on [B, heads, N, d] with a given [N, N] id map; bias_in is a
-    bias-mode table [num_buckets, bias_heads] (bias_heads 1 = shared by all heads)."""
+    bias-mode table [num_buckets, bias_heads] (bias_heads 1 = shared by all heads);
+    ids2, a second [N, N] map whose entries are added (the Cross mapping)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, heads, N, d = q.shape
     ids = _i32(ids)
     assert ids.shape == (N, N)
+    ids2 = _i32(ids2)
+    assert ids2 is None or ids2.shape == (N, N)
     tab_q, tab_k, tab_v = _f64(tab_q), _f64(tab_k), _f64(tab_v)
     bias_in = _f64(bias_in)
     bias_heads = 0 if bias_in is None else (1 if bias_in.ndim == 1 else bias_in.shape[1])
     slices, rows = _i32(slices), _i32(rows)
     out = np.zeros_like(q)
     _check(_load().orc_irpe_attention_ids(
-        B, heads, N, d, _ptr(ids), num_buckets, flags, _ptr(q), _ptr(k), _ptr(v),
+        B, heads, N, d, _ptr(ids), _ptr(ids2), num_buckets, flags, _ptr(q), _ptr(k), _ptr(v),
         _ptr(tab_q), _ptr(tab_k), _ptr(tab_v), _ptr(bias_in), bias_heads,
         0 if slices is None else len(slices), _ptr(slices),
         0 if rows is None else len(rows), _ptr(rows), _ptr(out)))
@@ -167,20 +193,22 @@ def clip_ids_1d(n: int, k: int):
 
 
 def attention(q, k, v, ids, num_buckets, tab_k=None, tab_q=None, tab_v=None,
-              bias=None, scale=None, rows=None, want_attn=False, bias_in=None):
+              bias=None, scale=None, rows=None, want_attn=False, bias_in=None, ids2=None):
     """One slice, every pair explicit. q, k, v: [n, d]. Returns out (and attn).
     bias: Swin scalar per bucket after the scaling; bias_in: iRPE bias-mode
-    scalar per bucket inside it."""
+    scalar per bucket inside it; ids2: a second id map added to ids (Cross)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     n, d = q.shape
     ids = _i32(ids)
+    ids2 = _i32(ids2)
     tab_k, tab_q, tab_v, bias = _f64(tab_k), _f64(tab_q), _f64(tab_v), _f64(bias)
     bias_in = _f64(bias_in)
     scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
     rows = _i32(rows)
     out = np.zeros((n, d))
     attn = np.zeros((n, n)) if want_attn else None
-    _check(_load().orc_attention(n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(ids), num_buckets,
+    _check(_load().orc_attention(n, d, _ptr(q), _ptr(k), _ptr(v), _ptr(ids), _ptr(ids2),
+                                 num_buckets,
                                  _ptr(tab_k), _ptr(tab_q), _ptr(tab_v), _ptr(bias),
                                  _ptr(bias_in), scale,
                                  0 if rows is None else len(rows), _ptr(rows),

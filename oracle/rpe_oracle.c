@@ -109,6 +109,52 @@ int orc_euclidean_bucket_ids(int H, int W, double alpha, double beta, double gam
     return 2 * half + 1;
 }
 
+/* iRPE section 3.2, Cross mapping (directed; eqs. 22-24): one bucket for the
+ * row offset and one for the column offset, each through the index function,
+ * with their two encodings added. The table has 2 * (2*int(beta)+1) entries
+ * (section 3.2: 2 x (2 beta + 1) buckets): row buckets first, then column
+ * buckets. Writes ids_row[i*N + j] in [0, span) and ids_col[i*N + j] in
+ * [span, 2*span), span = 2*int(beta)+1; returns 2*span. */
+int orc_cross_bucket_ids(int H, int W, double alpha, double beta, double gamma,
+                         int32_t *ids_row, int32_t *ids_col)
+{
+    int half = (int)beta;
+    int span = 2 * half + 1;
+    int N = H * W;
+    for (int i = 0; i < N; ++i) {
+        int ri = i / W, ci = i % W;
+        for (int j = 0; j < N; ++j) {
+            int rj = j / W, cj = j % W;
+            ids_row[(int64_t)i * N + j] = orc_piecewise_index((double)(ri - rj), alpha, beta, gamma) + half;
+            ids_col[(int64_t)i * N + j] = span + orc_piecewise_index((double)(ci - cj), alpha, beta, gamma) + half;
+        }
+    }
+    return 2 * span;
+}
+
+/* The clip index as a 2D index function (iRPE table 3, "clip versus
+ * piecewise"; the clip of SHAW's embedding-table section): each axis offset,
+ * query minus key as for the piecewise index, is clipped to [-k, k], and the
+ * two clipped offsets form a Product id (eq. 25) over (2k+1)^2 buckets.
+ * Writes ids[i*N + j]; returns (2k+1)^2. */
+int orc_clip_product_bucket_ids(int H, int W, int k, int32_t *ids)
+{
+    int span = 2 * k + 1;
+    int N = H * W;
+    for (int i = 0; i < N; ++i) {
+        int ri = i / W, ci = i % W;
+        for (int j = 0; j < N; ++j) {
+            int dr = ri - j / W, dc = ci - j % W;
+            if (dr < -k) dr = -k;
+            if (dr > k) dr = k;
+            if (dc < -k) dc = -k;
+            if (dc > k) dc = k;
+            ids[(int64_t)i * N + j] = (dr + k) * span + (dc + k);
+        }
+    }
+    return span * span;
+}
+
 /* SWIN2D sections 3.1-3.2: inside an M x M window the offsets lie in
  * [-(M-1), M-1]; shifting by M-1 moves them to [0, 2M-2]; the compact
  * (2M-1) x (2M-1) table is read at (dr', dc') and, flattened to 1D, at
@@ -167,12 +213,14 @@ static double dot(const double *a, const double *b, int d)
  *   z_i  = sum_j a_ij v_j + [tab_v] sum_j a_ij tab_v[id_ij]   (iRPE eq. 17)
  *
  * ids is n x n (query-major); tables are [num_buckets x d]; bias and bias_in
- * have one scalar per bucket. Any of tab_k, tab_q, tab_v, bias, bias_in may be
+ * have one scalar per bucket. ids2, when not NULL, is a second n x n id map
+ * whose entries of every iRPE term (tab_k, tab_q, tab_v, bias_in) are added
+ * to those of ids: the Cross mapping's column buckets (iRPE eqs. 22-24). Any of tab_k, tab_q, tab_v, bias, bias_in may be
  * NULL (term off).
  * rows lists the query rows to compute (NULL: all n); out and attn are
  * written only at those rows. attn may be NULL. Returns 0, or -1 on a bad id. */
 int orc_attention(int n, int d, const double *q, const double *k, const double *v,
-                  const int32_t *ids, int num_buckets,
+                  const int32_t *ids, const int32_t *ids2, int num_buckets,
                   const double *tab_k, const double *tab_q, const double *tab_v,
                   const double *bias, const double *bias_in, double scale,
                   int nrows, const int32_t *rows, double *out, double *attn)
@@ -187,11 +235,18 @@ int orc_attention(int n, int d, const double *q, const double *k, const double *
         for (int j = 0; j < n; ++j) {
             int id = ids[(int64_t)i * n + j];
             if (id < 0 || id >= num_buckets) { free(e); return -1; }
+            int id2 = ids2 ? ids2[(int64_t)i * n + j] : -1;
+            if (ids2 && (id2 < 0 || id2 >= num_buckets)) { free(e); return -1; }
             const double *kj = k + (int64_t)j * d;
             double logit = dot(qi, kj, d);
             if (tab_k) logit += dot(qi, tab_k + (int64_t)id * d, d);
             if (tab_q) logit += dot(kj, tab_q + (int64_t)id * d, d);
             if (bias_in) logit += bias_in[id];
+            if (ids2) {
+                if (tab_k) logit += dot(qi, tab_k + (int64_t)id2 * d, d);
+                if (tab_q) logit += dot(kj, tab_q + (int64_t)id2 * d, d);
+                if (bias_in) logit += bias_in[id2];
+            }
             logit *= scale;
             if (bias) logit += bias[id];
             e[j] = logit;
@@ -212,6 +267,10 @@ int orc_attention(int n, int d, const double *q, const double *k, const double *
             if (tab_v) {
                 const double *rv = tab_v + (int64_t)ids[(int64_t)i * n + j] * d;
                 for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
+                if (ids2) {
+                    rv = tab_v + (int64_t)ids2[(int64_t)i * n + j] * d;
+                    for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
+                }
             }
         }
     }
@@ -298,7 +357,7 @@ int orc_irpe_attention(int B, int heads, int H, int W, int d,
     for (int s = 0; s < count && status == 0; ++s) {
         int64_t bh = slice_list ? slice_list[s] : s;
         int64_t off = bh * (int64_t)N * d;
-        status = orc_attention(N, d, q + off, k + off, v + off, ids, K,
+        status = orc_attention(N, d, q + off, k + off, v + off, ids, NULL, K,
                                (flags & ORC_K) ? tab_k : NULL,
                                (flags & ORC_Q) ? tab_q : NULL,
                                (flags & ORC_V) ? tab_v : NULL,
@@ -310,12 +369,13 @@ int orc_irpe_attention(int B, int heads, int H, int W, int d,
 
 /* iRPE attention over q, k, v [B, heads, N, d] with a caller-given id map
  * ids [N, N] of num_buckets buckets (any mapping: Product, Euclidean, ...),
+ * an optional second map ids2 [N, N] whose entries are added (Cross),
  * head-shared contextual tables selected by flags, and an optional bias-mode
  * table bias_in [num_buckets, bias_heads] (iRPE eq. 14; bias_heads is 1 for
  * one table shared by every head, else heads; column h serves head h).
  * slice_list / rows as for orc_irpe_attention. */
 int orc_irpe_attention_ids(int B, int heads, int N, int d, const int32_t *ids,
-                           int num_buckets, unsigned flags,
+                           const int32_t *ids2, int num_buckets, unsigned flags,
                            const double *q, const double *k, const double *v,
                            const double *tab_q, const double *tab_k, const double *tab_v,
                            const double *bias_in, int bias_heads,
@@ -337,7 +397,7 @@ int orc_irpe_attention_ids(int B, int heads, int N, int d, const int32_t *ids,
             for (int b = 0; b < num_buckets; ++b) bias[b] = bias_in[(int64_t)b * bias_heads + h];
         }
         int64_t off = bh * (int64_t)N * d;
-        status = orc_attention(N, d, q + off, k + off, v + off, ids, num_buckets,
+        status = orc_attention(N, d, q + off, k + off, v + off, ids, ids2, num_buckets,
                                (flags & ORC_K) ? tab_k : NULL,
                                (flags & ORC_Q) ? tab_q : NULL,
                                (flags & ORC_V) ? tab_v : NULL,
@@ -369,7 +429,7 @@ int orc_swin_attention(int num_windows, int heads, int M, int d,
         int h = (int)(wh % heads);
         for (int b = 0; b < nb; ++b) bias[b] = table[(int64_t)b * heads + h];
         int64_t off = wh * (int64_t)n * d;
-        status = orc_attention(n, d, q + off, k + off, v + off, idx, nb,
+        status = orc_attention(n, d, q + off, k + off, v + off, idx, NULL, nb,
                                NULL, NULL, NULL, bias, NULL, scale, 0, NULL, out + off, NULL);
     }
     free(idx); free(bias);

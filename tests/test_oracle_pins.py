@@ -435,3 +435,134 @@ def test_irpe_attention_ids_matches_per_slice_calls():
     shared = oracle.irpe_attention_ids(q, k, v, ids, K, 0, bias_in=bias[:, 1])
     ref = oracle.attention(q[1, 2], k[1, 2], v[1, 2], ids, K, bias_in=bias[:, 1])
     assert np.max(np.abs(shared[1, 2] - ref)) < 1e-12
+
+
+# ------------------------------------------------------------ Cross mapping (eqs. 22-24)
+
+def test_cross_ids_are_the_printed_axis_indices():
+    # a row bucket is g(row offset) alone and a column bucket g(column offset)
+    # alone; 2 x (2 beta + 1) buckets (section 3.2), row buckets first
+    rows = read_golden("piecewise_r1p9.txt")
+    alpha, beta, gamma = rows[0]
+    half = int(beta)
+    span = 2 * half + 1
+    g = dict((int(o), int(i)) for o, i in rows[1:])
+    H, W = 9, 12
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, alpha, beta, gamma)
+    assert K == 2 * span == 14
+    for i in range(H * W):
+        for j in range(H * W):
+            dr, dc = i // W - j // W, i % W - j % W
+            assert ids_row[i, j] == half + (g[dr] if dr >= 0 else -g[-dr])
+            assert ids_col[i, j] == span + half + (g[dc] if dc >= 0 else -g[-dc])
+
+
+def test_cross_and_product_share_their_axis_indices():
+    # eq. 25 pairs the same two axis buckets that eqs. 22-24 add
+    H, W = 7, 11
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, *R19)
+    prod, Kp = oracle.product_bucket_ids(H, W, *R19)
+    span = K // 2
+    assert Kp == span * span
+    assert np.array_equal(prod, ids_row * span + (ids_col - span))
+
+
+def test_cross_terms_are_added():
+    # contextual K, Q, V and bias mode at once: the Cross result equals the
+    # Product result with the joint table T[a span + b] = R[a] + R[span + b]
+    # (encodings added); zeroing one half leaves the other half's single-id
+    # result, so a dropped row or column term fails
+    H, W, d = 4, 6, 8
+    n = H * W
+    q, k, v = _rand((n, d), 60), _rand((n, d), 61), _rand((n, d), 62)
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, *R19)
+    prod, Kp = oracle.product_bucket_ids(H, W, *R19)
+    span = K // 2
+    tk, tq, tv, bi = _rand((K, d), 63), _rand((K, d), 64), _rand((K, d), 65), _rand((K,), 66)
+    cross = oracle.attention(q, k, v, ids_row, K, tab_k=tk, tab_q=tq, tab_v=tv, bias_in=bi,
+                             ids2=ids_col)
+    a, b = np.divmod(np.arange(Kp), span)
+
+    def joint(t):
+        return t[a] + t[span + b]
+
+    ref = oracle.attention(q, k, v, prod, Kp, tab_k=joint(tk), tab_q=joint(tq), tab_v=joint(tv),
+                           bias_in=joint(bi))
+    assert np.max(np.abs(cross - ref)) < 1e-12
+    for keep in (slice(0, span), slice(span, K)):
+        m = np.zeros((K, 1))
+        m[keep] = 1
+        only = oracle.attention(q, k, v, ids_row, K, tab_k=tk * m, tab_q=tq * m, tab_v=tv * m,
+                                bias_in=bi * m[:, 0], ids2=ids_col)
+        single = ids_row if keep.start == 0 else ids_col
+        ref1 = oracle.attention(q, k, v, single, K, tab_k=tk * m, tab_q=tq * m, tab_v=tv * m,
+                                bias_in=bi * m[:, 0])
+        assert np.max(np.abs(only - ref1)) < 1e-12
+    assert np.max(np.abs(cross - oracle.attention(q, k, v, ids_row, K, tab_k=tk, tab_q=tq,
+                                                  tab_v=tv, bias_in=bi))) > 1e-2
+
+
+def test_cross_hard_bias_picks_the_left_neighbour():
+    # q = k = 0; a large bias on row bucket "row offset 0" and on column bucket
+    # "column offset +1" (query minus key): only the key one column to the left
+    # gets both, so each query with a left neighbour returns that key's v
+    H, W, d = 4, 5, 4
+    n = H * W
+    z = np.zeros((n, d))
+    v = _rand((n, d), 67)
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, *R19)
+    half, span = int(R19[1]), K // 2
+    bias = np.zeros(K)
+    bias[half + 0] = 40.0 * np.sqrt(d)
+    bias[span + half + 1] = 40.0 * np.sqrt(d)
+    out = oracle.attention(z, z, v, ids_row, K, bias_in=bias, ids2=ids_col)
+    for i in range(n):
+        if i % W > 0:
+            assert np.allclose(out[i], v[i - 1], atol=1e-12), i
+
+
+# ------------------------------------------------------------ clip index (table 3)
+
+def test_clip_product_on_one_row_is_shaws_1d_clip():
+    # on a 1 x n grid only the column index varies; it is the pinned Shaw clip
+    # of the offset with the opposite sign (Shaw clips key minus query)
+    n, k = 11, 3
+    span = 2 * k + 1
+    ids, K = oracle.clip_product_bucket_ids(1, n, k)
+    assert K == span * span == 49   # table 3: 50 buckets with the class token
+    shaw = oracle.clip_ids_1d(n, k)
+    assert np.array_equal(ids, k * span + (2 * k - shaw))
+
+
+def test_clip_and_piecewise_agree_up_to_their_first_difference():
+    # g is exact up to alpha and g(2) = 2 at r = 1.9, so the two index functions
+    # agree while both axis offsets are within 2; at 3 the piecewise index
+    # still says 2 (the Pitfalls list) where the clip says 3
+    H, W = 9, 9
+    clip, _ = oracle.clip_product_bucket_ids(H, W, 3)
+    pw, _ = oracle.product_bucket_ids(H, W, *R19)
+    for i in range(H * W):
+        for j in range(H * W):
+            dr, dc = abs(i // W - j // W), abs(i % W - j % W)
+            if max(dr, dc) <= 2:
+                assert clip[i, j] == pw[i, j]
+            elif max(dr, dc) == 3:
+                assert clip[i, j] != pw[i, j]
+
+
+def test_clip_product_is_translation_invariant_and_saturates():
+    H, W, k = 8, 10, 2
+    ids, K = oracle.clip_product_bucket_ids(H, W, k)
+    span = 2 * k + 1
+    assert set(np.unique(ids)) == set(range(K))
+    # (0, 0) attending every key at row offset <= -k, column offset <= -k: the corner bucket
+    far = [j for j in range(H * W) if j // W >= k and j % W >= k]
+    assert all(ids[0, j] == 0 for j in far)
+    # pairs with equal offsets share a bucket wherever they sit on the grid
+    seen = {}
+    for i in range(H * W):
+        for j in range(H * W):
+            off = (i // W - j // W, i % W - j % W)
+            assert seen.setdefault(off, ids[i, j]) == ids[i, j]
+    # query (3, 4) vs key (1, 5): offsets (2, -1) -> ((2+k) span + (-1+k))
+    assert ids[3 * W + 4, 1 * W + 5] == (2 + k) * span + (-1 + k)
