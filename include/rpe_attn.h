@@ -48,12 +48,19 @@ enum {
     RPE_ERR_TIMEOUT = 4      /* a bounded in-kernel wait ran out (device status) */
 };
 
-/* Offset-to-bucket mappings (iRPE section 3.2): Product (directed) and
- * Euclidean (undirected). Cross and Quantization are not built. */
-enum { RPE_MAP_PRODUCT = 0, RPE_MAP_EUCLIDEAN = 1 };
+/* Offset-to-bucket mappings (iRPE section 3.2): Product and Cross (directed),
+ * Euclidean (undirected), and the clip index of iRPE table 3 paired as a
+ * Product. Quantization is not built. */
+enum { RPE_MAP_PRODUCT = 0, RPE_MAP_EUCLIDEAN = 1, RPE_MAP_CROSS = 2, RPE_MAP_CLIP_PRODUCT = 3 };
 
-/* Which contextual terms rpe_attn_fwd adds (iRPE eqs. 15-17). */
-enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4 };
+/* Which contextual terms rpe_attn_fwd adds (iRPE eqs. 15-17). RPE_TABLES_CROSS
+ * (also a flag of rpe_attn_bias_fwd) says the tables are laid out for the
+ * Cross mapping: 2 * span rows, the row buckets 0..span-1 then the column
+ * buckets span..2 span-1, with bucket_lut holding the joint index
+ * a * span + b of row bucket a and column bucket span + b (as
+ * rpe_build_bucket_ids writes it for RPE_MAP_CROSS); each pair's term is then
+ * the sum of its row and column entries (eqs. 22-24). span = num_buckets / 2. */
+enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4, RPE_TABLES_CROSS = 8 };
 
 /* Element types of q, k, v, out and the iRPE tables. */
 enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
@@ -72,7 +79,16 @@ enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
  *   RPE_MAP_EUCLIDEAN: g of the offset's Euclidean length, rounded (half to
  *                      even) before the index as the original code does,
  *                        id = g(rint(sqrt(dr^2 + dc^2))) + h,
- *                      2h + 1 buckets (ids h..2h occur).
+ *                      2h + 1 buckets (ids h..2h occur);
+ *   RPE_MAP_CROSS:     a row bucket g(dr) + h and a column bucket
+ *                      (2h + 1) + g(dc) + h, 2 (2h + 1) buckets; the offset
+ *                      table holds the joint index (the Product id above),
+ *                      which the attention calls split with RPE_TABLES_CROSS;
+ *   RPE_MAP_CLIP_PRODUCT: each axis offset clipped to [-h, h] (iRPE table 3,
+ *                      the clip index in place of g), paired as
+ *                        id = (clip(dr) + h) * (2h + 1) + (clip(dc) + h),
+ *                      (2h + 1)^2 buckets; alpha and gamma are checked but
+ *                      not used.
  * Outputs (device, int32, written on `stream`):
  *   bucket_lut [(2H-1) * (2W-1)]  id of offset (dr, dc) at
  *                                 (dr + H - 1) * (2W - 1) + (dc + W - 1).
@@ -81,7 +97,9 @@ enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
  *                                 invariant, so the N x N map is this table
  *                                 read at each pair's offset.
  *   ids        [N * N] or NULL    the expanded map (query i, key j at i*N + j),
- *                                 N = H * W, read from the same table.
+ *                                 N = H * W, read from the same table; for
+ *                                 RPE_MAP_CROSS [2 * N * N]: the row buckets,
+ *                                 then the column buckets.
  *   num_buckets (host int*)       set to the mapping's bucket count.
  * Errors (RPE_ERR_INVALID_ARG): H or W < 1, N*N >= 2^31, alpha <= 0,
  * alpha > beta or beta > gamma or a non-finite constant, an unknown mode, a
@@ -105,10 +123,12 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids (or
  *                any table of ids indexed the same way; an id outside
  *                [0, num_buckets) is clamped into that range).
- * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention).
+ * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention),
+ *                plus RPE_TABLES_CROSS for tables of the Cross mapping.
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);
- * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 64;
+ * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 64
+ * (with RPE_TABLES_CROSS: num_buckets even and (num_buckets / 2)^2 <= 64);
  * N <= 65536. Anything else returns RPE_ERR_UNSUPPORTED.
  */
 int rpe_attn_fwd(const void *q, const void *k, const void *v,
@@ -129,12 +149,17 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
  *                bias_heads = heads (column h for head h) or 1 (one table
  *                shared by every head).
  * bucket_lut, num_buckets: as for rpe_attn_fwd (any mapping).
+ * flags        : 0, or RPE_TABLES_CROSS for a Cross-mapping table (the bias
+ *                of a pair is then b[a][h] + b[span + b'][h] for its joint
+ *                index a * span + b').
  * Supported: RPE_DTYPE_F32 on any grid with d <= 64; RPE_DTYPE_BF16 with
- * d == 64 and W in {14, 56}; num_buckets <= 64. Errors as for rpe_attn_fwd.
+ * d == 64 and W in {14, 56}; num_buckets <= 64 (Cross as for rpe_attn_fwd).
+ * Errors as for rpe_attn_fwd.
  */
 int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,
-                      int bias_heads, const int32_t *bucket_lut, int num_buckets, int B,
-                      int heads, int H, int W, int d, int dtype, void *out, void *stream);
+                      int bias_heads, const int32_t *bucket_lut, int num_buckets,
+                      unsigned flags, int B, int heads, int H, int W, int d, int dtype,
+                      void *out, void *stream);
 
 /*
  * swin_window_attn_fwd -- Swin window attention with the relative bias

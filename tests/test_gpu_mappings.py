@@ -1,13 +1,16 @@
-"""The Euclidean mapping and iRPE bias mode ("Rethinking and Improving Relative
-Position Encoding for Vision Transformer", Method, section 3.2 and eqs. 13-14)
-on the GPU against the oracle."""
+"""The Euclidean and Cross mappings, the clip index and iRPE bias mode
+("Rethinking and Improving Relative Position Encoding for Vision Transformer",
+Method, section 3.2, eqs. 13-14 and 22-24, table 3) on the GPU against the
+oracle."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 from vision_transformer_attention_gb300 import api, workloads
-from vision_transformer_attention_gb300._lib import RPE_MAP_EUCLIDEAN, RPE_MAP_PRODUCT, RpeError
+from vision_transformer_attention_gb300._lib import (RPE_MAP_CLIP_PRODUCT, RPE_MAP_CROSS,
+                                                    RPE_MAP_EUCLIDEAN, RPE_MAP_PRODUCT,
+                                                    RPE_TABLES_CROSS, RpeError)
 from vision_transformer_attention_gb300.workloads import FLAG_K, FLAG_Q, FLAG_V
 
 pytestmark = pytest.mark.gpu
@@ -129,3 +132,105 @@ def test_bias_mode_bf16_unsupported_width_is_an_error():
     g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
     with pytest.raises(RpeError):
         api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], workloads.bias_table(nb, 2).cuda(), lut, nb, 6, 9)
+
+
+# ------------------------------------------------------------ Cross mapping (eqs. 22-24)
+
+@pytest.mark.parametrize("H,W,ratio", [(14, 14, 1.9), (5, 9, 1.9), (56, 56, 1.9), (9, 4, 2.0),
+                                       (1, 1, 1.9)])
+def test_cross_ids_bit_exact(H, W, ratio):
+    consts = workloads.index_constants(ratio)
+    lut, ids, nb = api.rpe_build_bucket_ids(H, W, *consts, with_ids=True, mode=RPE_MAP_CROSS)
+    ref_row, ref_col, nb_ref = oracle.cross_bucket_ids(H, W, *consts)
+    assert nb == nb_ref == 2 * (2 * int(consts[1]) + 1)
+    got = ids.cpu().numpy()
+    assert np.array_equal(got[0], ref_row) and np.array_equal(got[1], ref_col)
+
+
+def _cross_case(B, heads, H, W, flags, dtype, table_std, seed, rows=None, slices=None):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_CROSS)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64 if dtype == "bf16" else 32, nb, flags, dtype,
+                                table_std=table_std, seed=seed)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags | RPE_TABLES_CROSS,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, *R19)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids_row, K, flags,
+                                    tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"],
+                                    ids2=ids_col, rows=rows, slices=slices)
+    return inp, out, ref
+
+
+@pytest.mark.parametrize("B,heads,H,W,flags,dtype,table_std", [
+    (2, 3, 14, 14, FLAG_K, "bf16", 1.0),                    # two-warpgroup kernel
+    (1, 2, 20, 14, FLAG_K, "bf16", 1.0),                    # same, ragged last key tile
+    (1, 2, 9, 12, FLAG_K | FLAG_Q | FLAG_V, "bf16", 0.5),   # general kernel, all terms
+    (1, 2, 11, 7, FLAG_Q | FLAG_V, "bf16", 0.5),
+    (1, 2, 5, 9, FLAG_K | FLAG_Q | FLAG_V, "f32", 1.0),     # fp32 path
+])
+def test_cross_attention_matches_oracle(B, heads, H, W, flags, dtype, table_std):
+    inp, out, ref = _cross_case(B, heads, H, W, flags, dtype, table_std, seed=H * W + flags)
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+    # negative control: the column half of the tables matters beyond the tolerance
+    ids_row, _, K = oracle.cross_bucket_ids(H, W, *R19)
+    rows_only = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids_row, K, flags,
+                                          tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert np.max(np.abs(rows_only - ref)) > 3 * TOL_BF16
+
+
+def test_cross_attention_56x56_sampled():
+    rows = np.unique(np.concatenate([np.arange(0, 24), np.arange(3110, 3136)]))
+    sl = np.array([0, 5])
+    B, heads, H, W = 2, 3, 56, 56
+    _, out, ref = _cross_case(B, heads, H, W, FLAG_K, "bf16", 1.0, seed=11, rows=rows, slices=sl)
+    S = B * heads
+    got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("H,W,dtype", [(14, 14, "bf16"), (5, 9, "f32")])
+def test_cross_bias_mode_matches_oracle(H, W, dtype):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_CROSS)
+    d = 64 if dtype == "bf16" else 32
+    inp = workloads.irpe_inputs(2, 3, H * W, d, nb, 0, dtype, seed=H + 3)
+    bias = workloads.bias_table(nb, 3, 2.0, seed=H + 4)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], bias.cuda(), lut, nb, H, W, cross=True)
+    ids_row, ids_col, K = oracle.cross_bucket_ids(H, W, *R19)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids_row, K, 0,
+                                    bias_in=bias.numpy(), ids2=ids_col)
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+def test_cross_tables_beyond_64_joint_ids_are_refused():
+    lut, _, nb = api.rpe_build_bucket_ids(14, 14, *workloads.index_constants(2.0), mode=RPE_MAP_CROSS)
+    assert nb == 18   # span 9: 81 joint ids
+    inp = workloads.irpe_inputs(1, 1, 196, 64, nb, FLAG_K, "bf16")
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    with pytest.raises(RpeError):
+        api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, 14, 14, FLAG_K | RPE_TABLES_CROSS,
+                         table_k=g["tab_k"])
+
+
+# ------------------------------------------------------------ clip index (table 3)
+
+@pytest.mark.parametrize("H,W,ratio", [(14, 14, 1.9), (7, 20, 1.9), (9, 9, 1.0), (56, 56, 2.0)])
+def test_clip_product_ids_bit_exact(H, W, ratio):
+    consts = workloads.index_constants(ratio)
+    lut, ids, nb = api.rpe_build_bucket_ids(H, W, *consts, with_ids=True, mode=RPE_MAP_CLIP_PRODUCT)
+    ref, nb_ref = oracle.clip_product_bucket_ids(H, W, int(consts[1]))
+    assert nb == nb_ref
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("H,W,flags", [(14, 14, FLAG_K), (6, 10, FLAG_K | FLAG_V)])
+def test_clip_product_attention_matches_oracle(H, W, flags):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_CLIP_PRODUCT)
+    inp = workloads.irpe_inputs(2, 3, H * W, 64, nb, flags, "bf16", table_std=1.0, seed=H + W + 1)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = oracle.clip_product_bucket_ids(H, W, int(R19[1]))
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
+                                    tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= TOL_BF16

@@ -45,7 +45,8 @@ def test_host_argument_checks_reject_before_any_launch():
     nb = ctypes.c_int(0)
     fake = ctypes.c_void_p(1 << 20)
     assert lib.rpe_build_bucket_ids(0, 14, 0, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
-    assert lib.rpe_build_bucket_ids(14, 14, 2, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
+    assert lib.rpe_build_bucket_ids(14, 14, 4, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
+    assert lib.rpe_build_bucket_ids(14, 14, -1, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     assert lib.rpe_build_bucket_ids(14, 14, 0, 3.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     # misaligned pointer
     bad = ctypes.c_void_p((1 << 20) + 4)
@@ -59,6 +60,19 @@ def test_host_argument_checks_reject_before_any_launch():
                             fake, None) == 2
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 49, 1, 1, 14, 14, 32, 1, 0,
                             fake, None) == 2
+    # Cross tables: an odd row count or (rows / 2)^2 joint ids above 64 are not
+    # served; an unknown flag bit is invalid
+    cross_k = _lib.RPE_TERM_K | _lib.RPE_TABLES_CROSS
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 18, 1, 1, 14, 14, 64, cross_k,
+                            0, fake, None) == 2
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 13, 1, 1, 14, 14, 64, cross_k,
+                            0, fake, None) == 2
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 16,
+                            0, fake, None) == 1
+    assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 14, 2, 1, 1, 14, 14, 64, 0,
+                                 fake, None) == 1
+    assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 18, _lib.RPE_TABLES_CROSS, 1, 1,
+                                 14, 14, 64, 0, fake, None) == 2
     assert lib.swin_window_attn_fwd(fake, fake, fake, fake, 4, 3, 8, 32, 0, fake, None) == 2
     assert lib.swin_window_attn_fwd(fake, fake, fake, fake, 0, 3, 7, 32, 0, fake, None) == 1
 

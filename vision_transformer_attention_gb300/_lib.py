@@ -18,7 +18,10 @@ RPE_ERR_CUDA = 3
 RPE_ERR_TIMEOUT = 4
 RPE_MAP_PRODUCT = 0
 RPE_MAP_EUCLIDEAN = 1
+RPE_MAP_CROSS = 2
+RPE_MAP_CLIP_PRODUCT = 3
 RPE_TERM_K, RPE_TERM_Q, RPE_TERM_V = 1, 2, 4
+RPE_TABLES_CROSS = 8
 RPE_DTYPE_BF16, RPE_DTYPE_F32 = 0, 1
 
 # name -> (restype, argtypes) for every symbol the header declares
@@ -29,7 +32,8 @@ SIGNATURES = {
     "swin_window_attn_fwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
     "swin_window_attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p]),
     "swin_window_attn_fwd_fmap": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),
-    "rpe_attn_bias_fwd": (_i, [_p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i, _i, _i, _p, _p]),
+    "rpe_attn_bias_fwd": (_i, [_p, _p, _p, _p, _i, _p, _i, ctypes.c_uint, _i, _i, _i, _i, _i, _i,
+                               _p, _p]),
     "rpe_device_status": (_i, [ctypes.POINTER(_u), _i]),
     "rpe_wait_probe": (_i, [_u64, _p]),
     "rpe_status_string": (ctypes.c_char_p, [_i]),

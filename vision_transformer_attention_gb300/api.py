@@ -40,11 +40,13 @@ def _need(t, name, dtype=None, shape=None, device=None):
 
 def rpe_build_bucket_ids(H, W, alpha, beta, gamma, device="cuda", with_ids=False,
                          mode=_lib.RPE_MAP_PRODUCT):
-    """iRPE eq. 18 + eq. 25 on the GPU. Returns (bucket_lut, ids or None, num_buckets):
-    bucket_lut int32 [(2H-1)*(2W-1)] indexed by offset, ids int32 [N, N]."""
+    """iRPE eq. 18 with a mapping of section 3.2 on the GPU. Returns (bucket_lut, ids or
+    None, num_buckets): bucket_lut int32 [(2H-1)*(2W-1)] indexed by offset, ids int32
+    [N, N] ([2, N, N] for the Cross mapping: row buckets, then column buckets)."""
     device = torch.device(device)
     lut = torch.empty((2 * H - 1) * (2 * W - 1), dtype=torch.int32, device=device)
-    ids = torch.empty((H * W, H * W), dtype=torch.int32, device=device) if with_ids else None
+    shape = (2, H * W, H * W) if mode == _lib.RPE_MAP_CROSS else (H * W, H * W)
+    ids = torch.empty(shape, dtype=torch.int32, device=device) if with_ids else None
     nb = ctypes.c_int(0)
     with torch.cuda.device(device):
         check("rpe_build_bucket_ids", _lib.lib().rpe_build_bucket_ids(
@@ -55,7 +57,8 @@ def rpe_build_bucket_ids(H, W, alpha, beta, gamma, device="cuda", with_ids=False
 
 def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, table_k=None,
                  table_v=None, out=None):
-    """iRPE contextual attention (eqs. 13, 15-17) on q, k, v [B, heads, H*W, d]."""
+    """iRPE contextual attention (eqs. 13, 15-17) on q, k, v [B, heads, H*W, d]; terms
+    may carry RPE_TABLES_CROSS for tables of the Cross mapping (eqs. 22-24)."""
     _need(q, "q")
     B, heads, N, d = q.shape
     if q.dtype not in _DTYPES:
@@ -81,9 +84,10 @@ def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, ta
     return out
 
 
-def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=None):
+def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=None, cross=False):
     """iRPE bias mode (eqs. 13-14) on q, k, v [B, heads, H*W, d]: bias_table is fp32
-    [num_buckets, heads] (per head) or [num_buckets] / [num_buckets, 1] (shared)."""
+    [num_buckets, heads] (per head) or [num_buckets] / [num_buckets, 1] (shared);
+    cross: the table is laid out for the Cross mapping (eqs. 22-24)."""
     _need(q, "q")
     B, heads, N, d = q.shape
     if q.dtype not in _DTYPES:
@@ -102,7 +106,8 @@ def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=No
     with torch.cuda.device(q.device):
         check("rpe_attn_bias_fwd", _lib.lib().rpe_attn_bias_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), bias_heads, _ptr(bucket_lut),
-            num_buckets, B, heads, H, W, d, _DTYPES[q.dtype], _ptr(out), _stream(q)))
+            num_buckets, _lib.RPE_TABLES_CROSS if cross else 0, B, heads, H, W, d,
+            _DTYPES[q.dtype], _ptr(out), _stream(q)))
     return out
 
 

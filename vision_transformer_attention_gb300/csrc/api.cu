@@ -118,7 +118,7 @@ extern "C" {
 
 int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, double gamma,
                          int32_t *bucket_lut, int32_t *ids, int *num_buckets, void *stream) {
-    if (H < 1 || W < 1 || (mode != RPE_MAP_PRODUCT && mode != RPE_MAP_EUCLIDEAN) ||
+    if (H < 1 || W < 1 || mode < RPE_MAP_PRODUCT || mode > RPE_MAP_CLIP_PRODUCT ||
         bucket_lut == nullptr || num_buckets == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (!std::isfinite(alpha) || !std::isfinite(beta) || !std::isfinite(gamma) || alpha <= 0.0 ||
@@ -128,7 +128,7 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, doub
     if (n * n >= (1LL << 31) || H > 32768 || W > 32768) return RPE_ERR_INVALID_ARG;
     const int half = static_cast<int>(beta);
     const int span = 2 * half + 1;
-    const int nb = mode == RPE_MAP_PRODUCT ? span * span : span;
+    const int nb = mode == RPE_MAP_EUCLIDEAN ? span : mode == RPE_MAP_CROSS ? 2 * span : span * span;
     if (nb > 256) return RPE_ERR_INVALID_ARG;
     if (!aligned16(bucket_lut) || (ids != nullptr && !aligned16(ids))) return RPE_ERR_INVALID_ARG;
     *num_buckets = nb;
@@ -143,7 +143,9 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bucket_lut == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
-    if ((terms & ~7u) != 0) return RPE_ERR_INVALID_ARG;
+    if ((terms & ~15u) != 0) return RPE_ERR_INVALID_ARG;
+    const int cross_span = (terms & RPE_TABLES_CROSS) ? num_buckets / 2 : 0;
+    terms &= 7u;
     if (((terms & RPE_TERM_K) && table_k == nullptr) || ((terms & RPE_TERM_Q) && table_q == nullptr) ||
         ((terms & RPE_TERM_V) && table_v == nullptr))
         return RPE_ERR_INVALID_ARG;
@@ -157,11 +159,14 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     const long long N = static_cast<long long>(H) * W;
     const long long slices = static_cast<long long>(B) * heads;
     if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
+        return RPE_ERR_UNSUPPORTED;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
         F32AttnArgs a{};
+        a.cross_span = cross_span;
         a.q = static_cast<const float *>(q);
         a.k = static_cast<const float *>(k);
         a.v = static_cast<const float *>(v);
@@ -200,17 +205,21 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.W = W;
     a.d = d;
     a.terms = terms;
+    a.cross_span = cross_span;
     return status_of(launch_rpe_bf16(a, st));
 }
 
 int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,
-                      int bias_heads, const int32_t *bucket_lut, int num_buckets, int B,
-                      int heads, int H, int W, int d, int dtype, void *out, void *stream) {
+                      int bias_heads, const int32_t *bucket_lut, int num_buckets,
+                      unsigned flags, int B, int heads, int H, int W, int d, int dtype,
+                      void *out, void *stream) {
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bias_table == nullptr ||
         bucket_lut == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
     if (bias_heads != 1 && bias_heads != heads) return RPE_ERR_INVALID_ARG;
+    if ((flags & ~static_cast<unsigned>(RPE_TABLES_CROSS)) != 0) return RPE_ERR_INVALID_ARG;
+    const int cross_span = (flags & RPE_TABLES_CROSS) ? num_buckets / 2 : 0;
     if (dtype != RPE_DTYPE_BF16 && dtype != RPE_DTYPE_F32) return RPE_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, out, bucket_lut, bias_table};
     for (const void *p : ptrs)
@@ -218,11 +227,14 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     const long long N = static_cast<long long>(H) * W;
     const long long slices = static_cast<long long>(B) * heads;
     if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
+        return RPE_ERR_UNSUPPORTED;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
         F32AttnArgs a{};
+        a.cross_span = cross_span;
         a.q = static_cast<const float *>(q);
         a.k = static_cast<const float *>(k);
         a.v = static_cast<const float *>(v);
@@ -258,6 +270,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     a.terms = 0;
     a.bias = bias_table;
     a.bias_heads = bias_heads;
+    a.cross_span = cross_span;
     return status_of(launch_rpe_bf16(a, st));
 }
 

@@ -10,7 +10,9 @@
 // mode scalar of eq. 14 inside the 1/sqrt(d) scaling) and the Swin form of
 // "Swin Transformer, section 3.2" (bias added after the scaling). The value term is eq. 17. The softmax takes
 // two passes over the keys, one for the row maximum and normaliser and one
-// for the weighted sum, so nothing needs rescaling.
+// for the weighted sum, so nothing needs rescaling. With Cross tables (iRPE
+// eqs. 22-24) a pair's joint id a*span + b selects table rows a and span + b,
+// and every term is the sum of the two rows' terms.
 #include "vta_internal.h"
 
 #include <cmath>
@@ -27,18 +29,25 @@ struct SmemF32 {
     float v[kKeys][kMaxD];
 };
 
-__device__ __forceinline__ int bucket_of(const F32AttnArgs &a, int i, int j) {
+// The table rows of a pair: {id, -1}, or for Cross tables {a, span + b} of the
+// joint id a*span + b. Ids outside the table are clamped into it.
+struct Rows {
+    int r0, r1;
+};
+
+__device__ __forceinline__ Rows bucket_of(const F32AttnArgs &a, int i, int j) {
     const int cols = 2 * a.W - 1;
     const int off = (i / a.W - j / a.W + a.H - 1) * cols + (i % a.W - j % a.W + a.W - 1);
-    return a.lut ? __ldg(a.lut + off) : off;
+    int id = a.lut ? __ldg(a.lut + off) : off;
+    const int nid = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
+    id = id < 0 ? 0 : (id >= nid ? nid - 1 : id);
+    if (a.cross_span > 0) return Rows{id / a.cross_span, a.cross_span + id % a.cross_span};
+    return Rows{id, -1};
 }
 
-__device__ __forceinline__ float logit(const F32AttnArgs &a, const float (&qi)[kMaxD],
-                                       const float *kj, int id, int head) {
+__device__ __forceinline__ float table_terms(const F32AttnArgs &a, const float (&qi)[kMaxD],
+                                             const float *kj, int id, int head) {
     float s = 0.f;
-#pragma unroll
-    for (int c = 0; c < kMaxD; ++c)
-        if (c < a.d) s = fmaf(qi[c], kj[c], s);
     if (a.tab_k) {
         const float *r = a.tab_k + static_cast<size_t>(id) * a.d;
 #pragma unroll
@@ -49,12 +58,27 @@ __device__ __forceinline__ float logit(const F32AttnArgs &a, const float (&qi)[k
         const float *r = a.tab_q + static_cast<size_t>(id) * a.d;
         for (int c = 0; c < a.d; ++c) s = fmaf(kj[c], __ldg(r + c), s);
     }
+    if (a.bias && a.bias_inside)
+        s += __ldg(a.bias + static_cast<size_t>(id) * a.bias_heads + (a.bias_heads == 1 ? 0 : head));
+    return s;
+}
+
+__device__ __forceinline__ float logit(const F32AttnArgs &a, const float (&qi)[kMaxD],
+                                       const float *kj, Rows ids, int head) {
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < kMaxD; ++c)
+        if (c < a.d) s = fmaf(qi[c], kj[c], s);
+    // the contextual terms and the iRPE bias (eqs. 13-16), inside the scaling
+    s += table_terms(a, qi, kj, ids.r0, head);
+    if (ids.r1 >= 0) s += table_terms(a, qi, kj, ids.r1, head);
+    const int id = ids.r0;
     if (a.bias) {
-        const float b = __ldg(a.bias + static_cast<size_t>(id) * a.bias_heads +
+        const float b = a.bias_inside ? 0.f
+                      : __ldg(a.bias + static_cast<size_t>(id) * a.bias_heads +
                               (a.bias_heads == 1 ? 0 : head));
-        if (a.bias_inside) s += b;  // iRPE bias mode (eqs. 13-14)
         s *= a.scale;
-        if (!a.bias_inside) s += b;  // Swin: after the scaling
+        s += b;  // Swin: after the scaling
     } else {
         s *= a.scale;
     }
@@ -114,16 +138,22 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(F32AttnArgs a) {
         __syncthreads();
         if (row_ok) {
             for (int jj = 0; jj < nk; ++jj) {
-                const int id = bucket_of(a, i, j0 + jj);
-                const float p = expf(logit(a, qi, sm.k[jj], id, head) - m) * inv_l;
+                const Rows ids = bucket_of(a, i, j0 + jj);
+                const float p = expf(logit(a, qi, sm.k[jj], ids, head) - m) * inv_l;
 #pragma unroll
                 for (int c = 0; c < kMaxD; ++c)
                     if (c < a.d) acc[c] = fmaf(p, sm.v[jj][c], acc[c]);
                 if (a.tab_v) {
-                    const float *r = a.tab_v + static_cast<size_t>(id) * a.d;
+                    const float *r = a.tab_v + static_cast<size_t>(ids.r0) * a.d;
 #pragma unroll
                     for (int c = 0; c < kMaxD; ++c)
                         if (c < a.d) acc[c] = fmaf(p, __ldg(r + c), acc[c]);
+                    if (ids.r1 >= 0) {
+                        r = a.tab_v + static_cast<size_t>(ids.r1) * a.d;
+#pragma unroll
+                        for (int c = 0; c < kMaxD; ++c)
+                            if (c < a.d) acc[c] = fmaf(p, __ldg(r + c), acc[c]);
+                    }
                 }
             }
         }

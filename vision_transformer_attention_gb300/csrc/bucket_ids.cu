@@ -14,6 +14,16 @@
 // code does (half to even; a length sqrt(k) is never exactly a half), shifted
 // by int(beta): ids int(beta)..2 int(beta) of 2 int(beta) + 1.
 //
+// The Cross mapping (eqs. 22-24) gives each pair a row bucket g(dr) + h and a
+// column bucket span + g(dc) + h of a 2 span-row table (span = 2h + 1). Its
+// offset table holds the pair of axis indices as one joint index
+// (g(dr) + h) span + (g(dc) + h), the Product id, from which the attention
+// kernels form the sum of the two entries; the expanded id map holds the two
+// buckets as two N x N planes.
+//
+// The clip index of table 3 replaces g by a clip of each axis offset to
+// [-h, h] and pairs the two as a Product id.
+//
 // A pair's id depends only on its offset, so the attention kernels read ids
 // from a table indexed by offset: lut[(dr + H - 1) * (2W - 1) + dc + W - 1].
 #include "rpe_attn.h"
@@ -50,7 +60,11 @@ __global__ void build_lut_kernel(int H, int W, int mode, double alpha, double be
         if (mode == RPE_MAP_EUCLIDEAN) {
             const double dist = rint(sqrt(static_cast<double>(dr) * dr + static_cast<double>(dc) * dc));
             lut[e] = piecewise_index_real(dist, alpha, beta, gamma) + half;
-        } else {
+        } else if (mode == RPE_MAP_CLIP_PRODUCT) {
+            const int cr = dr < -half ? -half : (dr > half ? half : dr);
+            const int cc = dc < -half ? -half : (dc > half ? half : dc);
+            lut[e] = (cr + half) * span + (cc + half);
+        } else {  // Product, and the joint index of Cross
             const int gr = piecewise_index(dr, alpha, beta, gamma);
             const int gc = piecewise_index(dc, alpha, beta, gamma);
             lut[e] = (gr + half) * span + (gc + half);
@@ -58,7 +72,9 @@ __global__ void build_lut_kernel(int H, int W, int mode, double alpha, double be
     }
 }
 
-__global__ void expand_ids_kernel(int H, int W, const int32_t *__restrict__ lut,
+// span > 0 (Cross): the joint index a span + b becomes row bucket a in the
+// first N x N plane and column bucket span + b in the second.
+__global__ void expand_ids_kernel(int H, int W, int span, const int32_t *__restrict__ lut,
                                   int32_t *__restrict__ ids) {
     const int N = H * W;
     const int cols = 2 * W - 1;
@@ -67,7 +83,13 @@ __global__ void expand_ids_kernel(int H, int W, const int32_t *__restrict__ lut,
          e += static_cast<long long>(gridDim.x) * blockDim.x) {
         const int i = static_cast<int>(e / N), j = static_cast<int>(e % N);
         const int dr = i / W - j / W, dc = i % W - j % W;
-        ids[e] = lut[(dr + H - 1) * cols + (dc + W - 1)];
+        const int id = lut[(dr + H - 1) * cols + (dc + W - 1)];
+        if (span > 0) {
+            ids[e] = id / span;
+            ids[total + e] = span + id % span;
+        } else {
+            ids[e] = id;
+        }
     }
 }
 
@@ -81,7 +103,8 @@ cudaError_t launch_build_bucket_lut(int H, int W, int mode, double alpha, double
     if (err != cudaSuccess || ids == nullptr) return err;
     const long long n2 = static_cast<long long>(H * W) * (H * W);
     const int blocks = static_cast<int>(std::min<long long>((n2 + 255) / 256, 8LL * sm_count()));
-    expand_ids_kernel<<<blocks, 256, 0, stream>>>(H, W, lut, ids);
+    const int span = mode == RPE_MAP_CROSS ? 2 * static_cast<int>(beta) + 1 : 0;
+    expand_ids_kernel<<<blocks, 256, 0, stream>>>(H, W, span, lut, ids);
     return cudaGetLastError();
 }
 

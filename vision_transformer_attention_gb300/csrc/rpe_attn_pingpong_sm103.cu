@@ -100,6 +100,8 @@ struct Geo {
 struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
     int single;  // 1: an item is one query tile (one group per CTA)
+    int cross;     // Cross tables: span (nb = span^2 joint ids); 0 otherwise
+    int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     const float *bias;  // bias mode: [nb, bias_heads] fp32
     int bias_heads, heads;
     uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
@@ -430,8 +432,11 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
                 if (HK) {
+                    // two 32-row boxes: table rows 0.. and rows tab_row2.. (for
+                    // Cross tables the column buckets land at row 32)
                     mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
                     tma_load_2d(sRK, &tm_rk, &bars.tab_full, 0, 0);
+                    tma_load_2d(sRK + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2);
                 }
                 int g = 0, it = 0;
                 int last_q[2] = {-1, -1};
@@ -640,7 +645,13 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 // the item's bias row, pre-scaled like the logits (eq. 13: inside
                 // the 1/sqrt(d) scaling); visible to the group after the barrier
                 const int col = P.bias_heads == 1 ? 0 : I.slice % P.heads;
-                if (t < P.nb) bias_row[t] = __ldg(P.bias + t * P.bias_heads + col) * P.c;
+                if (t < P.nb) {
+                    // Cross: joint id a*span + b takes row bucket a plus column bucket span + b
+                    const int r0 = P.cross ? t / P.cross : t;
+                    float b = __ldg(P.bias + r0 * P.bias_heads + col);
+                    if (P.cross) b += __ldg(P.bias + (P.cross + t % P.cross) * P.bias_heads + col);
+                    bias_row[t] = b * P.c;
+                }
                 named_bar_sync(group_bar, 128);
             }
             if (HK) {
@@ -652,9 +663,21 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     tmem_ld_wait();
                     tmem_ready(r0);
                     tmem_ready(r1);
+                    if (P.cross) {
+                        // joint id a*span + b: row bucket a (column a) plus column
+                        // bucket span + b (staged at table row 32 + b)
 #pragma unroll
-                    for (int b = 0; b < 64; ++b)
-                        if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b] : r1[b - 32]) * P.c;
+                        for (int a = 0; a < 8; ++a)
+#pragma unroll
+                            for (int b = 0; b < 8; ++b)
+                                if (a < P.cross && b < P.cross)
+                                    qr_t[(a * P.cross + b) * 128] =
+                                        (__uint_as_float(r0[a]) + __uint_as_float(r1[b])) * P.c;
+                    } else {
+#pragma unroll
+                        for (int b = 0; b < 64; ++b)
+                            if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b] : r1[b - 32]) * P.c;
+                    }
                 }
                 tc_fence_before();
                 mbar_arrive(&bars.slot_done[wg][slot]);
@@ -743,7 +766,9 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const int N = a.H * a.W;
     p.N = N;
     p.H = a.H;
-    p.nb = a.num_buckets;
+    p.cross = a.cross_span;
+    p.nb = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
+    p.tab_row2 = a.cross_span > 0 ? a.cross_span : 32;
     p.nkt = (a.H + G::R - 1) / G::R;
     p.qtiles = (N + 127) / 128;
     p.pairs_full = p.qtiles / 2;
@@ -798,7 +823,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const uint32_t box_kv[3] = {kD, static_cast<uint32_t>(G::KT), 1};  // one key tile
     const uint64_t tdims[2] = {kD, static_cast<uint64_t>(a.num_buckets)};
     const uint64_t tstrides[1] = {kD * 2};
-    const uint32_t tbox[2] = {kD, 64};
+    const uint32_t tbox[2] = {kD, 32};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     CUtensorMap tq, tk, tv, trk, to;

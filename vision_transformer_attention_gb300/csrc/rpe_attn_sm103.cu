@@ -13,6 +13,15 @@
 // Bucket ids come from a shared-memory copy of the offset table built by
 // rpe_build_bucket_ids; no n x n bias or id map is read from global memory.
 //
+// Cross tables (eqs. 22-24: a row bucket a and a column bucket span + b per
+// pair, their terms added) are staged with the row buckets at rows 0.. and
+// the column buckets at rows 32.. of the shared-memory table, so one product
+// gives both halves' QR / KR columns; the copies into shared memory then hold
+// the joint entry a*span + b as the fp32 sum of the two, and the per-score
+// gather is the same as for one bucket per pair. For the value term the joint
+// probability sums are reduced to per-row-bucket and per-column-bucket sums
+// before the PB R^V product.
+//
 // Structure (one CTA per SM, persistent over (slice, 128-query tile) items):
 //   warp 4  TMA producer: Q tile, then 128-key K/V tiles into a ring.
 //   warp 5  MMA issuer:   QR = Q R^K^T, S = Q K^T (+ KR = K R^Q^T) into one of
@@ -52,6 +61,8 @@ constexpr int kThreads = 192;
 
 struct RpeParams {
     int N, H, W, nb, nkt, qtiles, items, nst;
+    int cross;     // Cross tables: span (nb = span^2 joint ids); 0 otherwise
+    int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
         off_lut;
     int lut_len;
@@ -154,9 +165,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (HV) tab_bytes += kTileBytes / 2;
             if (tab_bytes) {
                 mbar_arrive_expect_tx(&bars.tab_full, tab_bytes);
-                if (HK) tma_load_2d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0);
-                if (HQ) tma_load_2d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0);
-                if (HV) tma_load_2d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0);
+                // each table as two 32-row boxes: rows 0.. and rows tab_row2..
+                if (HK) {
+                    tma_load_2d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0);
+                    tma_load_2d(smem + P.off_rk + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2);
+                }
+                if (HQ) {
+                    tma_load_2d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0);
+                    tma_load_2d(smem + P.off_rq + 4096, &tm_rq, &bars.tab_full, 0, P.tab_row2);
+                }
+                if (HV) {
+                    tma_load_2d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0);
+                    tma_load_2d(smem + P.off_rv + 4096, &tm_rv, &bars.tab_full, 0, P.tab_row2);
+                }
             }
             int g = 0, w = 0;
             int last_kv_use[2] = {-1, -1};
@@ -322,9 +343,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 tmem_ready(r0);
                 tmem_ready(r1);
+                if (P.cross) {
 #pragma unroll
-                for (int b = 0; b < 64; ++b)
-                    if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
+                    for (int a = 0; a < 8; ++a)
+#pragma unroll
+                        for (int b = 0; b < 8; ++b)
+                            if (a < P.cross && b < P.cross)
+                                qr_t[(a * P.cross + b) * 128] =
+                                    (__uint_as_float(r0[a]) + __uint_as_float(r1[b])) * P.c;
+                } else {
+#pragma unroll
+                    for (int b = 0; b < 64; ++b)
+                        if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
+                }
                 tc_fence_before();
                 mbar_arrive(&bars.qr_empty);
             }
@@ -354,9 +385,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ready(r0);
                     tmem_ready(r1);
                     float *kr = sKR + t * kKRStride;
+                    if (P.cross) {
 #pragma unroll
-                    for (int bb = 0; bb < 64; ++bb)
-                        if (bb < P.nb) kr[bb] = __uint_as_float(bb < 32 ? r0[bb & 31] : r1[bb & 31]) * P.c;
+                        for (int a = 0; a < 8; ++a)
+#pragma unroll
+                            for (int bb = 0; bb < 8; ++bb)
+                                if (a < P.cross && bb < P.cross)
+                                    kr[a * P.cross + bb] =
+                                        (__uint_as_float(r0[a]) + __uint_as_float(r1[bb])) * P.c;
+                    } else {
+#pragma unroll
+                        for (int bb = 0; bb < 64; ++bb)
+                            if (bb < P.nb) kr[bb] = __uint_as_float(bb < 32 ? r0[bb & 31] : r1[bb & 31]) * P.c;
+                    }
                 }
                 softmax_bar();
                 uint32_t s[128];
@@ -461,14 +502,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     kStatusTimeoutMma, &abort_flag));
                 ++pw;
                 if (!bar_red_and(ok)) break;
+                // Cross: slot a < 8 takes row bucket a's sum over the joint ids,
+                // slot 32 + b column bucket span + b's (the staged table rows)
+                float rsum[8], csum[8];
+#pragma unroll
+                for (int a = 0; a < 8; ++a) rsum[a] = csum[a] = 0.f;
+                if (P.cross) {
+#pragma unroll
+                    for (int a = 0; a < 8; ++a)
+#pragma unroll
+                        for (int b = 0; b < 8; ++b)
+                            if (a < P.cross && b < P.cross) {
+                                const float pv = pb_t[(a * P.cross + b) * 128];
+                                rsum[a] += pv;
+                                csum[b] += pv;
+                            }
+                }
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int b0 = c * 8 + 2 * e;
-                        const float v0 = b0 < P.nb ? pb_t[b0 * 128] : 0.f;
-                        const float v1 = b0 + 1 < P.nb ? pb_t[(b0 + 1) * 128] : 0.f;
+                        float v0, v1;
+                        if (P.cross) {
+                            v0 = b0 < 8 ? rsum[b0] : (b0 >= 32 && b0 < 40 ? csum[b0 - 32] : 0.f);
+                            v1 = b0 + 1 < 8 ? rsum[b0 + 1]
+                                            : (b0 + 1 >= 32 && b0 + 1 < 40 ? csum[b0 - 31] : 0.f);
+                        } else {
+                            v0 = b0 < P.nb ? pb_t[b0 * 128] : 0.f;
+                            v1 = b0 + 1 < P.nb ? pb_t[(b0 + 1) * 128] : 0.f;
+                        }
                         wv[e] = pack_bf16x2(v0, v1);
                     }
                     st_shared_v4(prow + ((c ^ (t & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
@@ -524,7 +588,9 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     p.N = N;
     p.H = a.H;
     p.W = a.W;
-    p.nb = a.num_buckets;
+    p.cross = a.cross_span;
+    p.nb = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
+    p.tab_row2 = a.cross_span > 0 ? a.cross_span : 32;
     p.nkt = (N + kBN - 1) / kBN;
     p.qtiles = (N + kBM - 1) / kBM;
     p.items = slices * p.qtiles;
@@ -570,7 +636,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
             const uint32_t box[3] = {kD, 128, 1};
             const uint64_t tdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(a.num_buckets)};
             const uint64_t tstrides[1] = {kD * 2};
-            const uint32_t tbox[2] = {kD, 64};
+            const uint32_t tbox[2] = {kD, 32};
             CUtensorMap tq, tk, tv, trk, trq, trv;
             const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
             const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;

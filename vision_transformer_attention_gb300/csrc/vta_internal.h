@@ -61,6 +61,7 @@ struct F32AttnArgs {
     int bias_heads;                      // columns of bias: 1 (shared by all heads) or heads
     bool bias_inside;                    // added before the scaling (iRPE bias mode) or after (Swin)
     float scale;
+    int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
 };
 cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
 
@@ -89,6 +90,7 @@ struct RpeBf16Args {
     unsigned terms;
     const float *bias = nullptr;  // bias mode: fp32 [num_buckets, bias_heads], inside the scaling
     int bias_heads = 0;
+    int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 
