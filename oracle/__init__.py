@@ -76,7 +76,7 @@ def _load():
         lib.orc_euclidean_bucket_ids.argtypes = [i32, i32, dbl, dbl, dbl, p]
         lib.orc_irpe_attention_ids.restype = i32
         lib.orc_irpe_attention_ids.argtypes = [i32, i32, i32, i32, p, p, i32, u32, p, p, p,
-                                               p, p, p, p, i32, i32, p, i32, p, p]
+                                               p, p, p, i32, p, i32, i32, p, i32, p, p]
         lib.orc_attention_efficient.restype = i32
         lib.orc_attention_efficient.argtypes = [i32, i32, p, p, p, p, i32, p, p, p,
                                                 p, dbl, p]
@@ -157,7 +157,9 @@ def irpe_attention_ids(q, k, v, ids, num_buckets, flags=0, tab_q=None, tab_k=Non
                        tab_v=None, bias_in=None, slices=None, rows=None, ids2=None):
     """iRPE attention on [B, heads, N, d] with a given [N, N] id map; bias_in is a
     bias-mode table [num_buckets, bias_heads] (bias_heads 1 = shared by all heads);
-    ids2, a second [N, N] map whose entries are added (the Cross mapping)."""
+    ids2, a second [N, N] map whose entries are added (the Cross mapping).
+    Contextual tables are [num_buckets, d] (shared by every head) or
+    [heads, num_buckets, d] (one per head)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, heads, N, d = q.shape
     ids = _i32(ids)
@@ -165,13 +167,18 @@ def irpe_attention_ids(q, k, v, ids, num_buckets, flags=0, tab_q=None, tab_k=Non
     ids2 = _i32(ids2)
     assert ids2 is None or ids2.shape == (N, N)
     tab_q, tab_k, tab_v = _f64(tab_q), _f64(tab_k), _f64(tab_v)
+    tabs = [t for t in (tab_q, tab_k, tab_v) if t is not None]
+    tab_heads = tabs[0].shape[0] if tabs and tabs[0].ndim == 3 else 1
+    for t in tabs:
+        assert t.shape[-2:] == (num_buckets, d) and (t.ndim == 2 or t.shape[0] == heads)
+        assert t.ndim == tabs[0].ndim  # all shared or all per head
     bias_in = _f64(bias_in)
     bias_heads = 0 if bias_in is None else (1 if bias_in.ndim == 1 else bias_in.shape[1])
     slices, rows = _i32(slices), _i32(rows)
     out = np.zeros_like(q)
     _check(_load().orc_irpe_attention_ids(
         B, heads, N, d, _ptr(ids), _ptr(ids2), num_buckets, flags, _ptr(q), _ptr(k), _ptr(v),
-        _ptr(tab_q), _ptr(tab_k), _ptr(tab_v), _ptr(bias_in), bias_heads,
+        _ptr(tab_q), _ptr(tab_k), _ptr(tab_v), tab_heads, _ptr(bias_in), bias_heads,
         0 if slices is None else len(slices), _ptr(slices),
         0 if rows is None else len(rows), _ptr(rows), _ptr(out)))
     return out

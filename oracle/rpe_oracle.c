@@ -370,6 +370,9 @@ int orc_irpe_attention(int B, int heads, int H, int W, int d,
 /* iRPE attention over q, k, v [B, heads, N, d] with a caller-given id map
  * ids [N, N] of num_buckets buckets (any mapping: Product, Euclidean, ...),
  * an optional second map ids2 [N, N] whose entries are added (Cross),
+ * contextual tables [tab_heads, num_buckets, d] (tab_heads 1: one table shared
+ * by every head; else one per head, head h reading table h; iRPE section 4.2,
+ * table 2: shared or separate per head),
  * head-shared contextual tables selected by flags, and an optional bias-mode
  * table bias_in [num_buckets, bias_heads] (iRPE eq. 14; bias_heads is 1 for
  * one table shared by every head, else heads; column h serves head h).
@@ -378,7 +381,7 @@ int orc_irpe_attention_ids(int B, int heads, int N, int d, const int32_t *ids,
                            const int32_t *ids2, int num_buckets, unsigned flags,
                            const double *q, const double *k, const double *v,
                            const double *tab_q, const double *tab_k, const double *tab_v,
-                           const double *bias_in, int bias_heads,
+                           int tab_heads, const double *bias_in, int bias_heads,
                            int nslices, const int32_t *slice_list,
                            int nrows, const int32_t *rows, double *out)
 {
@@ -397,10 +400,11 @@ int orc_irpe_attention_ids(int B, int heads, int N, int d, const int32_t *ids,
             for (int b = 0; b < num_buckets; ++b) bias[b] = bias_in[(int64_t)b * bias_heads + h];
         }
         int64_t off = bh * (int64_t)N * d;
+        int64_t toff = tab_heads == 1 ? 0 : (bh % heads) * (int64_t)num_buckets * d;
         status = orc_attention(N, d, q + off, k + off, v + off, ids, ids2, num_buckets,
-                               (flags & ORC_K) ? tab_k : NULL,
-                               (flags & ORC_Q) ? tab_q : NULL,
-                               (flags & ORC_V) ? tab_v : NULL,
+                               (flags & ORC_K) ? tab_k + toff : NULL,
+                               (flags & ORC_Q) ? tab_q + toff : NULL,
+                               (flags & ORC_V) ? tab_v + toff : NULL,
                                NULL, bias, scale, nrows, rows, out + off, NULL);
     }
     free(bias);

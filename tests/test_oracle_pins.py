@@ -566,3 +566,30 @@ def test_clip_product_is_translation_invariant_and_saturates():
             assert seen.setdefault(off, ids[i, j]) == ids[i, j]
     # query (3, 4) vs key (1, 5): offsets (2, -1) -> ((2+k) span + (-1+k))
     assert ids[3 * W + 4, 1 * W + 5] == (2 + k) * span + (-1 + k)
+
+
+# ------------------------------------------------------------ per-head tables (section 4.2)
+
+def test_per_head_tables_serve_their_own_head():
+    # head h of every batch reads table h: each slice equals the pinned one-table
+    # attention with that head's tables, and heads given different tables differ
+    B, heads, H, W, d = 2, 3, 4, 5, 8
+    n = H * W
+    q, k, v = (_rand((B, heads, n, d), s) for s in (70, 71, 72))
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    tk, tq, tv = (_rand((heads, K, d), s) for s in (73, 74, 75))
+    out = oracle.irpe_attention_ids(q, k, v, ids, K, 7, tab_q=tq, tab_k=tk, tab_v=tv)
+    for b in range(B):
+        for h in range(heads):
+            ref = oracle.attention(q[b, h], k[b, h], v[b, h], ids, K, tab_k=tk[h], tab_q=tq[h],
+                                   tab_v=tv[h])
+            assert np.max(np.abs(out[b, h] - ref)) < 1e-12
+            if h > 0:
+                other = oracle.attention(q[b, h], k[b, h], v[b, h], ids, K, tab_k=tk[0],
+                                         tab_q=tq[0], tab_v=tv[0])
+                assert np.max(np.abs(out[b, h] - other)) > 1e-2
+    # one table repeated per head is the shared table
+    shared = oracle.irpe_attention_ids(q, k, v, ids, K, 7, tab_q=tq[1], tab_k=tk[1], tab_v=tv[1])
+    rep = oracle.irpe_attention_ids(q, k, v, ids, K, 7, tab_q=np.stack([tq[1]] * heads),
+                                    tab_k=np.stack([tk[1]] * heads), tab_v=np.stack([tv[1]] * heads))
+    assert np.max(np.abs(shared - rep)) < 1e-12
