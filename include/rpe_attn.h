@@ -62,6 +62,11 @@ enum { RPE_MAP_PRODUCT = 0, RPE_MAP_EUCLIDEAN = 1, RPE_MAP_CROSS = 2, RPE_MAP_CL
  * the sum of its row and column entries (eqs. 22-24). span = num_buckets / 2. */
 enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4, RPE_TABLES_CROSS = 8 };
 
+/* Flag of rpe_attn_fwd: the contextual tables are [heads, num_buckets, d], one
+ * per head (head h reads table h), instead of one [num_buckets, d] table
+ * shared by every head (iRPE section 4.2, table 2). */
+enum { RPE_TABLES_PER_HEAD = 16 };
+
 /* Element types of q, k, v, out and the iRPE tables. */
 enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
 
@@ -118,13 +123,15 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *
  * q, k, v, out : device [B, heads, N, d], N = H * W, element type `dtype`.
  * table_q/k/v  : device [num_buckets, d], same element type, shared by all
- *                heads; NULL for a term whose bit is not set in `terms` (a
- *                table whose bit is off is not read).
+ *                heads, or [heads, num_buckets, d] with RPE_TABLES_PER_HEAD;
+ *                NULL for a term whose bit is not set in `terms` (a table
+ *                whose bit is off is not read).
  * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids (or
  *                any table of ids indexed the same way; an id outside
  *                [0, num_buckets) is clamped into that range).
  * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention),
- *                plus RPE_TABLES_CROSS for tables of the Cross mapping.
+ *                plus RPE_TABLES_CROSS for tables of the Cross mapping and
+ *                RPE_TABLES_PER_HEAD for one table per head.
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);
  * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 64

@@ -234,3 +234,52 @@ def test_clip_product_attention_matches_oracle(H, W, flags):
     ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
                                     tab_k=inp["tab_k"], tab_v=inp["tab_v"])
     assert _maxerr(out, ref) <= TOL_BF16
+
+
+# ------------------------------------------------------------ per-head tables (section 4.2)
+
+@pytest.mark.parametrize("B,heads,H,W,flags,mode,dtype,table_std", [
+    (2, 3, 14, 14, FLAG_K, RPE_MAP_PRODUCT, "bf16", 1.0),      # two-warpgroup kernel
+    (3, 2, 20, 14, FLAG_K, RPE_MAP_CROSS, "bf16", 1.0),        # same, Cross tables
+    (2, 3, 10, 10, FLAG_K, RPE_MAP_PRODUCT, "bf16", 1.0),      # general kernel
+    (2, 2, 9, 12, FLAG_K | FLAG_Q | FLAG_V, RPE_MAP_PRODUCT, "bf16", 0.5),
+    (1, 3, 12, 11, FLAG_Q | FLAG_V, RPE_MAP_CROSS, "bf16", 0.5),
+    (2, 2, 5, 9, FLAG_K | FLAG_Q | FLAG_V, RPE_MAP_PRODUCT, "f32", 1.0),
+])
+def test_per_head_tables_match_oracle(B, heads, H, W, flags, mode, dtype, table_std):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=mode)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64 if dtype == "bf16" else 32, nb, flags, dtype,
+                                table_std=table_std, seed=H * W + 5, per_head=True)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    cross = RPE_TABLES_CROSS if mode == RPE_MAP_CROSS else 0
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags | cross,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    if mode == RPE_MAP_CROSS:
+        ids, ids2, K = oracle.cross_bucket_ids(H, W, *R19)
+    else:
+        (ids, K), ids2 = oracle.product_bucket_ids(H, W, *R19), None
+    tabs = {n: inp[n] for n in ("tab_q", "tab_k", "tab_v")}
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, ids2=ids2, **tabs)
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+    # negative control: head 0's tables for every head would fail the bar
+    head0 = {n: (None if t is None else t[0]) for n, t in tabs.items()}
+    shared = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, ids2=ids2,
+                                       **head0)
+    assert np.max(np.abs(shared - ref)) > 3 * TOL_BF16
+
+
+def test_per_head_tables_56x56_sampled():
+    B, heads, H, W = 2, 3, 56, 56
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64, nb, FLAG_K, "bf16", table_std=1.0, seed=13,
+                                per_head=True)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, FLAG_K, table_k=g["tab_k"])
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    rows = np.unique(np.concatenate([np.arange(0, 24), np.arange(3110, 3136)]))
+    sl = np.array([1, 2, 3])
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K,
+                                    tab_k=inp["tab_k"], slices=sl, rows=rows)
+    S = B * heads
+    got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16

@@ -67,7 +67,7 @@ def test_host_argument_checks_reject_before_any_launch():
                             0, fake, None) == 2
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 13, 1, 1, 14, 14, 64, cross_k,
                             0, fake, None) == 2
-    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 16,
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 32,
                             0, fake, None) == 1
     assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 14, 2, 1, 1, 14, 14, 64, 0,
                                  fake, None) == 1

@@ -58,7 +58,9 @@ def rpe_build_bucket_ids(H, W, alpha, beta, gamma, device="cuda", with_ids=False
 def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, table_k=None,
                  table_v=None, out=None):
     """iRPE contextual attention (eqs. 13, 15-17) on q, k, v [B, heads, H*W, d]; terms
-    may carry RPE_TABLES_CROSS for tables of the Cross mapping (eqs. 22-24)."""
+    may carry RPE_TABLES_CROSS for tables of the Cross mapping (eqs. 22-24). Tables
+    are [num_buckets, d] (shared by every head) or [heads, num_buckets, d] (one per
+    head; RPE_TABLES_PER_HEAD is then set here)."""
     _need(q, "q")
     B, heads, N, d = q.shape
     if q.dtype not in _DTYPES:
@@ -68,9 +70,14 @@ def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, ta
     _need(bucket_lut, "bucket_lut", torch.int32, ((2 * H - 1) * (2 * W - 1),), q.device)
     tabs = {"table_q": (table_q, _lib.RPE_TERM_Q), "table_k": (table_k, _lib.RPE_TERM_K),
             "table_v": (table_v, _lib.RPE_TERM_V)}
+    used = [t for t, bit in tabs.values() if terms & bit]
+    per_head = bool(used) and used[0].dim() == 3
     for name, (t, bit) in tabs.items():
         if terms & bit:
-            _need(t, name, q.dtype, (num_buckets, d), q.device)
+            _need(t, name, q.dtype, (heads, num_buckets, d) if per_head else (num_buckets, d),
+                  q.device)
+    if per_head:
+        terms |= _lib.RPE_TABLES_PER_HEAD
     if out is None:
         out = torch.empty_like(q)
     else:

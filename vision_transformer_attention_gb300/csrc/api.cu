@@ -143,8 +143,9 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bucket_lut == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
-    if ((terms & ~15u) != 0) return RPE_ERR_INVALID_ARG;
+    if ((terms & ~31u) != 0) return RPE_ERR_INVALID_ARG;
     const int cross_span = (terms & RPE_TABLES_CROSS) ? num_buckets / 2 : 0;
+    const int tab_heads = (terms & RPE_TABLES_PER_HEAD) ? heads : 1;
     terms &= 7u;
     if (((terms & RPE_TERM_K) && table_k == nullptr) || ((terms & RPE_TERM_Q) && table_q == nullptr) ||
         ((terms & RPE_TERM_V) && table_v == nullptr))
@@ -182,6 +183,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         a.tab_k = (terms & RPE_TERM_K) ? static_cast<const float *>(table_k) : nullptr;
         a.tab_q = (terms & RPE_TERM_Q) ? static_cast<const float *>(table_q) : nullptr;
         a.tab_v = (terms & RPE_TERM_V) ? static_cast<const float *>(table_v) : nullptr;
+        a.tab_heads = tab_heads;
         a.bias = nullptr;
         a.bias_heads = 1;
         a.bias_inside = false;
@@ -206,6 +208,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.d = d;
     a.terms = terms;
     a.cross_span = cross_span;
+    a.tab_heads = tab_heads;
     return status_of(launch_rpe_bf16(a, st));
 }
 

@@ -45,17 +45,23 @@ __device__ __forceinline__ Rows bucket_of(const F32AttnArgs &a, int i, int j) {
     return Rows{id, -1};
 }
 
+// Offset of head `head`'s contextual tables: 0 when one table serves every head.
+__device__ __forceinline__ size_t table_offset(const F32AttnArgs &a, int head) {
+    return a.tab_heads > 1 ? static_cast<size_t>(head) * a.num_buckets * a.d : 0;
+}
+
 __device__ __forceinline__ float table_terms(const F32AttnArgs &a, const float (&qi)[kMaxD],
                                              const float *kj, int id, int head) {
     float s = 0.f;
+    const size_t toff = table_offset(a, head);
     if (a.tab_k) {
-        const float *r = a.tab_k + static_cast<size_t>(id) * a.d;
+        const float *r = a.tab_k + toff + static_cast<size_t>(id) * a.d;
 #pragma unroll
         for (int c = 0; c < kMaxD; ++c)
             if (c < a.d) s = fmaf(qi[c], __ldg(r + c), s);
     }
     if (a.tab_q) {
-        const float *r = a.tab_q + static_cast<size_t>(id) * a.d;
+        const float *r = a.tab_q + toff + static_cast<size_t>(id) * a.d;
         for (int c = 0; c < a.d; ++c) s = fmaf(kj[c], __ldg(r + c), s);
     }
     if (a.bias && a.bias_inside)
@@ -144,12 +150,13 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(F32AttnArgs a) {
                 for (int c = 0; c < kMaxD; ++c)
                     if (c < a.d) acc[c] = fmaf(p, sm.v[jj][c], acc[c]);
                 if (a.tab_v) {
-                    const float *r = a.tab_v + static_cast<size_t>(ids.r0) * a.d;
+                    const float *tv = a.tab_v + table_offset(a, head);
+                    const float *r = tv + static_cast<size_t>(ids.r0) * a.d;
 #pragma unroll
                     for (int c = 0; c < kMaxD; ++c)
                         if (c < a.d) acc[c] = fmaf(p, __ldg(r + c), acc[c]);
                     if (ids.r1 >= 0) {
-                        r = a.tab_v + static_cast<size_t>(ids.r1) * a.d;
+                        r = tv + static_cast<size_t>(ids.r1) * a.d;
 #pragma unroll
                         for (int c = 0; c < kMaxD; ++c)
                             if (c < a.d) acc[c] = fmaf(p, __ldg(r + c), acc[c]);

@@ -101,6 +101,7 @@ struct PPParams {
     int N, H, nb, nkt, qtiles, pairs_full, slices, items, nst, nq;
     int single;  // 1: an item is one query tile (one group per CTA)
     int cross;     // Cross tables: span (nb = span^2 joint ids); 0 otherwise
+    int tab_heads; // 1: one R^K shared by every head; heads: one per head
     int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     const float *bias;  // bias mode: [nb, bias_heads] fp32
     int bias_heads, heads;
@@ -431,12 +432,12 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
-                if (HK) {
+                if (HK && P.tab_heads == 1) {
                     // two 32-row boxes: table rows 0.. and rows tab_row2.. (for
                     // Cross tables the column buckets land at row 32)
                     mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
-                    tma_load_2d(sRK, &tm_rk, &bars.tab_full, 0, 0);
-                    tma_load_2d(sRK + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2);
+                    tma_load_3d(sRK, &tm_rk, &bars.tab_full, 0, 0, 0);
+                    tma_load_3d(sRK + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2, 0);
                 }
                 int g = 0, it = 0;
                 int last_q[2] = {-1, -1};
@@ -450,7 +451,17 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                                          &abort_flag)))
                         break;
                     uint8_t *qd = sQ + qb * NG * kTileBytes;
-                    mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes);
+                    // per-head tables travel with the item's Q tiles: the Q buffer's
+                    // release (after both groups' last products) frees its table too
+                    const bool tab_item = HK && P.tab_heads > 1;
+                    mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes +
+                                                                (tab_item ? kTileBytes / 2 : 0));
+                    if (tab_item) {
+                        uint8_t *rd = sRK + qb * (kTileBytes / 2);
+                        const int head = I.slice % P.heads;
+                        tma_load_3d(rd, &tm_rk, &bars.q_full[qb], 0, 0, head);
+                        tma_load_3d(rd + 4096, &tm_rk, &bars.q_full[qb], 0, P.tab_row2, head);
+                    }
                     tma_load_3d(qd, &tm_q, &bars.q_full[qb], 0, I.qt0 * 128, I.slice);
                     if (I.has_b)
                         tma_load_3d(qd + kTileBytes, &tm_q, &bars.q_full[qb], 0, (I.qt0 + 1) * 128,
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                 }
                 // drain: the most recent load on every barrier has landed
-                if (HK) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+                if (HK && P.tab_heads == 1) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
                 for (int b = 0; b < 2; ++b)
                     if (last_q[b] >= 0)
                         mbar_wait(&bars.q_full[b], last_q[b] & 1, drain, kStatusTimeoutDrain, nullptr);
@@ -503,7 +514,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 uint32_t u = 0;  // units issued
                 int ci = 0;      // items whose last P V was issued
                 bool ok = true;
-                if (HK) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+                if (HK && P.tab_heads == 1) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
                 // consume the oldest outstanding unit: wait until the group has
                 // released it, then issue its P V
                 auto consume = [&]() {
@@ -561,7 +572,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         uint32_t code;
                         if (kt < 0) {
                             tc_fence_after();
-                            const uint64_t dRK = hi128 | (smem_u32(sRK) >> 4);
+                            const uint32_t rk_off = P.tab_heads > 1 ? qb * (kTileBytes / 2) : 0;
+                            const uint64_t dRK = hi128 | (smem_u32(sRK + rk_off) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
                                 mma_bf16_ss(dS, dQ + kk * 2, dRK + kk * 2, kIdQR, kk > 0);
@@ -769,6 +781,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     p.cross = a.cross_span;
     p.nb = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
     p.tab_row2 = a.cross_span > 0 ? a.cross_span : 32;
+    p.tab_heads = a.tab_heads;
     p.nkt = (a.H + G::R - 1) / G::R;
     p.qtiles = (N + 127) / 128;
     p.pairs_full = p.qtiles / 2;
@@ -795,7 +808,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_q = off;
         off += nq * NG * kTileBytes;
         p.off_rk = off;
-        if (HK) off += kTileBytes / 2;
+        if (HK) off += (a.tab_heads > 1 ? nq : 1) * (kTileBytes / 2);
         p.off_qr = off;
         // each group's QR' table doubles as its 16 KB output staging tile
         p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, 128 * 128), 1024);
@@ -821,9 +834,11 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(N) * kD * 2};
     const uint32_t box[3] = {kD, 128, 1};
     const uint32_t box_kv[3] = {kD, static_cast<uint32_t>(G::KT), 1};  // one key tile
-    const uint64_t tdims[2] = {kD, static_cast<uint64_t>(a.num_buckets)};
-    const uint64_t tstrides[1] = {kD * 2};
-    const uint32_t tbox[2] = {kD, 32};
+    // tables [tab_heads][num_buckets][d]
+    const uint64_t tdims[3] = {kD, static_cast<uint64_t>(a.num_buckets),
+                               static_cast<uint64_t>(a.tab_heads)};
+    const uint64_t tstrides[2] = {kD * 2, static_cast<uint64_t>(a.num_buckets) * kD * 2};
+    const uint32_t tbox[3] = {kD, 32, 1};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
     CUtensorMap tq, tk, tv, trk, to;
@@ -831,7 +846,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&to, bf, 3, a.out, dims, strides, box, sw) ||
         !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
-        !encode_tensor_map(&trk, bf, 2, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
+        !encode_tensor_map(&trk, bf, 3, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
     cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG, BM>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,

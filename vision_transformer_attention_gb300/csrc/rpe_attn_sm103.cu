@@ -63,6 +63,7 @@ struct RpeParams {
     int N, H, W, nb, nkt, qtiles, items, nst;
     int cross;     // Cross tables: span (nb = span^2 joint ids); 0 otherwise
     int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
+    int tab_heads, heads;  // tab_heads 1: tables shared by every head; heads: one per head
     uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
         off_lut;
     int lut_len;
@@ -73,7 +74,7 @@ struct RpeParams {
 };
 
 struct Bars {
-    uint64_t tab_full, q_full, q_empty, qr_full, qr_empty, o_full, o_empty, p_full, p_empty;
+    uint64_t tab_full, tab_empty, q_full, q_empty, qr_full, qr_empty, o_full, o_empty, p_full, p_empty;
     uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2];
 };
 
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&bars.tab_full, 1);
+        mbar_init(&bars.tab_empty, 1);
         mbar_init(&bars.q_full, 1);
         mbar_init(&bars.q_empty, 1);
         mbar_init(&bars.qr_full, 1);
@@ -163,25 +165,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (HK) tab_bytes += kTileBytes / 2;
             if (HQ) tab_bytes += kTileBytes / 2;
             if (HV) tab_bytes += kTileBytes / 2;
-            if (tab_bytes) {
+            // each table as two 32-row boxes: rows 0.. and rows tab_row2.. of
+            // table `head` ([tab_heads][rows][d])
+            auto load_tables = [&](int head) {
                 mbar_arrive_expect_tx(&bars.tab_full, tab_bytes);
-                // each table as two 32-row boxes: rows 0.. and rows tab_row2..
                 if (HK) {
-                    tma_load_2d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0);
-                    tma_load_2d(smem + P.off_rk + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2);
+                    tma_load_3d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0, head);
+                    tma_load_3d(smem + P.off_rk + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2, head);
                 }
                 if (HQ) {
-                    tma_load_2d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0);
-                    tma_load_2d(smem + P.off_rq + 4096, &tm_rq, &bars.tab_full, 0, P.tab_row2);
+                    tma_load_3d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0, head);
+                    tma_load_3d(smem + P.off_rq + 4096, &tm_rq, &bars.tab_full, 0, P.tab_row2, head);
                 }
                 if (HV) {
-                    tma_load_2d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0);
-                    tma_load_2d(smem + P.off_rv + 4096, &tm_rv, &bars.tab_full, 0, P.tab_row2);
+                    tma_load_3d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0, head);
+                    tma_load_3d(smem + P.off_rv + 4096, &tm_rv, &bars.tab_full, 0, P.tab_row2, head);
                 }
-            }
+            };
+            // Shared tables are loaded once. Per-head tables are loaded for every
+            // item once the previous item's products are done with them, after
+            // the item's first K/V tile so that load is not held up.
+            const bool per_head = tab_bytes != 0 && P.tab_heads > 1;
+            if (tab_bytes && !per_head) load_tables(0);
             int g = 0, w = 0;
             int last_kv_use[2] = {-1, -1};
-            int last_q = -1;
+            int last_q = -1, last_tab = -1;
             for (int item = blockIdx.x; item < P.items; item += gridDim.x, ++w) {
                 const int slice = item / P.qtiles, qt = item % P.qtiles;
                 if (!mbar_wait(&bars.q_empty, (w & 1) ^ 1, wc, kStatusTimeoutSync, &abort_flag)) break;
@@ -201,11 +209,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tma_load_3d(kb, &tm_k, &bars.kv_full[st], 0, kt * kBN, slice);
                     tma_load_3d(kb + kTileBytes, &tm_v, &bars.kv_full[st], 0, kt * kBN, slice);
                     last_kv_use[st] = use;
+                    if (per_head && kt == 0) {
+                        if (w > 0 && !mbar_wait(&bars.tab_empty, (w - 1) & 1, wc, kStatusTimeoutSync,
+                                                &abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        load_tables(slice % P.heads);
+                        last_tab = w;
+                    }
                 }
                 if (!ok) break;
             }
             // drain: the most recent load on every barrier has landed
-            if (tab_bytes) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+            if (tab_bytes && !per_head) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+            if (last_tab >= 0) mbar_wait(&bars.tab_full, last_tab & 1, drain, kStatusTimeoutDrain, nullptr);
             if (last_q >= 0) mbar_wait(&bars.q_full, last_q & 1, drain, kStatusTimeoutDrain, nullptr);
             for (int st = 0; st < 2; ++st)
                 if (last_kv_use[st] >= 0)
@@ -228,10 +246,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_par = parity;
             };
             bool ok = true;
-            if (HK || HQ || HV) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+            const bool per_head = (HK || HQ || HV) && P.tab_heads > 1;
+            if ((HK || HQ || HV) && !per_head)
+                ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
             int g = 0, w = 0, pr = 0;
             for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++w) {
                 if (!(ok = mbar_wait(&bars.q_full, w & 1, wc, kStatusTimeoutLoad, &abort_flag))) break;
+                if (per_head && !(ok = mbar_wait(&bars.tab_full, w & 1, wc, kStatusTimeoutLoad, &abort_flag)))
+                    break;
                 tc_fence_after();
                 if (HK) {
                     if (!(ok = mbar_wait(&bars.qr_empty, (w & 1) ^ 1, wc, kStatusTimeoutSync,
@@ -312,6 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     commit(&bars.p_empty, (pr - 1) & 1);
                 }
                 commit(&bars.o_full, w & 1);
+                // every product of the item that reads the tables is done with them
+                if (per_head) commit(&bars.tab_empty, w & 1);
             }
             // drain: tcgen05 work completes in order, so the last commit covers it all
             if (last_bar != nullptr) mbar_wait(last_bar, last_par, drain, kStatusTimeoutDrain, nullptr);
@@ -591,6 +615,8 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     p.cross = a.cross_span;
     p.nb = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
     p.tab_row2 = a.cross_span > 0 ? a.cross_span : 32;
+    p.tab_heads = a.tab_heads;
+    p.heads = a.heads;
     p.nkt = (N + kBN - 1) / kBN;
     p.qtiles = (N + kBM - 1) / kBM;
     p.items = slices * p.qtiles;
@@ -634,9 +660,11 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
                                       static_cast<uint64_t>(slices)};
             const uint64_t strides[2] = {kD * 2, static_cast<uint64_t>(N) * kD * 2};
             const uint32_t box[3] = {kD, 128, 1};
-            const uint64_t tdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(a.num_buckets)};
-            const uint64_t tstrides[1] = {kD * 2};
-            const uint32_t tbox[2] = {kD, 32};
+            // tables [tab_heads][num_buckets][d]
+            const uint64_t tdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(a.num_buckets),
+                                       static_cast<uint64_t>(a.tab_heads)};
+            const uint64_t tstrides[2] = {kD * 2, static_cast<uint64_t>(a.num_buckets) * kD * 2};
+            const uint32_t tbox[3] = {kD, 32, 1};
             CUtensorMap tq, tk, tv, trk, trq, trv;
             const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
             const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -646,9 +674,9 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
                 return cudaErrorInvalidValue;
             // tables not in use get a valid (never read) map over q
             const void *rk = HK ? a.tab_k : a.q, *rq = HQ ? a.tab_q : a.q, *rv = HV ? a.tab_v : a.q;
-            if (!encode_tensor_map(&trk, bf, 2, rk, tdims, tstrides, tbox, sw) ||
-                !encode_tensor_map(&trq, bf, 2, rq, tdims, tstrides, tbox, sw) ||
-                !encode_tensor_map(&trv, bf, 2, rv, tdims, tstrides, tbox, sw))
+            if (!encode_tensor_map(&trk, bf, 3, rk, tdims, tstrides, tbox, sw) ||
+                !encode_tensor_map(&trq, bf, 3, rq, tdims, tstrides, tbox, sw) ||
+                !encode_tensor_map(&trv, bf, 3, rv, tdims, tstrides, tbox, sw))
                 return cudaErrorInvalidValue;
             cudaError_t err = cudaFuncSetAttribute(rpe_bf16_kernel<HK, HQ, HV>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,

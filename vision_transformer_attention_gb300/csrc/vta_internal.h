@@ -62,6 +62,7 @@ struct F32AttnArgs {
     bool bias_inside;                    // added before the scaling (iRPE bias mode) or after (Swin)
     float scale;
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
+    int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
 };
 cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
 
@@ -91,6 +92,7 @@ struct RpeBf16Args {
     const float *bias = nullptr;  // bias mode: fp32 [num_buckets, bias_heads], inside the scaling
     int bias_heads = 0;
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
+    int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 

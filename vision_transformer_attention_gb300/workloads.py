@@ -150,9 +150,10 @@ def window_reverse(x, M, batch, img_h, img_w):
     return x.permute(0, 1, 4, 2, 5, 3, 6).reshape(batch, img_h, img_w, heads * d)
 
 
-def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02, seed=0):
-    """q, k, v [B, heads, N, d] and head-shared tables [num_buckets, d] for the
-    enabled terms (None for a disabled one)."""
+def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02, seed=0,
+                per_head=False):
+    """q, k, v [B, heads, N, d] and tables for the enabled terms (None for a disabled
+    one): [num_buckets, d] shared by every head, or [heads, num_buckets, d] per head."""
     dt = _TORCH_DTYPE[dtype]
     shape = (B, heads, N, d)
     out = {
@@ -161,7 +162,8 @@ def irpe_inputs(B, heads, N, d, num_buckets, flags, dtype="bf16", table_std=0.02
         "v": _normal(shape, seed + 2).to(dt),
     }
     for t, (name, flag) in enumerate((("tab_q", FLAG_Q), ("tab_k", FLAG_K), ("tab_v", FLAG_V))):
-        out[name] = (_normal((num_buckets, d), seed + 3 + t, table_std).to(dt)
+        shape_t = (heads, num_buckets, d) if per_head else (num_buckets, d)
+        out[name] = (_normal(shape_t, seed + 3 + t, table_std).to(dt)
                      if flags & flag else None)
     return out
 
