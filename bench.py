@@ -82,6 +82,7 @@ DOMINANT = {
     "irpe_k_deit_s": ("rpe_pingpong_kernel<14,K>", "hbm", 29001472 + 0),
     "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29064960 + 2816),
     "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", 58131200 + 2073856),
+    "irpe_k_r2_deit_s": ("rpe_bf16_kernel<K>", "hbm", None),
 }
 
 
@@ -372,7 +373,8 @@ def gpu_arm(args):
 
     extra_cfgs = {}
     if not args.headline_only:
-        for name in ("swin_t_stage1", "swin_t_stage1_fmap", "irpe_qkv_deit_s", "irpe_k_56x56"):
+        for name in ("swin_t_stage1", "swin_t_stage1_fmap", "irpe_qkv_deit_s", "irpe_k_56x56",
+                     "irpe_k_r2_deit_s"):
             if name == args.workload:
                 continue
             c = workloads.CONFIGS[name]

@@ -134,9 +134,10 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                RPE_TABLES_PER_HEAD for one table per head.
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);
- * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 64
- * (with RPE_TABLES_CROSS: num_buckets even and (num_buckets / 2)^2 <= 64);
- * N <= 65536. Anything else returns RPE_ERR_UNSUPPORTED.
+ * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 256
+ * for fp32, <= 128 for bf16 (<= 64 with RPE_TERM_Q); with RPE_TABLES_CROSS
+ * num_buckets even and (num_buckets / 2)^2 <= 64; N <= 65536. Anything else
+ * returns RPE_ERR_UNSUPPORTED.
  */
 int rpe_attn_fwd(const void *q, const void *k, const void *v,
                  const void *table_q, const void *table_k, const void *table_v,
@@ -159,8 +160,9 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
  * flags        : 0, or RPE_TABLES_CROSS for a Cross-mapping table (the bias
  *                of a pair is then b[a][h] + b[span + b'][h] for its joint
  *                index a * span + b').
- * Supported: RPE_DTYPE_F32 on any grid with d <= 64; RPE_DTYPE_BF16 with
- * d == 64 and W in {14, 56}; num_buckets <= 64 (Cross as for rpe_attn_fwd).
+ * Supported: RPE_DTYPE_F32 on any grid with d <= 64 and num_buckets <= 256;
+ * RPE_DTYPE_BF16 with d == 64, W in {14, 56} and num_buckets <= 128 (Cross as
+ * for rpe_attn_fwd).
  * Errors as for rpe_attn_fwd.
  */
 int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,

@@ -283,3 +283,94 @@ def test_per_head_tables_56x56_sampled():
     S = B * heads
     got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
     assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
+
+
+# ------------------------------------------------------------ more than 64 buckets (r = 2.0)
+
+R20 = workloads.index_constants(2.0)
+
+
+def test_product_ids_r2_bit_exact():
+    lut, ids, nb = api.rpe_build_bucket_ids(25, 34, *R20, with_ids=True)
+    ref, K = oracle.product_bucket_ids(25, 34, *R20)
+    assert nb == K == 81
+    assert np.array_equal(ids.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("B,heads,H,W,flags,dtype,table_std", [
+    (2, 3, 14, 14, FLAG_K, "bf16", 1.0),            # general kernel, two QR rounds
+    (1, 2, 13, 17, FLAG_K | FLAG_V, "bf16", 0.5),   # ragged grid, 128-bucket PB R^V
+    (1, 2, 9, 9, FLAG_V, "bf16", 0.5),
+    (1, 2, 9, 11, FLAG_K | FLAG_Q | FLAG_V, "f32", 1.0),
+])
+def test_r2_81_buckets_match_oracle(B, heads, H, W, flags, dtype, table_std):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R20)
+    assert nb == 81
+    inp = workloads.irpe_inputs(B, heads, H * W, 64 if dtype == "bf16" else 32, nb, flags, dtype,
+                                table_std=table_std, seed=H * W + 17)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = oracle.product_bucket_ids(H, W, *R20)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
+                                    tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+    # negative control: buckets 64..80 (offsets with row index +3 or +4) matter
+    tabs = {n: inp[n] for n in ("tab_q", "tab_k", "tab_v")}
+    cut = {n: (None if t is None else torch.cat([t[:64], 0 * t[64:]])) for n, t in tabs.items()}
+    low = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, **cut)
+    assert np.max(np.abs(low - ref)) > 3 * TOL_BF16
+
+
+def test_r2_deit_s_config_sampled():
+    cfg = workloads.CONFIGS["irpe_k_r2_deit_s"]
+    lut, _, nb = api.rpe_build_bucket_ids(cfg.H, cfg.W, *workloads.index_constants(cfg.ratio))
+    assert nb == cfg.num_buckets == 81
+    inp = workloads.config_inputs(cfg)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, cfg.H, cfg.W, cfg.flags,
+                           table_k=g["tab_k"])
+    S = cfg.B * cfg.heads
+    rng = np.random.default_rng(4)
+    sl = np.unique(np.concatenate([rng.choice(S, 12, replace=False), [0, S - 1]]))
+    ids, K = oracle.product_bucket_ids(cfg.H, cfg.W, *R20)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, cfg.flags,
+                                    tab_k=inp["tab_k"], slices=sl).reshape(S, cfg.N, 64)[sl]
+    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_BF16
+
+
+def test_r2_bias_mode_on_the_two_warpgroup_kernel():
+    H, W = 14, 14
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R20)
+    inp = workloads.irpe_inputs(2, 3, H * W, 64, nb, 0, "bf16", seed=21)
+    bias = workloads.bias_table(nb, 3, 2.0, seed=22)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], bias.cuda(), lut, nb, H, W)
+    ids, K = oracle.product_bucket_ids(H, W, *R20)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=bias.numpy())
+    assert _maxerr(out, ref) <= TOL_BF16
+
+
+def test_fp32_takes_225_buckets():
+    ratio = 3.5   # beta 7: 15 x 15 buckets
+    H, W = 8, 12
+    consts = workloads.index_constants(ratio)
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *consts)
+    assert nb == 225
+    inp = workloads.irpe_inputs(1, 2, H * W, 16, nb, FLAG_K | FLAG_V, "f32", table_std=1.0, seed=3)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, FLAG_K | FLAG_V,
+                           table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = oracle.product_bucket_ids(H, W, *consts)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K | FLAG_V,
+                                    tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= TOL_F32
+
+
+def test_query_term_beyond_64_buckets_is_refused_in_bf16():
+    lut, _, nb = api.rpe_build_bucket_ids(14, 14, *R20)
+    inp = workloads.irpe_inputs(1, 1, 196, 64, nb, FLAG_Q, "bf16")
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    with pytest.raises(RpeError):
+        api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, 14, 14, FLAG_Q, table_q=g["tab_q"])

@@ -56,8 +56,12 @@ def test_host_argument_checks_reject_before_any_launch():
     assert lib.rpe_attn_fwd(fake, fake, fake, None, None, None, fake, 49, 1, 1, 14, 14, 64, 1, 0,
                             fake, None) == 1
     # unsupported: too many buckets, bf16 with d != 64, Swin bf16 with M != 7
-    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 81, 1, 1, 14, 14, 64, 1, 0,
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 129, 1, 1, 14, 14, 64, 1, 0,
                             fake, None) == 2
+    assert lib.rpe_attn_fwd(fake, fake, fake, fake, fake, None, fake, 81, 1, 1, 14, 14, 64, 3, 0,
+                            fake, None) == 2   # query term: 64 buckets at most in bf16
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 257, 1, 1, 14, 14, 32, 1, 1,
+                            fake, None) == 2   # fp32: 256 at most
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 49, 1, 1, 14, 14, 32, 1, 0,
                             fake, None) == 2
     # Cross tables: an odd row count or (rows / 2)^2 joint ids above 64 are not

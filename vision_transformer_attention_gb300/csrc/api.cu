@@ -159,7 +159,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         if (p != nullptr && !aligned16(p)) return RPE_ERR_INVALID_ARG;
     const long long N = static_cast<long long>(H) * W;
     const long long slices = static_cast<long long>(B) * heads;
-    if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (N > 65536 || num_buckets > 256) return RPE_ERR_UNSUPPORTED;
     if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
         return RPE_ERR_UNSUPPORTED;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
@@ -190,7 +190,10 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }
-    if (d != 64) return RPE_ERR_UNSUPPORTED;
+    // bf16: up to 128 buckets for the key and value terms (two 64-bucket halves),
+    // 64 for the query term
+    if (d != 64 || num_buckets > 128 || ((terms & RPE_TERM_Q) && num_buckets > 64))
+        return RPE_ERR_UNSUPPORTED;
     RpeBf16Args a{};
     a.q = q;
     a.k = k;
@@ -229,7 +232,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
     const long long N = static_cast<long long>(H) * W;
     const long long slices = static_cast<long long>(B) * heads;
-    if (N > 65536 || num_buckets > 64) return RPE_ERR_UNSUPPORTED;
+    if (N > 65536 || num_buckets > 256) return RPE_ERR_UNSUPPORTED;
     if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
         return RPE_ERR_UNSUPPORTED;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
@@ -257,7 +260,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         return status_of(launch_attn_f32(a, st));
     }
     // bf16: the two-warpgroup kernel, which is specialised for these grid widths
-    if (d != 64 || (W != 14 && W != 56)) return RPE_ERR_UNSUPPORTED;
+    if (d != 64 || (W != 14 && W != 56) || num_buckets > 128) return RPE_ERR_UNSUPPORTED;
     RpeBf16Args a{};
     a.q = q;
     a.k = k;

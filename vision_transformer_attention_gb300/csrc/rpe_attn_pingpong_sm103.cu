@@ -337,14 +337,18 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 }
 
 // BM: iRPE bias mode (a scalar per bucket and head, inside the scaling) in
-// place of the contextual key term; HK and BM are not both set.
-template <int W, bool HK, int NG, bool BM>
+// place of the contextual key term; HK and BM are not both set. TF, the
+// table form: bit 0, the table (R^K or the bias table) is laid out for the
+// Cross mapping; bit 1, R^K is one table per head.
+template <int W, bool HK, int NG, bool BM, int TF>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_rk,
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
+    constexpr bool X = (TF & 1) != 0;   // Cross table
+    constexpr bool PH = (TF & 2) != 0;  // one R^K per head
     using G = Geo<W>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
@@ -432,7 +436,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
-                if (HK && P.tab_heads == 1) {
+                if (HK && !PH) {
                     // two 32-row boxes: table rows 0.. and rows tab_row2.. (for
                     // Cross tables the column buckets land at row 32)
                     mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
@@ -453,7 +457,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     uint8_t *qd = sQ + qb * NG * kTileBytes;
                     // per-head tables travel with the item's Q tiles: the Q buffer's
                     // release (after both groups' last products) frees its table too
-                    const bool tab_item = HK && P.tab_heads > 1;
+                    constexpr bool tab_item = HK && PH;
                     mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes +
                                                                 (tab_item ? kTileBytes / 2 : 0));
                     if (tab_item) {
@@ -481,7 +485,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                 }
                 // drain: the most recent load on every barrier has landed
-                if (HK && P.tab_heads == 1) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+                if (HK && !PH) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
                 for (int b = 0; b < 2; ++b)
                     if (last_q[b] >= 0)
                         mbar_wait(&bars.q_full[b], last_q[b] & 1, drain, kStatusTimeoutDrain, nullptr);
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 uint32_t u = 0;  // units issued
                 int ci = 0;      // items whose last P V was issued
                 bool ok = true;
-                if (HK && P.tab_heads == 1) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+                if (HK && !PH) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
                 // consume the oldest outstanding unit: wait until the group has
                 // released it, then issue its P V
                 auto consume = [&]() {
@@ -572,7 +576,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         uint32_t code;
                         if (kt < 0) {
                             tc_fence_after();
-                            const uint32_t rk_off = P.tab_heads > 1 ? qb * (kTileBytes / 2) : 0;
+                            const uint32_t rk_off = PH ? qb * (kTileBytes / 2) : 0;
                             const uint64_t dRK = hi128 | (smem_u32(sRK + rk_off) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -659,9 +663,9 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 const int col = P.bias_heads == 1 ? 0 : I.slice % P.heads;
                 if (t < P.nb) {
                     // Cross: joint id a*span + b takes row bucket a plus column bucket span + b
-                    const int r0 = P.cross ? t / P.cross : t;
+                    const int r0 = X ? t / P.cross : t;
                     float b = __ldg(P.bias + r0 * P.bias_heads + col);
-                    if (P.cross) b += __ldg(P.bias + (P.cross + t % P.cross) * P.bias_heads + col);
+                    if (X) b += __ldg(P.bias + (P.cross + t % P.cross) * P.bias_heads + col);
                     bias_row[t] = b * P.c;
                 }
                 named_bar_sync(group_bar, 128);
@@ -675,7 +679,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     tmem_ld_wait();
                     tmem_ready(r0);
                     tmem_ready(r1);
-                    if (P.cross) {
+                    if constexpr (X) {
                         // joint id a*span + b: row bucket a (column a) plus column
                         // bucket span + b (staged at table row 32 + b)
 #pragma unroll
@@ -770,7 +774,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int W, bool HK, int NG, bool BM>
+template <int W, bool HK, int NG, bool BM, int TF>
 cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     using G = Geo<W>;
     using L = Layout<NG>;
@@ -848,31 +852,49 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 3, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG, BM>,
+    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG, BM, TF>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
-    return launch_pdl(rpe_pingpong_kernel<W, HK, NG, BM>, dim3(grid), dim3(L::kThreads), total, stream,
+    return launch_pdl(rpe_pingpong_kernel<W, HK, NG, BM, TF>, dim3(grid), dim3(L::kThreads), total, stream,
                       tq, tk, tv, trk, to, p);
 }
 
 }  // namespace
 
+namespace {
+
+template <int W>
+cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, bool bm) {
+    constexpr int NG = kGroupsPerCta;
+    const int tf = (a.cross_span > 0 ? 1 : 0) | (a.tab_heads > 1 ? 2 : 0);
+    if (bm) return (tf & 1) ? launch_pp<W, false, NG, true, 1>(a, stream)
+                            : launch_pp<W, false, NG, true, 0>(a, stream);
+    if (hk) {
+        switch (tf) {
+            case 0: return launch_pp<W, true, NG, false, 0>(a, stream);
+            case 1: return launch_pp<W, true, NG, false, 1>(a, stream);
+            case 2: return launch_pp<W, true, NG, false, 2>(a, stream);
+            default: return launch_pp<W, true, NG, false, 3>(a, stream);
+        }
+    }
+    return launch_pp<W, false, NG, false, 0>(a, stream);
+}
+
+}  // namespace
+
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
-    if (a.d != kD || (a.terms & ~1u) != 0 || a.num_buckets > 64) return false;
+    if (a.d != kD || (a.terms & ~1u) != 0) return false;
     const bool hk = (a.terms & 1u) != 0;
     const bool bm = a.bias != nullptr;
     if (hk && bm) return false;
-    constexpr int NG = kGroupsPerCta;
+    // the QR' product and copy cover 64 buckets; a bias row, one per thread, 128
+    if ((hk && a.num_buckets > 64) || (bm && a.num_buckets > 128)) return false;
     if (a.W == 14)
-        *err = bm ? launch_pp<14, false, NG, true>(a, stream)
-             : hk ? launch_pp<14, true, NG, false>(a, stream)
-                  : launch_pp<14, false, NG, false>(a, stream);
+        *err = launch_width<14>(a, stream, hk, bm);
     else if (a.W == 56)
-        *err = bm ? launch_pp<56, false, NG, true>(a, stream)
-             : hk ? launch_pp<56, true, NG, false>(a, stream)
-                  : launch_pp<56, false, NG, false>(a, stream);
+        *err = launch_width<56>(a, stream, hk, bm);
     else
         return false;
     return true;

@@ -64,6 +64,7 @@ struct RpeParams {
     int cross;     // Cross tables: span (nb = span^2 joint ids); 0 otherwise
     int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     int tab_heads, heads;  // tab_heads 1: tables shared by every head; heads: one per head
+    int nr;        // 64-row halves of each table: 1, or 2 for 65..128 buckets (K and V terms)
     uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
         off_lut;
     int lut_len;
@@ -93,7 +94,10 @@ __device__ __forceinline__ bool bar_red_and(bool v) {
 
 __device__ __forceinline__ void softmax_bar() { named_bar_sync(1, 128); }
 
-template <bool HK, bool HQ, bool HV>
+// EXT: the extended table forms (Cross tables, 65..128 buckets in two 64-row
+// halves, one table per head); the other instantiations keep the code for one
+// shared table of at most 64 buckets.
+template <bool HK, bool HQ, bool HV, bool EXT>
 __global__ void __launch_bounds__(kThreads, 1)
     rpe_bf16_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -162,30 +166,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             uint32_t tab_bytes = 0;
-            if (HK) tab_bytes += kTileBytes / 2;
-            if (HQ) tab_bytes += kTileBytes / 2;
-            if (HV) tab_bytes += kTileBytes / 2;
-            // each table as two 32-row boxes: rows 0.. and rows tab_row2.. of
-            // table `head` ([tab_heads][rows][d])
+            const int nr = EXT ? P.nr : 1;
+            if (HK) tab_bytes += nr * (kTileBytes / 2);
+            if (HQ) tab_bytes += nr * (kTileBytes / 2);
+            if (HV) tab_bytes += nr * (kTileBytes / 2);
+            // each table as 32-row boxes of table `head` ([tab_heads][rows][d]):
+            // rows 0.. and rows tab_row2.. (then 64.. and 96.. for a second half)
+            auto load_table = [&](uint8_t *dst, const CUtensorMap *m, int head) {
+                tma_load_3d(dst, m, &bars.tab_full, 0, 0, head);
+                tma_load_3d(dst + 4096, m, &bars.tab_full, 0, P.tab_row2, head);
+                for (int r = 2; r < 2 * nr; ++r)
+                    tma_load_3d(dst + r * 4096, m, &bars.tab_full, 0, 32 * r, head);
+            };
             auto load_tables = [&](int head) {
                 mbar_arrive_expect_tx(&bars.tab_full, tab_bytes);
-                if (HK) {
-                    tma_load_3d(smem + P.off_rk, &tm_rk, &bars.tab_full, 0, 0, head);
-                    tma_load_3d(smem + P.off_rk + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2, head);
-                }
-                if (HQ) {
-                    tma_load_3d(smem + P.off_rq, &tm_rq, &bars.tab_full, 0, 0, head);
-                    tma_load_3d(smem + P.off_rq + 4096, &tm_rq, &bars.tab_full, 0, P.tab_row2, head);
-                }
-                if (HV) {
-                    tma_load_3d(smem + P.off_rv, &tm_rv, &bars.tab_full, 0, 0, head);
-                    tma_load_3d(smem + P.off_rv + 4096, &tm_rv, &bars.tab_full, 0, P.tab_row2, head);
-                }
+                if (HK) load_table(smem + P.off_rk, &tm_rk, head);
+                if (HQ) load_table(smem + P.off_rq, &tm_rq, head);
+                if (HV) load_table(smem + P.off_rv, &tm_rv, head);
             };
             // Shared tables are loaded once. Per-head tables are loaded for every
             // item once the previous item's products are done with them, after
             // the item's first K/V tile so that load is not held up.
-            const bool per_head = tab_bytes != 0 && P.tab_heads > 1;
+            const bool per_head = EXT && tab_bytes != 0 && P.tab_heads > 1;
             if (tab_bytes && !per_head) load_tables(0);
             int g = 0, w = 0;
             int last_kv_use[2] = {-1, -1};
@@ -246,27 +248,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_par = parity;
             };
             bool ok = true;
-            const bool per_head = (HK || HQ || HV) && P.tab_heads > 1;
+            const bool per_head = EXT && (HK || HQ || HV) && P.tab_heads > 1;
             if ((HK || HQ || HV) && !per_head)
                 ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
             int g = 0, w = 0, pr = 0;
+            uint32_t qrc = 0;  // QR rounds issued (one per 64-row half of R^K)
             for (int item = blockIdx.x; ok && item < P.items; item += gridDim.x, ++w) {
                 if (!(ok = mbar_wait(&bars.q_full, w & 1, wc, kStatusTimeoutLoad, &abort_flag))) break;
                 if (per_head && !(ok = mbar_wait(&bars.tab_full, w & 1, wc, kStatusTimeoutLoad, &abort_flag)))
                     break;
                 tc_fence_after();
-                if (HK) {
-                    if (!(ok = mbar_wait(&bars.qr_empty, (w & 1) ^ 1, wc, kStatusTimeoutSync,
+                // QR = Q R^K^T, one 64-bucket half per round through the same
+                // 64 TMEM columns (the softmax warps copy each round out)
+                for (int r = 0; HK && ok && r < (EXT ? P.nr : 1); ++r, ++qrc) {
+                    if (!(ok = mbar_wait(&bars.qr_empty, (qrc & 1) ^ 1, wc, kStatusTimeoutSync,
                                          &abort_flag)))
                         break;
                     tc_fence_after();
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ss(tmem + kColQR, smem_desc(aQ + kk * 32, 16, 1024, kSwizzle128B),
-                                    smem_desc(smem_u32(smem + P.off_rk) + kk * 32, 16, 1024,
-                                              kSwizzle128B),
+                                    smem_desc(smem_u32(smem + P.off_rk) + r * (kTileBytes / 2) + kk * 32,
+                                              16, 1024, kSwizzle128B),
                                     kIdT, kk > 0);
-                    commit(&bars.qr_full, w & 1);
+                    commit(&bars.qr_full, qrc & 1);
                 }
+                if (!ok) break;
                 // S for key tile g (and KR with it); returns false on abort
                 auto issue_s = [&](int gg, int kt) -> bool {
                     const int st = gg % P.nst, b = gg & 1;
@@ -325,9 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     ++pr;
                     tc_fence_after();
-                    for (int kk = 0; kk < 4; ++kk)
+                    for (int kk = 0; kk < 4 * (EXT ? P.nr : 1); ++kk)
                         mma_bf16_ss(tmem + kColO,
-                                    smem_desc(smem_u32(sP) + kk * 32, 16, 1024, kSwizzle128B),
+                                    smem_desc(smem_u32(sP) + (kk >> 2) * kTileBytes + (kk & 3) * 32,
+                                              16, 1024, kSwizzle128B),
                                     smem_desc(smem_u32(smem + P.off_rv) + kk * 2048, 16, 1024,
                                               kSwizzle128B),
                                     kIdO, 1u);
@@ -350,16 +357,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         float *pb_t = sPB + t;
         const uint32_t prow = smem_u32(sP) + t * 128;
         int g = 0, w = 0, pw = 0;
+        uint32_t qrc = 0;  // QR rounds copied
         for (int item = blockIdx.x; item < P.items; item += gridDim.x, ++w) {
             const int slice = item / P.qtiles, qt = item % P.qtiles;
             const int i = qt * kBM + t;
             const int ic = i < P.N ? i : P.N - 1;
             const int base_i = (ic / P.W) * cols + (ic % P.W) + (P.H - 1) * cols + (P.W - 1);
             const uint8_t *lut_i = sLut + base_i;
-            if (HK) {
-                bool ok = __all_sync(~0u, mbar_wait(&bars.qr_full, w & 1, wc, kStatusTimeoutMma,
+            bool qr_ok = true;
+            for (int r = 0; HK && r < (EXT ? P.nr : 1); ++r, ++qrc) {
+                // one round per item unless EXT: the item counter is the phase
+                const uint32_t qph = EXT ? qrc : static_cast<uint32_t>(w);
+                bool ok = __all_sync(~0u, mbar_wait(&bars.qr_full, qph & 1, wc, kStatusTimeoutMma,
                                                     &abort_flag));
-                if (!bar_red_and(ok)) break;
+                if (!bar_red_and(ok)) {
+                    qr_ok = false;
+                    break;
+                }
                 tc_fence_after();
                 uint32_t r0[32], r1[32];
                 tmem_ld32(tmem + lane_off + kColQR, r0);
@@ -367,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld_wait();
                 tmem_ready(r0);
                 tmem_ready(r1);
-                if (P.cross) {
+                if (EXT && P.cross) {
 #pragma unroll
                     for (int a = 0; a < 8; ++a)
 #pragma unroll
@@ -376,13 +390,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 qr_t[(a * P.cross + b) * 128] =
                                     (__uint_as_float(r0[a]) + __uint_as_float(r1[b])) * P.c;
                 } else {
+                    float *qr_r = qr_t + r * 64 * 128;
+                    const int nb_r = P.nb - r * 64;
 #pragma unroll
                     for (int b = 0; b < 64; ++b)
-                        if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
+                        if (b < nb_r) qr_r[b * 128] = __uint_as_float(b < 32 ? r0[b & 31] : r1[b & 31]) * P.c;
                 }
                 tc_fence_before();
                 mbar_arrive(&bars.qr_empty);
             }
+            if (!qr_ok) break;
             if (HV)
                 for (int b = 0; b < P.nb; ++b) pb_t[b * 128] = 0.f;
             float m = -INFINITY, l = 0.f;
@@ -409,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_ready(r0);
                     tmem_ready(r1);
                     float *kr = sKR + t * kKRStride;
-                    if (P.cross) {
+                    if (EXT && P.cross) {
 #pragma unroll
                         for (int a = 0; a < 8; ++a)
 #pragma unroll
@@ -531,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float rsum[8], csum[8];
 #pragma unroll
                 for (int a = 0; a < 8; ++a) rsum[a] = csum[a] = 0.f;
-                if (P.cross) {
+                if (EXT && P.cross) {
 #pragma unroll
                     for (int a = 0; a < 8; ++a)
 #pragma unroll
@@ -542,14 +559,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 csum[b] += pv;
                             }
                 }
+                // buckets 0..63 in P's first block, 64..127 (if any) in its second
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
+                for (int c = 0; c < 16; ++c) {
+                    if (c >= 8 * (EXT ? P.nr : 1)) continue;
                     uint32_t wv[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int b0 = c * 8 + 2 * e;
                         float v0, v1;
-                        if (P.cross) {
+                        if (EXT && P.cross) {
                             v0 = b0 < 8 ? rsum[b0] : (b0 >= 32 && b0 < 40 ? csum[b0 - 32] : 0.f);
                             v1 = b0 + 1 < 8 ? rsum[b0 + 1]
                                             : (b0 + 1 >= 32 && b0 + 1 < 40 ? csum[b0 - 31] : 0.f);
@@ -559,7 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         wv[e] = pack_bf16x2(v0, v1);
                     }
-                    st_shared_v4(prow + ((c ^ (t & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+                    st_shared_v4(prow + (c >> 3) * kTileBytes + (((c & 7) ^ (t & 7)) << 4), wv[0], wv[1],
+                                 wv[2], wv[3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -604,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <bool HK, bool HQ, bool HV>
+template <bool HK, bool HQ, bool HV, bool EXT>
 cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     const int N = a.H * a.W;
     const int slices = a.B * a.heads;
@@ -617,6 +637,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     p.tab_row2 = a.cross_span > 0 ? a.cross_span : 32;
     p.tab_heads = a.tab_heads;
     p.heads = a.heads;
+    p.nr = a.num_buckets > 64 ? 2 : 1;
     p.nkt = (N + kBN - 1) / kBN;
     p.qtiles = (N + kBM - 1) / kBM;
     p.items = slices * p.qtiles;
@@ -635,11 +656,11 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_p = off;
         off += 2 * kTileBytes;
         p.off_rk = off;
-        if (HK) off += kTileBytes / 2;
+        if (HK) off += p.nr * (kTileBytes / 2);
         p.off_rq = off;
-        if (HQ) off += kTileBytes / 2;
+        if (HQ) off += p.nr * (kTileBytes / 2);
         p.off_rv = off;
-        if (HV) off += kTileBytes / 2;
+        if (HV) off += p.nr * (kTileBytes / 2);
         p.off_qr = off;
         if (HK) off += align_up(p.nb * 512, 1024);
         p.off_kr = off;
@@ -678,12 +699,12 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
                 !encode_tensor_map(&trq, bf, 3, rq, tdims, tstrides, tbox, sw) ||
                 !encode_tensor_map(&trv, bf, 3, rv, tdims, tstrides, tbox, sw))
                 return cudaErrorInvalidValue;
-            cudaError_t err = cudaFuncSetAttribute(rpe_bf16_kernel<HK, HQ, HV>,
+            cudaError_t err = cudaFuncSetAttribute(rpe_bf16_kernel<HK, HQ, HV, EXT>,
                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                    static_cast<int>(total));
             if (err != cudaSuccess) return err;
             const int grid = std::min(p.items, sm_count());
-            rpe_bf16_kernel<HK, HQ, HV><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, trq, trv, p);
+            rpe_bf16_kernel<HK, HQ, HV, EXT><<<grid, kThreads, total, stream>>>(tq, tk, tv, trk, trq, trv, p);
             return cudaGetLastError();
         }
     }
@@ -692,19 +713,29 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
 
 }  // namespace
 
+namespace {
+
+template <bool EXT>
+cudaError_t launch_terms(const RpeBf16Args &a, cudaStream_t stream) {
+    const bool k = a.terms & 1u, q = a.terms & 2u, v = a.terms & 4u;
+    if (!k && !q && !v) return launch_tmpl<false, false, false, EXT>(a, stream);
+    if (k && !q && !v) return launch_tmpl<true, false, false, EXT>(a, stream);
+    if (!k && q && !v) return launch_tmpl<false, true, false, EXT>(a, stream);
+    if (!k && !q && v) return launch_tmpl<false, false, true, EXT>(a, stream);
+    if (k && q && !v) return launch_tmpl<true, true, false, EXT>(a, stream);
+    if (k && !q && v) return launch_tmpl<true, false, true, EXT>(a, stream);
+    if (!k && q && v) return launch_tmpl<false, true, true, EXT>(a, stream);
+    return launch_tmpl<true, true, true, EXT>(a, stream);
+}
+
+}  // namespace
+
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
     if (launch_rpe_bf16_pingpong(a, stream, &err)) return err;
     if (a.bias != nullptr) return cudaErrorInvalidValue;  // bias mode: ping-pong kernel only
-    const bool k = a.terms & 1u, q = a.terms & 2u, v = a.terms & 4u;
-    if (!k && !q && !v) return launch_tmpl<false, false, false>(a, stream);
-    if (k && !q && !v) return launch_tmpl<true, false, false>(a, stream);
-    if (!k && q && !v) return launch_tmpl<false, true, false>(a, stream);
-    if (!k && !q && v) return launch_tmpl<false, false, true>(a, stream);
-    if (k && q && !v) return launch_tmpl<true, true, false>(a, stream);
-    if (k && !q && v) return launch_tmpl<true, false, true>(a, stream);
-    if (!k && q && v) return launch_tmpl<false, true, true>(a, stream);
-    return launch_tmpl<true, true, true>(a, stream);
+    if (a.cross_span > 0 || a.num_buckets > 64 || a.tab_heads > 1) return launch_terms<true>(a, stream);
+    return launch_terms<false>(a, stream);
 }
 
 }  // namespace vta

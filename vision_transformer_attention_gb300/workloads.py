@@ -96,6 +96,10 @@ CONFIGS = {
                                   FLAG_Q | FLAG_K | FLAG_V, "bf16"),
     # high-resolution global attention, 56x56 grid
     "irpe_k_56x56": IrpeConfig("irpe_k_56x56", 8, 6, 56, 56, 64, FLAG_K, "bf16"),
+    # the r = 2.0 index function (9 x 9 = 81 Product buckets, as DETR's encoder
+    # uses it) on the DeiT-S shape
+    "irpe_k_r2_deit_s": IrpeConfig("irpe_k_r2_deit_s", 64, 6, 14, 14, 64, FLAG_K, "bf16",
+                                   ratio=2.0),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
