@@ -70,6 +70,8 @@ def _load():
                                       i32, p, p, p]
         lib.orc_cross_bucket_ids.restype = i32
         lib.orc_cross_bucket_ids.argtypes = [i32, i32, dbl, dbl, dbl, p, p]
+        lib.orc_add_cls_bucket.restype = i32
+        lib.orc_add_cls_bucket.argtypes = [i32, p, i32, p]
         lib.orc_clip_product_bucket_ids.restype = i32
         lib.orc_clip_product_bucket_ids.argtypes = [i32, i32, i32, p]
         lib.orc_euclidean_bucket_ids.restype = i32
@@ -143,6 +145,16 @@ def cross_bucket_ids(H: int, W: int, alpha: float, beta: float, gamma: float):
     ids_col = np.zeros((N, N), dtype=np.int32)
     K = _load().orc_cross_bucket_ids(H, W, alpha, beta, gamma, _ptr(ids_row), _ptr(ids_col))
     return ids_row, ids_col, int(K)
+
+
+def add_cls_bucket(ids, K: int):
+    """Section 4.1's class-token bucket: the [N, N] patch id map becomes the
+    [N+1, N+1] map of token 0 (class) and the patches; returns (ids, K + 1)."""
+    ids = _i32(ids)
+    N = ids.shape[0]
+    out = np.zeros((N + 1, N + 1), dtype=np.int32)
+    K1 = _load().orc_add_cls_bucket(N, _ptr(ids), K, _ptr(out))
+    return out, int(K1)
 
 
 def clip_product_bucket_ids(H: int, W: int, k: int):

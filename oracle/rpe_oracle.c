@@ -155,6 +155,20 @@ int orc_clip_product_bucket_ids(int H, int W, int k, int32_t *ids)
     return span * span;
 }
 
+/* iRPE section 4.1: the class token gets one extra bucket for all its
+ * pairs. Token 0 is the class token and tokens 1..N the patches (patch t at
+ * grid token t - 1). Given the patches' id map ids [N, N] of K buckets,
+ * writes the (N+1) x (N+1) map out with bucket K on row 0 and column 0 and
+ * ids[i-1][j-1] elsewhere. Returns K + 1. */
+int orc_add_cls_bucket(int N, const int32_t *ids, int K, int32_t *out)
+{
+    int n = N + 1;
+    for (int i = 0; i < n; ++i)
+        for (int j = 0; j < n; ++j)
+            out[(int64_t)i * n + j] = (i == 0 || j == 0) ? K : ids[(int64_t)(i - 1) * N + (j - 1)];
+    return K + 1;
+}
+
 /* SWIN2D sections 3.1-3.2: inside an M x M window the offsets lie in
  * [-(M-1), M-1]; shifting by M-1 moves them to [0, 2M-2]; the compact
  * (2M-1) x (2M-1) table is read at (dr', dc') and, flattened to 1D, at

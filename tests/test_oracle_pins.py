@@ -593,3 +593,49 @@ def test_per_head_tables_serve_their_own_head():
     rep = oracle.irpe_attention_ids(q, k, v, ids, K, 7, tab_q=np.stack([tq[1]] * heads),
                                     tab_k=np.stack([tk[1]] * heads), tab_v=np.stack([tv[1]] * heads))
     assert np.max(np.abs(shared - rep)) < 1e-12
+
+
+# ------------------------------------------------------------ class-token bucket (section 4.1)
+
+def test_cls_bucket_count_is_the_pages_fifty():
+    # Pitfalls and table 3: 7 x 7 Product buckets plus one for the class token
+    H, W = 14, 14
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    cls, K1 = oracle.add_cls_bucket(ids, K)
+    assert (K, K1) == (49, 50)
+    assert cls.shape == (H * W + 1, H * W + 1)
+    assert np.all(cls[0] == 49) and np.all(cls[:, 0] == 49)
+    assert np.array_equal(cls[1:, 1:], ids)
+
+
+def test_cls_hard_bias_routes_every_patch_to_the_class_token():
+    # q = k = 0 and a large bias on the class bucket: each patch query sees one
+    # key in that bucket (token 0) and returns v_0; the class query has every
+    # pair in that bucket, so its logits are equal and it averages all of v
+    H, W, d = 3, 4, 4
+    n = H * W + 1
+    z = np.zeros((n, d))
+    v = _rand((n, d), 80)
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    cls, K1 = oracle.add_cls_bucket(ids, K)
+    bias = np.zeros(K1)
+    bias[K] = 50.0 * np.sqrt(d)
+    out = oracle.attention(z, z, v, cls, K1, bias_in=bias)
+    assert np.allclose(out[1:], v[0], atol=1e-12)
+    assert np.allclose(out[0], v.mean(axis=0), atol=1e-12)
+
+
+def test_cls_suppressed_leaves_the_patch_attention():
+    # a -1e4 logit on the class bucket removes key 0 for every patch query, whose
+    # result is then the patch-only attention with the same tables
+    H, W, d = 4, 5, 8
+    n = H * W
+    q, k, v = (_rand((n + 1, d), s) for s in (81, 82, 83))
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    cls, K1 = oracle.add_cls_bucket(ids, K)
+    tk, tv = _rand((K1, d), 84), _rand((K1, d), 85)
+    bias = np.zeros(K1)
+    bias[K] = -1e4 * np.sqrt(d)
+    full = oracle.attention(q, k, v, cls, K1, tab_k=tk, tab_v=tv, bias_in=bias)
+    patch = oracle.attention(q[1:], k[1:], v[1:], ids, K, tab_k=tk[:K], tab_v=tv[:K])
+    assert np.max(np.abs(full[1:] - patch)) < 1e-12
