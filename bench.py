@@ -70,6 +70,7 @@ def workload_config(cfg):
     terms = "".join(t for t, f in (("Q", 2), ("K", 1), ("V", 4)) if cfg.flags & f)
     return {"workload": cfg.name, "B": cfg.B, "heads": cfg.heads, "grid": [cfg.H, cfg.W],
             "N": cfg.N, "d": cfg.d, "terms": terms or "none", "num_buckets": cfg.num_buckets,
+            "cls_token": cfg.cls,
             "index_fn": {"alpha": cfg.ratio, "beta": 2 * cfg.ratio, "gamma": 8 * cfg.ratio}}
 
 
@@ -83,6 +84,7 @@ DOMINANT = {
     "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29064960 + 2816),
     "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", 58131200 + 2073856),
     "irpe_k_r2_deit_s": ("rpe_bf16_kernel<K>", "hbm", None),
+    "irpe_k_deit_s_cls": ("rpe_bf16_kernel<K>", "hbm", None),
 }
 
 
@@ -178,7 +180,7 @@ def make_step(cfg, sets):
         def step(i):
             s = sets[i % len(sets)]
             api.rpe_attn_fwd(s["q"], s["k"], s["v"], s["lut"], cfg.num_buckets, cfg.H, cfg.W,
-                             cfg.flags, table_q=s["tab_q"], table_k=s["tab_k"],
+                             cfg.flags, cls_token=cfg.cls, table_q=s["tab_q"], table_k=s["tab_k"],
                              table_v=s["tab_v"], out=s["out"])
     return step
 
@@ -268,7 +270,7 @@ def e2e_run(cfg, dev, steps, barrier):
             dq[k].copy_(host[k], non_blocking=True)
         if lut is not None:
             api.rpe_attn_fwd(dq["q"], dq["k"], dq["v"], lut, cfg.num_buckets, cfg.H, cfg.W,
-                             cfg.flags, table_q=tabs["tab_q"], table_k=tabs["tab_k"],
+                             cfg.flags, cls_token=cfg.cls, table_q=tabs["tab_q"], table_k=tabs["tab_k"],
                              table_v=tabs["tab_v"], out=out)
         else:
             if cfg.fmap:
@@ -306,6 +308,13 @@ def cpu_baseline(cfg, budget_s=12.0):
         S, per_unit_tokens = cfg.num_windows * cfg.heads, cfg.n / cfg.heads
         run = lambda sl: oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"],  # noqa: E731
                                                 cfg.M, slices=sl)
+    elif cfg.cls:
+        S, per_unit_tokens = cfg.B * cfg.heads, cfg.N / cfg.heads
+        ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(
+            cfg.H, cfg.W, *workloads.index_constants(cfg.ratio)))
+        run = lambda sl: oracle.irpe_attention_ids(  # noqa: E731
+            inp["q"], inp["k"], inp["v"], ids, K, cfg.flags, tab_q=inp["tab_q"],
+            tab_k=inp["tab_k"], tab_v=inp["tab_v"], slices=sl)
     else:
         S, per_unit_tokens = cfg.B * cfg.heads, cfg.N / cfg.heads
         a, b, g = workloads.index_constants(cfg.ratio)
@@ -374,7 +383,7 @@ def gpu_arm(args):
     extra_cfgs = {}
     if not args.headline_only:
         for name in ("swin_t_stage1", "swin_t_stage1_fmap", "irpe_qkv_deit_s", "irpe_k_56x56",
-                     "irpe_k_r2_deit_s"):
+                     "irpe_k_r2_deit_s", "irpe_k_deit_s_cls"):
             if name == args.workload:
                 continue
             c = workloads.CONFIGS[name]
@@ -445,12 +454,19 @@ def reference_arm(args):
     S = cfg.B * cfg.heads
     q64, k64, v64, tk64 = (oracle._f64(inp[x]) for x in ("q", "k", "v", "tab_k"))
 
+    cls_ids = (oracle.add_cls_bucket(*oracle.product_bucket_ids(cfg.H, cfg.W, a, b, g))
+               if getattr(cfg, "cls", False) else None)
+
     def step(i):
         sl = np.array([i % S])
         r0 = (i * rows_per_step) % cfg.N
         rows = (np.arange(rows_per_step) + r0) % cfg.N
-        oracle.irpe_attention(q64, k64, v64, cfg.H, cfg.W, a, b, g, cfg.flags,
-                              tab_k=tk64, slices=sl, rows=rows)
+        if cls_ids is not None:
+            oracle.irpe_attention_ids(q64, k64, v64, cls_ids[0], cls_ids[1], cfg.flags,
+                                      tab_k=tk64, slices=sl, rows=rows)
+        else:
+            oracle.irpe_attention(q64, k64, v64, cfg.H, cfg.W, a, b, g, cfg.flags,
+                                  tab_k=tk64, slices=sl, rows=rows)
     for i in range(args.warmup):
         step(i)
     t0 = time.perf_counter()

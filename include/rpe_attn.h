@@ -67,6 +67,13 @@ enum { RPE_TERM_K = 1, RPE_TERM_Q = 2, RPE_TERM_V = 4, RPE_TABLES_CROSS = 8 };
  * shared by every head (iRPE section 4.2, table 2). */
 enum { RPE_TABLES_PER_HEAD = 16 };
 
+/* Flag of rpe_attn_fwd and rpe_attn_bias_fwd: token 0 is a class token (iRPE
+ * section 4.1). q, k, v and out then hold N = H * W + 1 tokens, token t >= 1
+ * being grid token t - 1, and every pair involving token 0 takes the extra
+ * bucket num_buckets - 1 (the offset table's ids lie below it). Not combined
+ * with RPE_TABLES_CROSS; bf16 bias mode does not take it. */
+enum { RPE_CLS_TOKEN = 32 };
+
 /* Element types of q, k, v, out and the iRPE tables. */
 enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
 
@@ -130,8 +137,9 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                any table of ids indexed the same way; an id outside
  *                [0, num_buckets) is clamped into that range).
  * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention),
- *                plus RPE_TABLES_CROSS for tables of the Cross mapping and
- *                RPE_TABLES_PER_HEAD for one table per head.
+ *                plus RPE_TABLES_CROSS for tables of the Cross mapping,
+ *                RPE_TABLES_PER_HEAD for one table per head and RPE_CLS_TOKEN
+ *                for a class token at token 0 (then N = H * W + 1).
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);
  * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 256
@@ -159,7 +167,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
  * bucket_lut, num_buckets: as for rpe_attn_fwd (any mapping).
  * flags        : 0, or RPE_TABLES_CROSS for a Cross-mapping table (the bias
  *                of a pair is then b[a][h] + b[span + b'][h] for its joint
- *                index a * span + b').
+ *                index a * span + b'), or RPE_CLS_TOKEN (fp32 only).
  * Supported: RPE_DTYPE_F32 on any grid with d <= 64 and num_buckets <= 256;
  * RPE_DTYPE_BF16 with d == 64, W in {14, 56} and num_buckets <= 128 (Cross as
  * for rpe_attn_fwd).

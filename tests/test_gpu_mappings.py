@@ -374,3 +374,88 @@ def test_query_term_beyond_64_buckets_is_refused_in_bf16():
     g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
     with pytest.raises(RpeError):
         api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, 14, 14, FLAG_Q, table_q=g["tab_q"])
+
+
+# ------------------------------------------------------------ class token (section 4.1)
+
+def _cls_case(B, heads, H, W, flags, dtype, table_std, seed, ratio=1.9, per_head=False,
+              rows=None, slices=None):
+    consts = workloads.index_constants(ratio)
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *consts)
+    K1 = nb + 1
+    inp = workloads.irpe_inputs(B, heads, H * W + 1, 64 if dtype == "bf16" else 32, K1, flags,
+                                dtype, table_std=table_std, seed=seed, per_head=per_head)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, K1, H, W, flags, cls_token=True,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(H, W, *consts))
+    tabs = {n: inp[n] for n in ("tab_q", "tab_k", "tab_v")}
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, rows=rows,
+                                    slices=slices, **tabs)
+    return inp, out, ref, ids, K
+
+
+@pytest.mark.parametrize("B,heads,H,W,flags,dtype,table_std,ratio,per_head", [
+    (2, 3, 14, 14, FLAG_K, "bf16", 1.0, 1.9, False),           # DeiT-S grid + class token
+    (1, 2, 9, 12, FLAG_K | FLAG_Q | FLAG_V, "bf16", 0.5, 1.9, False),
+    (2, 2, 11, 11, FLAG_K, "bf16", 1.0, 1.9, True),            # per-head tables
+    (1, 2, 10, 13, FLAG_K | FLAG_V, "bf16", 0.5, 2.0, False),  # 82 buckets
+    (1, 1, 1, 1, FLAG_K, "bf16", 1.0, 1.9, False),             # one patch and the class token
+    (2, 2, 5, 9, FLAG_K | FLAG_Q | FLAG_V, "f32", 1.0, 1.9, False),
+])
+def test_cls_token_matches_oracle(B, heads, H, W, flags, dtype, table_std, ratio, per_head):
+    inp, out, ref, ids, K = _cls_case(B, heads, H, W, flags, dtype, table_std, seed=H * W + 31,
+                                      ratio=ratio, per_head=per_head)
+    assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+    if H * W > 1:
+        # negative control: the class bucket's table row matters beyond the tolerance
+        tabs = {n: inp[n] for n in ("tab_q", "tab_k", "tab_v")}
+        cut = {}
+        for n, t in tabs.items():
+            if t is not None:
+                t = t.clone()
+                t[..., K - 1, :] = 0
+            cut[n] = t
+        without = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, **cut)
+        assert np.max(np.abs(without - ref)) > 3 * TOL_BF16
+
+
+def test_cls_token_56x56_sampled():
+    rows = np.array([0, 1, 2, 1500, 3135, 3136])
+    sl = np.array([0, 4])
+    B, heads, H, W = 1, 6, 56, 56
+    _, out, ref, _, _ = _cls_case(B, heads, H, W, FLAG_K, "bf16", 1.0, seed=41, rows=rows,
+                                  slices=sl)
+    N = H * W + 1
+    got = out.reshape(B * heads, N, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref.reshape(B * heads, N, 64)[sl][:, rows]) <= TOL_BF16
+
+
+def test_cls_bias_mode_fp32():
+    H, W = 6, 7
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19)
+    inp = workloads.irpe_inputs(2, 3, H * W + 1, 32, nb + 1, 0, "f32", seed=43)
+    bias = workloads.bias_table(nb + 1, 3, 2.0, seed=44)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], bias.cuda(), lut, nb + 1, H, W,
+                                cls_token=True)
+    ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(H, W, *R19))
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=bias.numpy())
+    assert _maxerr(out, ref) <= TOL_F32
+
+
+def test_deit_s_cls_config_sampled():
+    cfg = workloads.CONFIGS["irpe_k_deit_s_cls"]
+    assert (cfg.N, cfg.num_buckets) == (197, 50)
+    lut, _, nb = api.rpe_build_bucket_ids(cfg.H, cfg.W, *workloads.index_constants(cfg.ratio))
+    inp = workloads.config_inputs(cfg)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, cfg.num_buckets, cfg.H, cfg.W, cfg.flags,
+                           cls_token=True, table_k=g["tab_k"])
+    S = cfg.B * cfg.heads
+    sl = np.array([0, 77, S - 1])
+    ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(cfg.H, cfg.W, *R19))
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, cfg.flags,
+                                    tab_k=inp["tab_k"], slices=sl).reshape(S, cfg.N, 64)[sl]
+    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_BF16

@@ -71,8 +71,14 @@ def test_host_argument_checks_reject_before_any_launch():
                             0, fake, None) == 2
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 13, 1, 1, 14, 14, 64, cross_k,
                             0, fake, None) == 2
-    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 32,
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 64,
                             0, fake, None) == 1
+    # class token with Cross tables, or in bf16 bias mode, is not served
+    cls_cross = cross_k | _lib.RPE_CLS_TOKEN
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64,
+                            cls_cross, 0, fake, None) == 2
+    assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 50, _lib.RPE_CLS_TOKEN, 1, 1,
+                                 14, 14, 64, 0, fake, None) == 2
     assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 14, 2, 1, 1, 14, 14, 64, 0,
                                  fake, None) == 1
     assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 18, _lib.RPE_TABLES_CROSS, 1, 1,

@@ -23,6 +23,7 @@ RPE_MAP_CLIP_PRODUCT = 3
 RPE_TERM_K, RPE_TERM_Q, RPE_TERM_V = 1, 2, 4
 RPE_TABLES_CROSS = 8
 RPE_TABLES_PER_HEAD = 16
+RPE_CLS_TOKEN = 32
 RPE_DTYPE_BF16, RPE_DTYPE_F32 = 0, 1
 
 # name -> (restype, argtypes) for every symbol the header declares

@@ -56,13 +56,18 @@ def rpe_build_bucket_ids(H, W, alpha, beta, gamma, device="cuda", with_ids=False
 
 
 def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, table_k=None,
-                 table_v=None, out=None):
+                 table_v=None, out=None, cls_token=False):
     """iRPE contextual attention (eqs. 13, 15-17) on q, k, v [B, heads, H*W, d]; terms
     may carry RPE_TABLES_CROSS for tables of the Cross mapping (eqs. 22-24). Tables
     are [num_buckets, d] (shared by every head) or [heads, num_buckets, d] (one per
-    head; RPE_TABLES_PER_HEAD is then set here)."""
+    head; RPE_TABLES_PER_HEAD is then set here). cls_token: token 0 is a class token
+    (section 4.1; q, k, v hold H*W + 1 tokens, its pairs use bucket num_buckets - 1)."""
     _need(q, "q")
     B, heads, N, d = q.shape
+    if cls_token:
+        terms |= _lib.RPE_CLS_TOKEN
+    if N != H * W + (1 if terms & _lib.RPE_CLS_TOKEN else 0):
+        raise ValueError(f"q has {N} tokens; the {H}x{W} grid needs H*W (+1 with a class token)")
     if q.dtype not in _DTYPES:
         raise TypeError("q must be bfloat16 or float32")
     for name, t in (("k", k), ("v", v)):
@@ -91,12 +96,16 @@ def rpe_attn_fwd(q, k, v, bucket_lut, num_buckets, H, W, terms, table_q=None, ta
     return out
 
 
-def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=None, cross=False):
+def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=None, cross=False,
+                      cls_token=False):
     """iRPE bias mode (eqs. 13-14) on q, k, v [B, heads, H*W, d]: bias_table is fp32
     [num_buckets, heads] (per head) or [num_buckets] / [num_buckets, 1] (shared);
-    cross: the table is laid out for the Cross mapping (eqs. 22-24)."""
+    cross: the table is laid out for the Cross mapping (eqs. 22-24); cls_token:
+    token 0 is a class token (section 4.1, H*W + 1 tokens)."""
     _need(q, "q")
     B, heads, N, d = q.shape
+    if N != H * W + (1 if cls_token else 0):
+        raise ValueError(f"q has {N} tokens; the {H}x{W} grid needs H*W (+1 with a class token)")
     if q.dtype not in _DTYPES:
         raise TypeError("q must be bfloat16 or float32")
     for name, t in (("k", k), ("v", v)):
@@ -113,7 +122,8 @@ def rpe_attn_bias_fwd(q, k, v, bias_table, bucket_lut, num_buckets, H, W, out=No
     with torch.cuda.device(q.device):
         check("rpe_attn_bias_fwd", _lib.lib().rpe_attn_bias_fwd(
             _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), bias_heads, _ptr(bucket_lut),
-            num_buckets, _lib.RPE_TABLES_CROSS if cross else 0, B, heads, H, W, d,
+            num_buckets, (_lib.RPE_TABLES_CROSS if cross else 0) | (_lib.RPE_CLS_TOKEN if cls_token else 0),
+            B, heads, H, W, d,
             _DTYPES[q.dtype], _ptr(out), _stream(q)))
     return out
 

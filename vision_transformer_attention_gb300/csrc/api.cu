@@ -143,9 +143,10 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || bucket_lut == nullptr)
         return RPE_ERR_INVALID_ARG;
     if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
-    if ((terms & ~31u) != 0) return RPE_ERR_INVALID_ARG;
+    if ((terms & ~63u) != 0) return RPE_ERR_INVALID_ARG;
     const int cross_span = (terms & RPE_TABLES_CROSS) ? num_buckets / 2 : 0;
     const int tab_heads = (terms & RPE_TABLES_PER_HEAD) ? heads : 1;
+    const int cls = (terms & RPE_CLS_TOKEN) ? 1 : 0;
     terms &= 7u;
     if (((terms & RPE_TERM_K) && table_k == nullptr) || ((terms & RPE_TERM_Q) && table_q == nullptr) ||
         ((terms & RPE_TERM_V) && table_v == nullptr))
@@ -157,17 +158,19 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
                           (terms & RPE_TERM_V) ? table_v : nullptr};
     for (const void *p : ptrs)
         if (p != nullptr && !aligned16(p)) return RPE_ERR_INVALID_ARG;
-    const long long N = static_cast<long long>(H) * W;
+    const long long N = static_cast<long long>(H) * W + cls;  // token 0: the class token
     const long long slices = static_cast<long long>(B) * heads;
     if (N > 65536 || num_buckets > 256) return RPE_ERR_UNSUPPORTED;
-    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
+    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64 || cls))
         return RPE_ERR_UNSUPPORTED;
+    if (cls && num_buckets < 2) return RPE_ERR_INVALID_ARG;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
         F32AttnArgs a{};
         a.cross_span = cross_span;
+        a.cls = cls;
         a.q = static_cast<const float *>(q);
         a.k = static_cast<const float *>(k);
         a.v = static_cast<const float *>(v);
@@ -212,6 +215,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.terms = terms;
     a.cross_span = cross_span;
     a.tab_heads = tab_heads;
+    a.cls = cls;
     return status_of(launch_rpe_bf16(a, st));
 }
 
@@ -224,23 +228,27 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         return RPE_ERR_INVALID_ARG;
     if (B < 1 || heads < 1 || H < 1 || W < 1 || d < 1 || num_buckets < 1) return RPE_ERR_INVALID_ARG;
     if (bias_heads != 1 && bias_heads != heads) return RPE_ERR_INVALID_ARG;
-    if ((flags & ~static_cast<unsigned>(RPE_TABLES_CROSS)) != 0) return RPE_ERR_INVALID_ARG;
+    if ((flags & ~static_cast<unsigned>(RPE_TABLES_CROSS | RPE_CLS_TOKEN)) != 0)
+        return RPE_ERR_INVALID_ARG;
     const int cross_span = (flags & RPE_TABLES_CROSS) ? num_buckets / 2 : 0;
+    const int cls = (flags & RPE_CLS_TOKEN) ? 1 : 0;
     if (dtype != RPE_DTYPE_BF16 && dtype != RPE_DTYPE_F32) return RPE_ERR_INVALID_ARG;
     const void *ptrs[] = {q, k, v, out, bucket_lut, bias_table};
     for (const void *p : ptrs)
         if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
-    const long long N = static_cast<long long>(H) * W;
+    const long long N = static_cast<long long>(H) * W + cls;  // token 0: the class token
     const long long slices = static_cast<long long>(B) * heads;
     if (N > 65536 || num_buckets > 256) return RPE_ERR_UNSUPPORTED;
-    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64))
+    if (cross_span > 0 && (num_buckets % 2 != 0 || cross_span * cross_span > 64 || cls))
         return RPE_ERR_UNSUPPORTED;
+    if (cls && num_buckets < 2) return RPE_ERR_INVALID_ARG;
     if (slices * N * d >= (1LL << 40)) return RPE_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
         F32AttnArgs a{};
         a.cross_span = cross_span;
+        a.cls = cls;
         a.q = static_cast<const float *>(q);
         a.k = static_cast<const float *>(k);
         a.v = static_cast<const float *>(v);
@@ -260,7 +268,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         return status_of(launch_attn_f32(a, st));
     }
     // bf16: the two-warpgroup kernel, which is specialised for these grid widths
-    if (d != 64 || (W != 14 && W != 56) || num_buckets > 128) return RPE_ERR_UNSUPPORTED;
+    if (d != 64 || (W != 14 && W != 56) || num_buckets > 128 || cls) return RPE_ERR_UNSUPPORTED;
     RpeBf16Args a{};
     a.q = q;
     a.k = k;

@@ -36,6 +36,12 @@ struct Rows {
 };
 
 __device__ __forceinline__ Rows bucket_of(const F32AttnArgs &a, int i, int j) {
+    // class token (iRPE section 4.1): token 0, every pair with it in the last bucket
+    if (a.cls) {
+        if (i == 0 || j == 0) return Rows{a.num_buckets - 1, -1};
+        --i;
+        --j;
+    }
     const int cols = 2 * a.W - 1;
     const int off = (i / a.W - j / a.W + a.H - 1) * cols + (i % a.W - j % a.W + a.W - 1);
     int id = a.lut ? __ldg(a.lut + off) : off;

@@ -885,7 +885,7 @@ cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, boo
 }  // namespace
 
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
-    if (a.d != kD || (a.terms & ~1u) != 0) return false;
+    if (a.d != kD || (a.terms & ~1u) != 0 || a.cls) return false;  // key tiles are whole grid rows
     const bool hk = (a.terms & 1u) != 0;
     const bool bm = a.bias != nullptr;
     if (hk && bm) return false;

@@ -65,6 +65,7 @@ struct RpeParams {
     int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     int tab_heads, heads;  // tab_heads 1: tables shared by every head; heads: one per head
     int nr;        // 64-row halves of each table: 1, or 2 for 65..128 buckets (K and V terms)
+    int cls;       // 1: token 0 is a class token (bucket nb - 1 for all its pairs)
     uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
         off_lut;
     int lut_len;
@@ -154,6 +155,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int id = __ldg(P.lut + e);
         sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
     }
+    // Class token (iRPE section 4.1): entries lut_len..2 lut_len hold the extra
+    // bucket nb - 1. The class key's offset term reaches there from every patch
+    // query and the class query's base reaches there for every key, so a pair
+    // with token 0 reads the extra bucket through the same gather.
+    if (EXT && P.cls)
+        for (int e = P.lut_len + tid; e <= 2 * P.lut_len; e += kThreads)
+            sLut[e] = static_cast<uint8_t>(P.nb - 1);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -362,7 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slice = item / P.qtiles, qt = item % P.qtiles;
             const int i = qt * kBM + t;
             const int ic = i < P.N ? i : P.N - 1;
-            const int base_i = (ic / P.W) * cols + (ic % P.W) + (P.H - 1) * cols + (P.W - 1);
+            const int centre = (P.H - 1) * cols + (P.W - 1);  // offset (0, 0)
+            const bool cls = EXT && P.cls;
+            const int pi = cls ? ic - 1 : ic;                    // grid position of the query
+            const int base_i = pi < 0 ? P.lut_len + centre : (pi / P.W) * cols + (pi % P.W) + centre;
             const uint8_t *lut_i = sLut + base_i;
             bool qr_ok = true;
             for (int r = 0; HK && r < (EXT ? P.nr : 1); ++r, ++qrc) {
@@ -416,7 +427,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int kbase = kt * kBN;
                 {
                     const int j = kbase + t < P.N ? kbase + t : P.N - 1;  // clamp padding keys
-                    sKterm[t] = (j / P.W) * cols + (j % P.W);
+                    const int pj = cls ? j - 1 : j;                       // grid position of the key
+                    sKterm[t] = pj < 0 ? centre - P.lut_len : (pj / P.W) * cols + (pj % P.W);
                 }
                 if (HQ) {
                     uint32_t r0[32], r1[32];
@@ -626,7 +638,7 @@ uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
 template <bool HK, bool HQ, bool HV, bool EXT>
 cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
-    const int N = a.H * a.W;
+    const int N = a.H * a.W + a.cls;  // the class token, if any, is token 0
     const int slices = a.B * a.heads;
     RpeParams p{};
     p.N = N;
@@ -642,6 +654,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     p.qtiles = (N + kBM - 1) / kBM;
     p.items = slices * p.qtiles;
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
+    p.cls = a.cls;
     p.lut = a.lut;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
@@ -670,7 +683,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_kterm = off;
         off += 512;
         p.off_lut = off;
-        off += align_up(p.lut_len, 16);
+        off += align_up(a.cls ? 2 * p.lut_len + 1 : p.lut_len, 16);
         const uint32_t total = 1024 + std::max<uint32_t>(off, 120 * 1024);
         if (total <= smem_cap) {
             p.nst = nst;
@@ -734,7 +747,8 @@ cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
     if (launch_rpe_bf16_pingpong(a, stream, &err)) return err;
     if (a.bias != nullptr) return cudaErrorInvalidValue;  // bias mode: ping-pong kernel only
-    if (a.cross_span > 0 || a.num_buckets > 64 || a.tab_heads > 1) return launch_terms<true>(a, stream);
+    if (a.cross_span > 0 || a.num_buckets > 64 || a.tab_heads > 1 || a.cls)
+        return launch_terms<true>(a, stream);
     return launch_terms<false>(a, stream);
 }
 

@@ -63,6 +63,7 @@ struct F32AttnArgs {
     float scale;
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
     int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
+    int cls = 0;         // 1: token 0 is a class token, its pairs in bucket num_buckets - 1
 };
 cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
 
@@ -93,6 +94,7 @@ struct RpeBf16Args {
     int bias_heads = 0;
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
     int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
+    int cls = 0;         // 1: token 0 is a class token, its pairs in bucket num_buckets - 1
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 

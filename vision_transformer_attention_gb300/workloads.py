@@ -66,15 +66,16 @@ class IrpeConfig:
     flags: int
     dtype: str
     ratio: float = IRPE_RATIO
+    cls: bool = False  # a class token at token 0, with its own extra bucket
 
     @property
     def N(self) -> int:
-        return self.H * self.W
+        return self.H * self.W + (1 if self.cls else 0)
 
     @property
     def num_buckets(self) -> int:
         span = 2 * int(2.0 * self.ratio) + 1
-        return span * span
+        return span * span + (1 if self.cls else 0)
 
     @property
     def tokens(self) -> int:
@@ -100,6 +101,9 @@ CONFIGS = {
     # uses it) on the DeiT-S shape
     "irpe_k_r2_deit_s": IrpeConfig("irpe_k_r2_deit_s", 64, 6, 14, 14, 64, FLAG_K, "bf16",
                                    ratio=2.0),
+    # DeiT-S with its class token: 197 tokens, 49 + 1 buckets
+    "irpe_k_deit_s_cls": IrpeConfig("irpe_k_deit_s_cls", 64, 6, 14, 14, 64, FLAG_K, "bf16",
+                                    cls=True),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
