@@ -79,9 +79,9 @@ constexpr int kMaxStages = 8;
 constexpr int kMaxSlots = 3;       // score slots per group (see Geo::SLOTS)
 constexpr uint32_t kColSlot0 = 64;  // within the group's 256 columns
 
-template <int W>
+template <int W, int RR>
 struct Geo {
-    static constexpr int R = 96 / W;                // grid rows per key tile
+    static constexpr int R = RR;                    // grid rows per key tile
     static constexpr int KT = R * W;                // keys per tile
     static constexpr int NS = (KT + 15) / 16 * 16;  // N of QK^T, K of PV
     static constexpr int HS = NS;  // keys per thread and tile (one thread owns a row)
@@ -194,9 +194,9 @@ __device__ __noinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_ba
 // One half (H2 = 0: keys [0, HS) of the tile, 1: keys [HS, 2 HS)) of one row's tile.
 // GATHER: the logits add a term read by bucket id from a shared-memory table
 // at stride QS floats per bucket (QR' rows: 128; a bias-mode row: 1).
-template <int W, bool GATHER, int H2, int QS = 128>
+template <int W, int R, bool GATHER, int H2, int QS = 128>
 struct HalfTile {
-    using G = Geo<W>;
+    using G = Geo<W, R>;
     static constexpr int J0 = G::HS * H2;                       // first key of the half
     static constexpr int NK = (G::KT - J0 < G::HS) ? G::KT - J0 : G::HS;  // keys of the half
     static constexpr int NQ = (NK + 15) / 16;                   // 16-key chunks holding them
@@ -330,9 +330,9 @@ struct HalfTile {
 
 // Tensor-memory column (relative to the slot) of the A operand of P V step kk
 // (keys 16 kk .. 16 kk + 15): half kk*16 / HS, chunk within it.
-template <int W>
+template <int W, int R>
 __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
-    using G = Geo<W>;
+    using G = Geo<W, R>;
     return static_cast<uint32_t>((16 * kk / G::HS) * G::HS + ((16 * kk) % G::HS) / 2);
 }
 
@@ -340,7 +340,7 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // place of the contextual key term; HK and BM are not both set. TF, the
 // table form: bit 0, the table (R^K or the bias table) is laid out for the
 // Cross mapping; bit 1, R^K is one table per head.
-template <int W, bool HK, int NG, bool BM, int TF>
+template <int W, int R, bool HK, int NG, bool BM, int TF>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     constexpr bool X = (TF & 1) != 0;   // Cross table
     constexpr bool PH = (TF & 2) != 0;  // one R^K per head
-    using G = Geo<W>;
+    using G = Geo<W, R>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
     extern __shared__ uint8_t smem_raw[];
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
 #pragma unroll
                     for (int kk = 0; kk < G::NS / 16; ++kk)
-                        mma_bf16_ts(tG, aP + p_col<W>(kk), dV + kk * (2048 >> 4), kIdO,
+                        mma_bf16_ts(tG, aP + p_col<W, R>(kk), dV + kk * (2048 >> 4), kIdO,
                                     kk > 0 ? 1u : acc0);
                     mma_commit(&bars.pv_done[w]);
                     mma_commit(&bars.kv_empty[st]);
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
                 if (warp_active) {
-                    const float mt = HalfTile<W, HK || BM, 0, BM ? 1 : 128>::logits(
+                    const float mt = HalfTile<W, R, HK || BM, 0, BM ? 1 : 128>::logits(
                         tSl, lutw, e0, BM ? bias_row : qr_t, P.c);
                     // lazy rescale: the reference max moves only when it grows by > 2^8
                     float alpha = 1.f;
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                     if (kt > 0 && __any_sync(~0u, alpha < 1.f))
                         ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
-                    l += HalfTile<W, HK || BM, 0, BM ? 1 : 128>::probs(tSl, m);
+                    l += HalfTile<W, R, HK || BM, 0, BM ? 1 : 128>::probs(tSl, m);
                     tmem_st_wait();
                 }
                 tc_fence_before();
@@ -774,9 +774,9 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
 
 uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-template <int W, bool HK, int NG, bool BM, int TF>
+template <int W, int R, bool HK, int NG, bool BM, int TF>
 cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
-    using G = Geo<W>;
+    using G = Geo<W, R>;
     using L = Layout<NG>;
     PPParams p{};
     const int N = a.H * a.W;
@@ -852,12 +852,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 3, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
-    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, HK, NG, BM, TF>,
+    cudaError_t err = cudaFuncSetAttribute(rpe_pingpong_kernel<W, R, HK, NG, BM, TF>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
-    return launch_pdl(rpe_pingpong_kernel<W, HK, NG, BM, TF>, dim3(grid), dim3(L::kThreads), total, stream,
+    return launch_pdl(rpe_pingpong_kernel<W, R, HK, NG, BM, TF>, dim3(grid), dim3(L::kThreads), total, stream,
                       tq, tk, tv, trk, to, p);
 }
 
@@ -865,21 +865,21 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
 
 namespace {
 
-template <int W>
+template <int W, int R>
 cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, bool bm) {
     constexpr int NG = kGroupsPerCta;
     const int tf = (a.cross_span > 0 ? 1 : 0) | (a.tab_heads > 1 ? 2 : 0);
-    if (bm) return (tf & 1) ? launch_pp<W, false, NG, true, 1>(a, stream)
-                            : launch_pp<W, false, NG, true, 0>(a, stream);
+    if (bm) return (tf & 1) ? launch_pp<W, R, false, NG, true, 1>(a, stream)
+                            : launch_pp<W, R, false, NG, true, 0>(a, stream);
     if (hk) {
         switch (tf) {
-            case 0: return launch_pp<W, true, NG, false, 0>(a, stream);
-            case 1: return launch_pp<W, true, NG, false, 1>(a, stream);
-            case 2: return launch_pp<W, true, NG, false, 2>(a, stream);
-            default: return launch_pp<W, true, NG, false, 3>(a, stream);
+            case 0: return launch_pp<W, R, true, NG, false, 0>(a, stream);
+            case 1: return launch_pp<W, R, true, NG, false, 1>(a, stream);
+            case 2: return launch_pp<W, R, true, NG, false, 2>(a, stream);
+            default: return launch_pp<W, R, true, NG, false, 3>(a, stream);
         }
     }
-    return launch_pp<W, false, NG, false, 0>(a, stream);
+    return launch_pp<W, R, false, NG, false, 0>(a, stream);
 }
 
 }  // namespace
@@ -892,9 +892,12 @@ bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaErr
     // the QR' product and copy cover 64 buckets; a bias row, one per thread, 128
     if ((hk && a.num_buckets > 64) || (bm && a.num_buckets > 128)) return false;
     if (a.W == 14)
-        *err = launch_width<14>(a, stream, hk, bm);
+        // key tiles of 5 or 6 grid rows (70 or 84 keys in 80 or 96 score
+        // columns), whichever leaves fewer score columns per query row
+        *err = ((a.H + 4) / 5) * 80 < ((a.H + 5) / 6) * 96 ? launch_width<14, 5>(a, stream, hk, bm)
+                                                          : launch_width<14, 6>(a, stream, hk, bm);
     else if (a.W == 56)
-        *err = launch_width<56>(a, stream, hk, bm);
+        *err = launch_width<56, 1>(a, stream, hk, bm);
     else
         return false;
     return true;
