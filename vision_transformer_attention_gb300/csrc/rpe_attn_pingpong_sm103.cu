@@ -173,7 +173,7 @@ __device__ __forceinline__ bool red_and(int id, int nthreads, bool v) {
 
 // Multiply this row's O (64 columns) by alpha once the group's previous P V
 // has completed. Out of line: it runs only when a row's reference max moves.
-__device__ __noinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
+__device__ __forceinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
                                        uint32_t pv_parity, const WaitCtl &wc,
                                        volatile int *abort) {
     if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort))) return false;
@@ -215,18 +215,19 @@ struct HalfTile {
     static constexpr int NA = (W < NK ? W : NK) / 4 + 1;  // >= run_words of any row
     static constexpr int first_chunk(int r) { return ((J0 > r * W ? J0 : r * W) - J0) / 16; }
 
-    // Pass 1: x = S c + QR'[id] over the half's keys, stored back over the
-    // scores, 16 keys at a time; returns the half's max. lutw: the offset
-    // table as words; e0: byte index in it of the tile's key 0 for this row;
-    // qr_t: this row's QR' for bucket 0 (buckets 128 floats apart).
+    // Pass 1: x = S c + QR'[id] over the half's keys, 16 keys at a time, kept
+    // in registers (s, the scores' own registers) for pass 2; returns the
+    // half's max. lutw: the offset table as words; e0: byte index in it of the
+    // tile's key 0 for this row; qr_t: this row's QR' for bucket 0 (buckets
+    // 128 floats apart).
     static __device__ __forceinline__ float logits(uint32_t tS, const uint32_t *lutw, int e0,
-                                                   const float *qr_t, float c) {
+                                                   const float *qr_t, float c,
+                                                   uint32_t (&s)[NQ][16]) {
         uint32_t ida[NROWS][NA];
         float mx = -INFINITY;
         const float2 c2 = make_float2(c, c);
         // all of the row's scores in one tensor-memory round trip; its latency
         // overlaps the first chunk's gathers
-        uint32_t s[NQ][16];
 #pragma unroll
         for (int q = 0; q < NQ; ++q) tmem_ld16(tS + J0 + 16 * q, s[q]);
 #pragma unroll
@@ -282,28 +283,19 @@ struct HalfTile {
             const float d = fmax3(x[6], x[7], x[8]), e = fmax3(x[9], x[10], x[11]);
             const float f = fmax3(x[12], x[13], x[14]);
             mx = fmax3(mx, fmax3(a, b, d), fmax3(e, f, x[15]));
-            uint32_t xs[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xs[j] = __float_as_uint(x[j]);
-            tmem_st16(tS + jc, xs);
+            for (int j = 0; j < 16; ++j) s[q][j] = __float_as_uint(x[j]);
         }
         return mx;
     }
 
-    // Pass 2: p = 2^(x - m) as bf16 pairs; chunk q's 8 columns go to J0 + 8q,
-    // over logits already read. Keys past the tile contribute 0. Returns sum p.
-    static __device__ __forceinline__ float probs(uint32_t tS, float m) {
-        tmem_st_wait();
+    // Pass 2: p = 2^(x - m) as bf16 pairs from pass 1's registers; chunk q's
+    // 8 columns go to J0 + 8q, over scores already read. Keys past the tile
+    // contribute 0. Returns sum p.
+    static __device__ __forceinline__ float probs(uint32_t tS, float m,
+                                                  const uint32_t (&xs)[NQ][16]) {
         float sum = 0.f;
         const float2 nm = make_float2(-m, -m);
-        // all of the row's logits in one round trip (so no chunk's P overwrites
-        // logits still to be read)
-        uint32_t xs[NQ][16];
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) tmem_ld16(tS + J0 + 16 * q, xs[q]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) tmem_ready(xs[q]);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             const int jc = J0 + 16 * q;
@@ -708,9 +700,10 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 tc_fence_after();
                 const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
+                using Tile = HalfTile<W, R, HK || BM, 0, BM ? 1 : 128>;
                 if (warp_active) {
-                    const float mt = HalfTile<W, R, HK || BM, 0, BM ? 1 : 128>::logits(
-                        tSl, lutw, e0, BM ? bias_row : qr_t, P.c);
+                    uint32_t xs[Tile::NQ][16];  // the row's logits, pass 1 to pass 2
+                    const float mt = Tile::logits(tSl, lutw, e0, BM ? bias_row : qr_t, P.c, xs);
                     // lazy rescale: the reference max moves only when it grows by > 2^8
                     float alpha = 1.f;
                     if (mt > m + kRescaleLog2) {
@@ -720,7 +713,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                     if (kt > 0 && __any_sync(~0u, alpha < 1.f))
                         ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
-                    l += HalfTile<W, R, HK || BM, 0, BM ? 1 : 128>::probs(tSl, m);
+                    l += Tile::probs(tSl, m, xs);
                     tmem_st_wait();
                 }
                 tc_fence_before();
