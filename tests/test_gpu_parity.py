@@ -249,3 +249,32 @@ def test_irpe_bf16_pingpong_rescale_path():
     inp["v"] = (0.5 * inp["v"].float()).to(torch.bfloat16)
     _, out = _irpe_run(1, 2, H, W, flags, inp=inp)
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
+
+
+# ------------------------------------------------------------ split tail items (two-warpgroup kernel)
+
+@pytest.mark.parametrize("flags,bias", [(FLAG_K, False), (0, True)])
+def test_irpe_bf16_split_tail_items(flags, bias):
+    # 200 slices of one item each on 152 SMs: the last 48 items run as two parts
+    # on two CTAs each and are merged; check whole slices on both sides of the
+    # boundary, and that repeating the call gives the same bits
+    B, heads, H, W = 40, 5, 14, 14
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *workloads.index_constants())
+    inp = workloads.irpe_inputs(B, heads, H * W, 64, nb, flags, "bf16", 1.0, seed=51)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    ids, K = oracle.product_bucket_ids(H, W, *workloads.index_constants())
+    if bias:
+        tab = workloads.bias_table(nb, heads, 2.0, seed=52)
+        run = lambda: api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], tab.cuda(), lut, nb, H, W)  # noqa: E731
+    else:
+        tab = None
+        run = lambda: api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,  # noqa: E731
+                                       table_k=g["tab_k"])
+    out = run()
+    S = B * heads
+    sl = np.array([0, 151, 152, 170, S - 1])
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags, tab_k=inp["tab_k"],
+                                    bias_in=None if tab is None else tab.numpy(), slices=sl)
+    got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, H * W, 64)[sl]) <= TOL_BF16
+    assert torch.equal(run(), out)

@@ -18,6 +18,9 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 unsigned *g_status[kMaxDevices] = {};
+float *g_split_ws[kMaxDevices] = {};
+size_t g_split_ws_floats[kMaxDevices] = {};
+int *g_split_cnt[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -57,6 +60,35 @@ unsigned *device_status_word() {
         g_status[dev] = static_cast<unsigned *>(p);
     }
     return g_status[dev];
+}
+
+bool device_split_workspace(size_t floats, float **ws, int **counters) {
+    const int dev = current_device();
+    if (dev < 0) return false;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_split_cnt[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, kSplitCounters * sizeof(int)) != cudaSuccess) return false;
+        if (cudaMemset(p, 0, kSplitCounters * sizeof(int)) != cudaSuccess) {
+            cudaFree(p);
+            return false;
+        }
+        g_split_cnt[dev] = static_cast<int *>(p);
+    }
+    if (g_split_ws_floats[dev] < floats) {
+        void *p = nullptr;
+        if (cudaMalloc(&p, floats * sizeof(float)) != cudaSuccess) return false;
+        if (g_split_ws[dev] != nullptr) {
+            // an earlier launch may still read the old buffer
+            cudaDeviceSynchronize();
+            cudaFree(g_split_ws[dev]);
+        }
+        g_split_ws[dev] = static_cast<float *>(p);
+        g_split_ws_floats[dev] = floats;
+    }
+    *ws = g_split_ws[dev];
+    *counters = g_split_cnt[dev];
+    return true;
 }
 
 int sm_count() {

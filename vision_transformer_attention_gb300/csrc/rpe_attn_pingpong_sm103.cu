@@ -108,6 +108,14 @@ struct PPParams {
     uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
+    // Tail split: items [0, whole) run whole, in full rounds over the grid; the
+    // `tail` items after them run as two parts on two CTAs, part A over key
+    // tiles [0, ka), part B over [ka, nkt), merged by the later part through
+    // ws (per (tail item, group, part): O [64][128], m [128], l [128]) and
+    // the arrival counters cnt (one per tail item and group).
+    int whole, tail, ka;
+    float *ws;
+    int *cnt;
     const int32_t *lut;
     float c;  // log2(e) / sqrt(d)
     WaitCtl wc;
@@ -125,14 +133,33 @@ struct PPBars {
 struct Item {
     int slice, qt0;
     bool has_b;
+    int kt0, kt1;  // key tiles of this entry
+    int part;      // 0: the whole item; 1, 2: part A, B of tail item tidx
+    int tidx;
 };
 
 // Items: full pairs of query tiles (slice-major), then the odd last tiles,
 // dealt round-robin over the CTAs (an odd tile takes about as long as a pair:
-// the two groups of a pair run side by side). item_at(P, k) is the k-th item
+// the two groups of a pair run side by side). item_at<SP>(P, k) is the k-th item
 // of this CTA, -1 past its last; every role walks the same sequence.
-__device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
+template <bool SP>
+__device__ __forceinline__ Item decode_item(const PPParams &P, int entry) {
     Item r;
+    int item = entry;
+    r.kt0 = 0;
+    r.kt1 = P.nkt;
+    r.part = 0;
+    r.tidx = 0;
+    if (SP && entry >= P.items) {  // a part of a split tail item
+        const int j = (entry - P.items) % P.tail;
+        r.part = 1 + (entry - P.items) / P.tail;
+        r.tidx = j;
+        item = P.whole + j;
+        if (r.part == 1)
+            r.kt1 = P.ka;
+        else
+            r.kt0 = P.ka;
+    }
     if (P.single) {
         r.slice = item / P.qtiles;
         r.qt0 = item % P.qtiles;
@@ -152,9 +179,22 @@ __device__ __forceinline__ Item decode_item(const PPParams &P, int item) {
     return r;
 }
 
+// The k-th entry of this CTA: whole items in full rounds, then the tail parts.
+// With T <= G / 2 tail items on G CTAs, CTA c < T runs part A of tail item c
+// and CTA T + j part B of tail item j, so no CTA runs more than one part and
+// the last round takes about half an item. Entries >= items encode parts:
+// items + j (A) and items + T + j (B).
+template <bool SP>
 __device__ __forceinline__ int item_at(const PPParams &P, int k) {
-    const int item = blockIdx.x + k * gridDim.x;
-    return item < P.items ? item : -1;
+    const int G = gridDim.x, c = blockIdx.x;
+    if (!SP || P.tail == 0) {
+        const int item = c + k * G;
+        return item < P.items ? item : -1;
+    }
+    const int r0 = P.whole / G;
+    if (k < r0) return c + k * G;
+    if (k > r0 || c >= 2 * P.tail) return -1;
+    return P.items + c;  // c < T: A part of tail item c; else B part of tail item c - T
 }
 
 // AND-reduction of v over the nthreads threads that use named barrier id.
@@ -331,7 +371,8 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // BM: iRPE bias mode (a scalar per bucket and head, inside the scaling) in
 // place of the contextual key term; HK and BM are not both set. TF, the
 // table form: bit 0, the table (R^K or the bias table) is laid out for the
-// Cross mapping; bit 1, R^K is one table per head.
+// Cross mapping; bit 1, R^K is one table per head; bit 2, the tail items may
+// run split in two parts (see item_at).
 template <int W, int R, bool HK, int NG, bool BM, int TF>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -341,6 +382,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     constexpr bool X = (TF & 1) != 0;   // Cross table
     constexpr bool PH = (TF & 2) != 0;  // one R^K per head
+    constexpr bool SP = (TF & 4) != 0;  // the tail items may run split
     using G = Geo<W, R>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
@@ -350,6 +392,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     __shared__ PPBars bars;
     __shared__ uint32_t tmem_base_s;
     __shared__ volatile int abort_flag;
+    __shared__ volatile int split_arrivals[2];  // per group: arrivals before this part
 
     griddep_launch_dependents();
     const int tid = threadIdx.x;
@@ -440,8 +483,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 int last_use[kMaxStages];
                 for (int st = 0; st < kMaxStages; ++st) last_use[st] = -1;
                 bool ok = true;
-                for (int item = item_at(P, 0); ok && item >= 0; item = item_at(P, ++it)) {
-                    const Item I = decode_item(P, item);
+                for (int item = item_at<SP>(P, 0); ok && item >= 0; item = item_at<SP>(P, ++it)) {
+                    const Item I = decode_item<SP>(P, item);
                     const int qb = it % P.nq, quse = it / P.nq;
                     if (!(ok = mbar_wait(&bars.q_empty[qb], (quse & 1) ^ 1, wc, kStatusTimeoutSync,
                                          &abort_flag)))
@@ -463,7 +506,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         tma_load_3d(qd + kTileBytes, &tm_q, &bars.q_full[qb], 0, (I.qt0 + 1) * 128,
                                     I.slice);
                     last_q[qb] = quse;
-                    for (int kt = 0; kt < P.nkt; ++kt, ++g) {
+                    for (int kt = I.kt0; kt < I.kt1; ++kt, ++g) {
                         const int st = g % P.nst, use = g / P.nst;
                         if (!(ok = mbar_wait(&bars.kv_empty[st], (use & 1) ^ 1, wc,
                                              kStatusTimeoutSync, &abort_flag)))
@@ -542,15 +585,15 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     }
                 };
                 int g = 0, it = 0;
-                for (int item = item_at(P, 0); ok && item >= 0; item = item_at(P, ++it)) {
-                    const Item I = decode_item(P, item);
+                for (int item = item_at<SP>(P, 0); ok && item >= 0; item = item_at<SP>(P, ++it)) {
+                    const Item I = decode_item<SP>(P, item);
                     const int qb = it % P.nq;
                     ok = mbar_wait(&bars.q_full[qb], (it / P.nq) & 1, wc, kStatusTimeoutLoad, &abort_flag);
                     if (w == 1 && !I.has_b) {
                         // the outstanding units' P V release K/V stages that the
                         // loads below may be waiting for: issue them first
                         while (ok && np > 0) consume();
-                        for (int kt = 0; ok && kt < P.nkt; ++kt, ++g) {
+                        for (int kt = I.kt0; ok && kt < I.kt1; ++kt, ++g) {
                             const int st = g % P.nst;
                             ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc, kStatusTimeoutLoad,
                                            &abort_flag);
@@ -560,13 +603,13 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         continue;
                     }
                     const uint64_t dQ = hi128 | ((aQ + qb * NG * kTileBytes) >> 4);
-                    for (int kt = HK ? -1 : 0; ok && kt < P.nkt; ++kt) {
+                    for (int kt = HK ? I.kt0 - 1 : I.kt0; ok && kt < I.kt1; ++kt) {
                         if (np == G::SLOTS) consume();
                         if (!ok) break;
                         const uint32_t slot = u % G::SLOTS;
                         const uint32_t dS = tG + kColSlot0 + slot * G::NS;
                         uint32_t code;
-                        if (kt < 0) {
+                        if (kt < I.kt0) {  // the QR' unit
                             tc_fence_after();
                             const uint32_t rk_off = PH ? qb * (kTileBytes / 2) : 0;
                             const uint64_t dRK = hi128 | (smem_u32(sRK + rk_off) >> 4);
@@ -589,11 +632,11 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                                 const uint64_t dMA = smem_desc(smem_u32(smem + P.off_mask), 16, 256, kSwizzle32B);
                                 mma_bf16_ss(dS, dMA, dMA + (4096 >> 4), kIdS, 1u);
                             }
-                            code = static_cast<uint32_t>(st) | (kt == 0 ? 0x20u : 0u) | (last ? 0x40u : 0u);
+                            code = static_cast<uint32_t>(st) | (kt == I.kt0 ? 0x20u : 0u) | (kt == I.kt1 - 1 ? 0x40u : 0u);
                             ++g;
                         }
                         mma_commit(&bars.slot_full[w][slot]);
-                        if (kt == P.nkt - 1) mma_commit(&bars.q_empty[qb]);
+                        if (kt == I.kt1 - 1) mma_commit(&bars.q_empty[qb]);
                         if (np == 0) pend0 = code; else if (np == 1) pend1 = code; else pend2 = code;
                         ++np;
                         ++u;
@@ -633,8 +676,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         const uint32_t *lutw = reinterpret_cast<const uint32_t *>(sLut);
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
-        for (int item = item_at(P, 0), k_item = 0; item >= 0; item = item_at(P, ++k_item)) {
-            const Item I = decode_item(P, item);
+        for (int item = item_at<SP>(P, 0), k_item = 0; item >= 0; item = item_at<SP>(P, ++k_item)) {
+            const Item I = decode_item<SP>(P, item);
             if (wg == 1 && !I.has_b) continue;
             const int qt = I.qt0 + wg;
             const int i = qt * 128 + t;
@@ -692,7 +735,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 ++u;
             }
             float m = -INFINITY, l = 0.f;
-            for (int kt = 0; kt < P.nkt; ++kt, ++gw, ++u) {
+            for (int kt = I.kt0; kt < I.kt1; ++kt, ++gw, ++u) {
                 slot = u % G::SLOTS;
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
                                                kStatusTimeoutMma, &abort_flag)) && ok;
@@ -711,7 +754,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         m = mt;
                         l *= alpha;
                     }
-                    if (kt > 0 && __any_sync(~0u, alpha < 1.f))
+                    if (kt > I.kt0 && __any_sync(~0u, alpha < 1.f))
                         ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
                     l += Tile::probs(tSl, m, xs);
                     tmem_st_wait();
@@ -724,14 +767,65 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                                                &abort_flag));
             if (!red_and(group_bar, 128, ok)) break;
             tc_fence_after();
+            float inv = 1.f / l;
+            // A part of a split tail item hands its unnormalised state (O, m, l)
+            // to the workspace and counts its arrival; the later of the two
+            // parts merges the other's state into its own and writes the
+            // output, the earlier one is done. No part waits for the other.
+            float a_self = 1.f, a_other = 0.f;
+            const float *other = nullptr;
+            if (SP && I.part != 0) {
+                constexpr size_t kSlot = 66 * 128;  // O [64][128], m [128], l [128]
+                const size_t pair = static_cast<size_t>(I.tidx * 2 + wg) * 2;
+                float *mine = P.ws + (pair + (I.part - 1)) * kSlot;
+                if (warp_active) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 4; ++c2) {
+                        uint32_t o[16];
+                        tmem_ld16(tOl + 16 * c2, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) mine[(16 * c2 + e) * 128 + t] = __uint_as_float(o[e]);
+                    }
+                    mine[64 * 128 + t] = m;
+                    mine[65 * 128 + t] = l;
+                }
+                __threadfence();
+                named_bar_sync(group_bar, 128);
+                if (leader) split_arrivals[wg] = atomicAdd(P.cnt + I.tidx * 2 + wg, 1);
+                named_bar_sync(group_bar, 128);
+                if (split_arrivals[wg] == 0) {
+                    tc_fence_before();
+                    mbar_arrive(&bars.o_empty[wg]);
+                    ++it_w;
+                    continue;
+                }
+                __threadfence();
+                if (leader) P.cnt[I.tidx * 2 + wg] = 0;  // both arrived: ready for the next launch
+                other = P.ws + (pair + (2 - I.part)) * kSlot;
+                if (warp_active) {
+                    // symmetric in the two parts (separately rounded products, one
+                    // sum), so the result does not depend on which part came later
+                    const float m2 = __ldcg(other + 64 * 128 + t), l2 = __ldcg(other + 65 * 128 + t);
+                    const float mm = fmaxf(m, m2);
+                    a_self = ex2_approx(m - mm);
+                    a_other = ex2_approx(m2 - mm);
+                    inv = 1.f / (__fmul_rn(l, a_self) + __fmul_rn(l2, a_other));
+                }
+            }
             // normalise the row's 64 output columns into the staging tile, 16 at a time
-            const float inv = 1.f / l;
 #pragma unroll
             for (int c2 = 0; c2 < 4; ++c2) {
                 uint32_t o[16];
                 if (warp_active) {
                     tmem_ld16(tOl + 16 * c2, o);
                     tmem_ld_wait(o);
+                    if (other != nullptr) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), a_self) +
+                                                   __fmul_rn(__ldcg(other + (16 * c2 + e) * 128 + t), a_other));
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -850,6 +944,28 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
                                            static_cast<int>(total));
     if (err != cudaSuccess) return err;
     const int grid = std::min(p.items, sm_count() * L::kCtasPerSm);
+    // Tail split: the items of the last, partial round run as two parts each
+    // (see item_at) when that round fills at most half the grid, so each CTA
+    // runs one part at most. (With more, some CTAs would run two parts, and
+    // at a few key tiles per item two parts cost more than a whole item: the
+    // DeiT-S shape, 80 tail items on 152 SMs, measured 22.5 -> 32.3 us.)
+    p.whole = p.items;
+    p.tail = 0;
+    p.ka = p.nkt;
+    if constexpr ((TF & 4) != 0) {
+        const int T = p.items % grid;
+        if (T > 0 && p.nkt >= 2 && 2 * T <= grid && 2 * T <= kSplitCounters) {
+            float *ws = nullptr;
+            int *cnt = nullptr;
+            if (device_split_workspace(static_cast<size_t>(T) * 4 * 66 * 128, &ws, &cnt)) {
+                p.whole = p.items - T;
+                p.tail = T;
+                p.ws = ws;
+                p.cnt = cnt;
+                p.ka = (p.nkt + 1) / 2;  // part A: the first half of the key tiles
+            }
+        }
+    }
     return launch_pdl(rpe_pingpong_kernel<W, R, HK, NG, BM, TF>, dim3(grid), dim3(L::kThreads), total, stream,
                       tq, tk, tv, trk, to, p);
 }
@@ -862,17 +978,30 @@ template <int W, int R>
 cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, bool bm) {
     constexpr int NG = kGroupsPerCta;
     const int tf = (a.cross_span > 0 ? 1 : 0) | (a.tab_heads > 1 ? 2 : 0);
+    // the split-tail variant (shared, non-Cross tables only) when the last round
+    // of items fills at most half the grid (the rule launch_pp applies)
+    bool sp = false;
+    if (tf == 0) {
+        const int N = a.H * a.W, qtiles = (N + 127) / 128, slices = a.B * a.heads;
+        const int items = slices * (qtiles / 2) + ((qtiles & 1) ? slices : 0);
+        const int grid = std::min(items, sm_count() * Layout<NG>::kCtasPerSm);
+        const int T = items % grid, nkt = (a.H + R - 1) / R;
+        sp = T > 0 && nkt >= 2 && 2 * T <= grid;
+    }
     if (bm) return (tf & 1) ? launch_pp<W, R, false, NG, true, 1>(a, stream)
+                 : sp       ? launch_pp<W, R, false, NG, true, 4>(a, stream)
                             : launch_pp<W, R, false, NG, true, 0>(a, stream);
     if (hk) {
         switch (tf) {
-            case 0: return launch_pp<W, R, true, NG, false, 0>(a, stream);
+            case 0: return sp ? launch_pp<W, R, true, NG, false, 4>(a, stream)
+                              : launch_pp<W, R, true, NG, false, 0>(a, stream);
             case 1: return launch_pp<W, R, true, NG, false, 1>(a, stream);
             case 2: return launch_pp<W, R, true, NG, false, 2>(a, stream);
             default: return launch_pp<W, R, true, NG, false, 3>(a, stream);
         }
     }
-    return launch_pp<W, R, false, NG, false, 0>(a, stream);
+    return sp ? launch_pp<W, R, false, NG, false, 4>(a, stream)
+              : launch_pp<W, R, false, NG, false, 0>(a, stream);
 }
 
 }  // namespace

@@ -15,6 +15,14 @@ struct WaitCtl;
 // Device status word of the current device (allocated on first use; NULL if
 // that failed) and the default bound on in-kernel waits.
 unsigned *device_status_word();
+
+// Workspace of the split tail items of the two-warpgroup kernel on the current
+// device: at least `floats` fp32 (grown on demand, never shrunk) and
+// kSplitCounters arrival counters (zero between launches: the last arrival
+// resets its counter). False if an allocation failed. Launches that overlap on
+// one device share both, so they must not run the split path concurrently.
+constexpr int kSplitCounters = 4096;
+bool device_split_workspace(size_t floats, float **ws, int **counters);
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // Number of SMs of the current device (cached per device).
