@@ -105,7 +105,7 @@ struct PPParams {
     int tab_row2;  // table row staged at shared-memory row 32: span (Cross) or 32
     const float *bias;  // bias mode: [nb, bias_heads] fp32
     int bias_heads, heads;
-    uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask;
+    uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask, off_stage;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
     // Tail split: items [0, whole) run whole, in full rounds over the grid; the
@@ -665,17 +665,119 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         const uint32_t lane_off = static_cast<uint32_t>(lq * 32) << 16;
         const uint32_t tG = tmem + wg * 256;
         const uint32_t tOl = tG + lane_off;
-        // The group's QR' table [bucket][128 rows] fp32; during the epilogue it
-        // holds the output tile (128 rows x 128 bytes, 128-byte swizzle) for the
-        // TMA store. A thread reads and writes only its own row of it.
+        // The group's QR' table [bucket][128 rows] fp32 (a thread reads and
+        // writes only its own row of it).
         uint8_t *qr_base = smem + P.off_qr + wg * P.qr_stride;
         float *qr_t = reinterpret_cast<float *>(qr_base) + t;
         // bias mode: the item's head's bias row, scaled, in the same region
         float *bias_row = reinterpret_cast<float *>(qr_base);
-        const uint32_t stage_row = smem_u32(qr_base) + t * 128;
         const uint32_t *lutw = reinterpret_cast<const uint32_t *>(sLut);
         uint32_t u = 0;  // this group's unit counter
         int it_w = 0, gw = 0;
+        // The group's output staging tile (128 rows x 128 bytes, 128-byte
+        // swizzle) for the TMA store; a thread writes only its own row.
+        uint8_t *stage = smem + P.off_stage + wg * kTileBytes;
+        const uint32_t stage_row = smem_u32(stage) + t * 128;
+        // The item whose epilogue is still due. It runs after the next item's QR'
+        // copy (or after the last item), so that the copy overlaps the wait for
+        // the item's last P V.
+        bool ok = true, due = false;
+        Item D{};
+        float due_m = 0.f, due_l = 1.f;
+        auto epilogue = [&]() -> bool {
+            const bool okd = ok && __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc,
+                                                            kStatusTimeoutMma, &abort_flag));
+            // the previous TMA store has read the staging tile (the vote's
+            // barrier orders this before the group's staging writes)
+            if (leader) bulk_wait_read_all();
+            if (!red_and(group_bar, 128, okd)) return false;
+            tc_fence_after();
+            const int dqt = D.qt0 + wg;
+            const int di = dqt * 128 + t;
+            const bool dactive = dqt * 128 + lq * 32 < P.N;
+            float inv = 1.f / due_l;
+            // A part of a split tail item hands its unnormalised state (O, m, l)
+            // to the workspace and counts its arrival; the later of the two
+            // parts merges the other's state into its own and writes the
+            // output, the earlier one is done. No part waits for the other.
+            float a_self = 1.f, a_other = 0.f;
+            const float *other = nullptr;
+            if (SP && D.part != 0) {
+                constexpr size_t kSlot = 66 * 128;  // O [64][128], m [128], l [128]
+                const size_t pair = static_cast<size_t>(D.tidx * 2 + wg) * 2;
+                float *mine = P.ws + (pair + (D.part - 1)) * kSlot;
+                if (dactive) {
+#pragma unroll
+                    for (int c2 = 0; c2 < 4; ++c2) {
+                        uint32_t o[16];
+                        tmem_ld16(tOl + 16 * c2, o);
+                        tmem_ld_wait(o);
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) mine[(16 * c2 + e) * 128 + t] = __uint_as_float(o[e]);
+                    }
+                    mine[64 * 128 + t] = due_m;
+                    mine[65 * 128 + t] = due_l;
+                }
+                __threadfence();
+                named_bar_sync(group_bar, 128);
+                if (leader) split_arrivals[wg] = atomicAdd(P.cnt + D.tidx * 2 + wg, 1);
+                named_bar_sync(group_bar, 128);
+                if (split_arrivals[wg] == 0) {
+                    tc_fence_before();
+                    mbar_arrive(&bars.o_empty[wg]);
+                    ++it_w;
+                    return true;
+                }
+                __threadfence();
+                if (leader) P.cnt[D.tidx * 2 + wg] = 0;  // both arrived: ready for the next launch
+                other = P.ws + (pair + (2 - D.part)) * kSlot;
+                if (dactive) {
+                    // symmetric in the two parts (separately rounded products, one
+                    // sum), so the result does not depend on which part came later
+                    const float m2 = __ldcg(other + 64 * 128 + t), l2 = __ldcg(other + 65 * 128 + t);
+                    const float mm = fmaxf(due_m, m2);
+                    a_self = ex2_approx(due_m - mm);
+                    a_other = ex2_approx(m2 - mm);
+                    inv = 1.f / (__fmul_rn(due_l, a_self) + __fmul_rn(l2, a_other));
+                }
+            }
+            // normalise the row's 64 output columns into the staging tile, 16 at a time
+#pragma unroll
+            for (int c2 = 0; c2 < 4; ++c2) {
+                uint32_t o[16];
+                if (dactive) {
+                    tmem_ld16(tOl + 16 * c2, o);
+                    tmem_ld_wait(o);
+                    if (other != nullptr) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), a_self) +
+                                                   __fmul_rn(__ldcg(other + (16 * c2 + e) * 128 + t), a_other));
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    const uint32_t *src = o + 8 * c;
+                    const int chunk = 2 * c2 + c;
+                    st_shared_v4(stage_row + ((chunk ^ (t & 7)) << 4),
+                                 pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
+                                 pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars.o_empty[wg]);
+            fence_proxy_async_smem();
+            named_bar_sync(group_bar, 128);
+            if (leader) {
+                // rows past the grid fall outside the tensor map and are not written
+                tma_store_3d(&tm_o, stage, 0, dqt * 128, D.slice);
+                bulk_commit_group();
+            }
+            ++it_w;
+            return true;
+        };
         for (int item = item_at<SP>(P, 0), k_item = 0; item >= 0; item = item_at<SP>(P, ++k_item)) {
             const Item I = decode_item<SP>(P, item);
             if (wg == 1 && !I.has_b) continue;
@@ -684,14 +786,14 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             const bool warp_active = qt * 128 + lq * 32 < P.N;
             const int ic = i < P.N ? i : P.N - 1;
             const int base_i = (ic / W) * G::COLS + (ic % W) + (P.H - 1) * G::COLS + (W - 1);
-            // the previous item's TMA store has read the staging area (the QR' table)
-            if (leader && it_w > 0) bulk_wait_read_all();
-            bool ok = true;
             uint32_t slot = u % G::SLOTS;
             if (HK)
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
-                                               kStatusTimeoutMma, &abort_flag));
-            if (!red_and(group_bar, 128, ok)) break;
+                                               kStatusTimeoutMma, &abort_flag)) && ok;
+            if (!red_and(group_bar, 128, ok)) {
+                ok = false;
+                break;
+            }
             if (BM) {
                 // the item's bias row, pre-scaled like the logits (eq. 13: inside
                 // the 1/sqrt(d) scaling); visible to the group after the barrier
@@ -734,6 +836,10 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 mbar_arrive(&bars.slot_done[wg][slot]);
                 ++u;
             }
+            if (due && !epilogue()) {
+                ok = false;
+                break;
+            }
             float m = -INFINITY, l = 0.f;
             for (int kt = I.kt0; kt < I.kt1; ++kt, ++gw, ++u) {
                 slot = u % G::SLOTS;
@@ -762,93 +868,12 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 tc_fence_before();
                 mbar_arrive(&bars.slot_done[wg][slot]);
             }
-            if (ok)
-                ok = __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc, kStatusTimeoutMma,
-                                               &abort_flag));
-            if (!red_and(group_bar, 128, ok)) break;
-            tc_fence_after();
-            float inv = 1.f / l;
-            // A part of a split tail item hands its unnormalised state (O, m, l)
-            // to the workspace and counts its arrival; the later of the two
-            // parts merges the other's state into its own and writes the
-            // output, the earlier one is done. No part waits for the other.
-            float a_self = 1.f, a_other = 0.f;
-            const float *other = nullptr;
-            if (SP && I.part != 0) {
-                constexpr size_t kSlot = 66 * 128;  // O [64][128], m [128], l [128]
-                const size_t pair = static_cast<size_t>(I.tidx * 2 + wg) * 2;
-                float *mine = P.ws + (pair + (I.part - 1)) * kSlot;
-                if (warp_active) {
-#pragma unroll
-                    for (int c2 = 0; c2 < 4; ++c2) {
-                        uint32_t o[16];
-                        tmem_ld16(tOl + 16 * c2, o);
-                        tmem_ld_wait(o);
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) mine[(16 * c2 + e) * 128 + t] = __uint_as_float(o[e]);
-                    }
-                    mine[64 * 128 + t] = m;
-                    mine[65 * 128 + t] = l;
-                }
-                __threadfence();
-                named_bar_sync(group_bar, 128);
-                if (leader) split_arrivals[wg] = atomicAdd(P.cnt + I.tidx * 2 + wg, 1);
-                named_bar_sync(group_bar, 128);
-                if (split_arrivals[wg] == 0) {
-                    tc_fence_before();
-                    mbar_arrive(&bars.o_empty[wg]);
-                    ++it_w;
-                    continue;
-                }
-                __threadfence();
-                if (leader) P.cnt[I.tidx * 2 + wg] = 0;  // both arrived: ready for the next launch
-                other = P.ws + (pair + (2 - I.part)) * kSlot;
-                if (warp_active) {
-                    // symmetric in the two parts (separately rounded products, one
-                    // sum), so the result does not depend on which part came later
-                    const float m2 = __ldcg(other + 64 * 128 + t), l2 = __ldcg(other + 65 * 128 + t);
-                    const float mm = fmaxf(m, m2);
-                    a_self = ex2_approx(m - mm);
-                    a_other = ex2_approx(m2 - mm);
-                    inv = 1.f / (__fmul_rn(l, a_self) + __fmul_rn(l2, a_other));
-                }
-            }
-            // normalise the row's 64 output columns into the staging tile, 16 at a time
-#pragma unroll
-            for (int c2 = 0; c2 < 4; ++c2) {
-                uint32_t o[16];
-                if (warp_active) {
-                    tmem_ld16(tOl + 16 * c2, o);
-                    tmem_ld_wait(o);
-                    if (other != nullptr) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), a_self) +
-                                                   __fmul_rn(__ldcg(other + (16 * c2 + e) * 128 + t), a_other));
-                    }
-                }
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const uint32_t *src = o + 8 * c;
-                    const int chunk = 2 * c2 + c;
-                    st_shared_v4(stage_row + ((chunk ^ (t & 7)) << 4),
-                                 pack_bf16x2(__uint_as_float(src[0]) * inv, __uint_as_float(src[1]) * inv),
-                                 pack_bf16x2(__uint_as_float(src[2]) * inv, __uint_as_float(src[3]) * inv),
-                                 pack_bf16x2(__uint_as_float(src[4]) * inv, __uint_as_float(src[5]) * inv),
-                                 pack_bf16x2(__uint_as_float(src[6]) * inv, __uint_as_float(src[7]) * inv));
-                }
-            }
-            tc_fence_before();
-            mbar_arrive(&bars.o_empty[wg]);
-            fence_proxy_async_smem();
-            named_bar_sync(group_bar, 128);
-            if (leader) {
-                // rows past the grid fall outside the tensor map and are not written
-                tma_store_3d(&tm_o, qr_base, 0, qt * 128, I.slice);
-                bulk_commit_group();
-            }
-            ++it_w;
+            due = true;
+            D = I;
+            due_m = m;
+            due_l = l;
         }
+        if (due) epilogue();
         if (leader) bulk_wait_all();
     }
     tc_fence_before();
@@ -901,9 +926,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_rk = off;
         if (HK) off += (a.tab_heads > 1 ? nq : 1) * (kTileBytes / 2);
         p.off_qr = off;
-        // each group's QR' table doubles as its 16 KB output staging tile
-        p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, 128 * 128), 1024);
+        // each group's QR' table (or bias row)
+        p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, BM ? 512 : 0), 1024);
         off += NG * p.qr_stride;
+        // each group's output staging tile (128 rows x 128 bytes, 128-byte swizzle)
+        p.off_stage = off;
+        off += NG * kTileBytes;
         p.off_mask = off;
         off += 2 * 4096;
         p.off_lut = off;
