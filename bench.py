@@ -80,11 +80,11 @@ def workload_config(cfg):
 DOMINANT = {
     "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", 57840640 + 1616128),
     "swin_t_stage1_fmap": ("swin_bf16_kernel<7,32,fmap>", "hbm", 57851136 + 1450752),
-    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,K>", "hbm", 29001472 + 0),
-    "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29064960 + 2816),
-    "irpe_k_56x56": ("rpe_pingpong_kernel<56,K>", "tensor", 58131200 + 2073856),
-    "irpe_k_r2_deit_s": ("rpe_bf16_kernel<K>", "hbm", None),
-    "irpe_k_deit_s_cls": ("rpe_bf16_kernel<K>", "hbm", None),
+    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,5,K>", "hbm", 29005568 + 0),
+    "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29142272 + 2304),
+    "irpe_k_56x56": ("rpe_pingpong_kernel<56,1,K,split>", "tensor", 58197504 + 2228736),
+    "irpe_k_r2_deit_s": ("rpe_bf16_kernel<K,ext>", "hbm", 29024768 + 768),
+    "irpe_k_deit_s_cls": ("rpe_bf16_kernel<K,ext>", "hbm", 29167104 + 1024),
 }
 
 
