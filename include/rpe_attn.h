@@ -146,6 +146,13 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  * for fp32, <= 128 for bf16 (<= 64 with RPE_TERM_Q); with RPE_TABLES_CROSS
  * num_buckets even and (num_buckets / 2)^2 <= 64; N <= 65536. Anything else
  * returns RPE_ERR_UNSUPPORTED.
+ * Device memory: the library allocates, on first use per device and never
+ * frees, a status word and, for bf16 calls on the two-warpgroup kernel whose
+ * last round of (batch, head) work items fills at most half the GPU, a
+ * workspace (grown on demand: the call that grows it synchronizes the device,
+ * so make the first call of a shape outside stream capture) through which two
+ * CTAs merge a split item. Such calls that overlap on one device share the
+ * workspace and must not run concurrently.
  */
 int rpe_attn_fwd(const void *q, const void *k, const void *v,
                  const void *table_q, const void *table_k, const void *table_v,
