@@ -459,3 +459,23 @@ def test_deit_s_cls_config_sampled():
                                     tab_k=inp["tab_k"], slices=sl).reshape(S, cfg.N, 64)[sl]
     got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
     assert _maxerr(got, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("B,heads,H,W,per_head", [
+    (2, 3, 14, 14, False),   # two-warpgroup kernel, 5-row key tiles, 197 tokens
+    (1, 2, 28, 14, False),   # 6-row key tiles, 393 tokens
+    (2, 2, 1, 14, False),    # one grid row: 15 tokens, one query tile
+    (1, 3, 9, 14, True),     # 127 tokens (one query tile), per-head tables
+    (1, 2, 10, 14, True),    # 141 tokens (a pair of query tiles), per-head tables
+])
+def test_cls_token_two_warpgroup_kernel(B, heads, H, W, per_head):
+    # the class key is folded into each row after the grid keys and the class
+    # query reads the class bucket for every key; the hard-to-fake part is the
+    # class key's own term, so the tables are large (std 1)
+    inp, out, ref, ids, K = _cls_case(B, heads, H, W, FLAG_K, "bf16", 1.0, seed=H * 7 + heads,
+                                      per_head=per_head)
+    assert _maxerr(out, ref) <= TOL_BF16
+    tab = inp["tab_k"].clone()
+    tab[..., K - 1, :] = 0
+    without = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K, tab_k=tab)
+    assert np.max(np.abs(without - ref)) > 3 * TOL_BF16

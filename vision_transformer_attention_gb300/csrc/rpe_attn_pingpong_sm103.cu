@@ -108,6 +108,13 @@ struct PPParams {
     uint32_t off_q, off_kv, off_rk, off_qr, qr_stride, off_lut, off_mask, off_stage;
     int lut_len, lut_pad;
     int nvalid_last;  // keys of the last key tile that lie on the grid
+    // Class token (token 0; its pairs take bucket nb - 1): the grid keys are
+    // tokens 1.., the offset table is followed by cls_len bytes of the class
+    // bucket from which the class query reads (its base offset cls_base), and
+    // the class key is folded into each row in the epilogue, its value row
+    // read from v_cls + slice * N * 64.
+    int cls_len, cls_base;
+    const uint16_t *v_cls;
     // Tail split: items [0, whole) run whole, in full rounds over the grid; the
     // `tail` items after them run as two parts on two CTAs, part A over key
     // tiles [0, ka), part B over [ka, nkt), merged by the later part through
@@ -372,17 +379,24 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // place of the contextual key term; HK and BM are not both set. TF, the
 // table form: bit 0, the table (R^K or the bias table) is laid out for the
 // Cross mapping; bit 1, R^K is one table per head; bit 2, the tail items may
-// run split in two parts (see item_at).
+// run split in two parts (see item_at); bit 3, token 0 is a class token (with
+// the key term, W = 14).
 template <int W, int R, bool HK, int NG, bool BM, int TF>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v,
                         const __grid_constant__ CUtensorMap tm_rk,
+                        const __grid_constant__ CUtensorMap tm_kc,
                         const __grid_constant__ CUtensorMap tm_o, const PPParams P) {
     constexpr bool X = (TF & 1) != 0;   // Cross table
     constexpr bool PH = (TF & 2) != 0;  // one R^K per head
     constexpr bool SP = (TF & 4) != 0;  // the tail items may run split
+    constexpr bool CL = (TF & 8) != 0;  // token 0 is a class token
+    // R^K goes with each item (per-head tables, or the class key rows)
+    constexpr bool RK_ITEM = PH || CL;
+    // the item's R^K buffer: 64 table rows, then (CL) the slice's first 16 keys
+    constexpr uint32_t kRkBytes = CL ? 80 * 128 : kTileBytes / 2;
     using G = Geo<W, R>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
@@ -457,6 +471,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             const int id = __ldg(P.lut + e);
             sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
         }
+        if (CL)
+            for (int e = tid; e < P.cls_len; e += kThreads) sLut[P.lut_len + e] = static_cast<uint8_t>(P.nb - 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -471,7 +487,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 prefetch_tmap(&tm_q);
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
-                if (HK && !PH) {
+                if (HK && !RK_ITEM) {
                     // two 32-row boxes: table rows 0.. and rows tab_row2.. (for
                     // Cross tables the column buckets land at row 32)
                     mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
@@ -492,14 +508,16 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     uint8_t *qd = sQ + qb * NG * kTileBytes;
                     // per-head tables travel with the item's Q tiles: the Q buffer's
                     // release (after both groups' last products) frees its table too
-                    constexpr bool tab_item = HK && PH;
+                    constexpr bool tab_item = HK && RK_ITEM;
                     mbar_arrive_expect_tx(&bars.q_full[qb], (I.has_b ? 2 : 1) * kTileBytes +
-                                                                (tab_item ? kTileBytes / 2 : 0));
+                                                                (tab_item ? kRkBytes : 0));
                     if (tab_item) {
-                        uint8_t *rd = sRK + qb * (kTileBytes / 2);
-                        const int head = I.slice % P.heads;
+                        uint8_t *rd = sRK + qb * kRkBytes;
+                        const int head = PH ? I.slice % P.heads : 0;
                         tma_load_3d(rd, &tm_rk, &bars.q_full[qb], 0, 0, head);
                         tma_load_3d(rd + 4096, &tm_rk, &bars.q_full[qb], 0, P.tab_row2, head);
+                        // keys 0..15 of the slice (key 0: the class token) as rows 64..79
+                        if (CL) tma_load_3d(rd + 8192, &tm_kc, &bars.q_full[qb], 0, 0, I.slice);
                     }
                     tma_load_3d(qd, &tm_q, &bars.q_full[qb], 0, I.qt0 * 128, I.slice);
                     if (I.has_b)
@@ -513,14 +531,15 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                             break;
                         uint8_t *kb = sKV + st * 2 * G::KV_BYTES;
                         mbar_arrive_expect_tx(&bars.kv_full[st], 2 * G::KT * 128);
-                        tma_load_3d(kb, &tm_k, &bars.kv_full[st], 0, kt * G::KT, I.slice);
-                        tma_load_3d(kb + G::KV_BYTES, &tm_v, &bars.kv_full[st], 0, kt * G::KT,
-                                    I.slice);
+                        // the grid keys are tokens 1.. when token 0 is a class token
+                        const int k0 = (CL ? 1 : 0) + kt * G::KT;
+                        tma_load_3d(kb, &tm_k, &bars.kv_full[st], 0, k0, I.slice);
+                        tma_load_3d(kb + G::KV_BYTES, &tm_v, &bars.kv_full[st], 0, k0, I.slice);
                         last_use[st] = use;
                     }
                 }
                 // drain: the most recent load on every barrier has landed
-                if (HK && !PH) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
+                if (HK && !RK_ITEM) mbar_wait(&bars.tab_full, 0, drain, kStatusTimeoutDrain, nullptr);
                 for (int b = 0; b < 2; ++b)
                     if (last_q[b] >= 0)
                         mbar_wait(&bars.q_full[b], last_q[b] & 1, drain, kStatusTimeoutDrain, nullptr);
@@ -540,7 +559,9 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             const int w = warp - (4 * NG + 1);
             if (lane == 0) {
                 constexpr uint32_t kIdS = idesc_bf16(128, G::NS, false, false);
-                constexpr uint32_t kIdQR = idesc_bf16(128, 64, false, false);
+                // QR' = Q R^K^T: 64 bucket columns, and (CL) 16 more against the
+                // slice's first keys, of which column 64 is q . k_class
+                constexpr uint32_t kIdQR = idesc_bf16(128, CL ? 80 : 64, false, false);
                 constexpr uint32_t kIdO = idesc_bf16(128, 64, false, true);
                 const uint64_t hi128 = smem_desc(0, 16, 1024, kSwizzle128B);
                 const uint32_t tG = tmem + w * 256;
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 uint32_t u = 0;  // units issued
                 int ci = 0;      // items whose last P V was issued
                 bool ok = true;
-                if (HK && !PH) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+                if (HK && !RK_ITEM) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
                 // consume the oldest outstanding unit: wait until the group has
                 // released it, then issue its P V
                 auto consume = [&]() {
@@ -611,7 +632,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         uint32_t code;
                         if (kt < I.kt0) {  // the QR' unit
                             tc_fence_after();
-                            const uint32_t rk_off = PH ? qb * (kTileBytes / 2) : 0;
+                            const uint32_t rk_off = RK_ITEM ? qb * kRkBytes : 0;
                             const uint64_t dRK = hi128 | (smem_u32(sRK + rk_off) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -683,7 +704,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         // the item's last P V.
         bool ok = true, due = false;
         Item D{};
-        float due_m = 0.f, due_l = 1.f;
+        float due_m = 0.f, due_l = 1.f, due_xc = -INFINITY;
         auto epilogue = [&]() -> bool {
             const bool okd = ok && __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc,
                                                             kStatusTimeoutMma, &abort_flag));
@@ -696,6 +717,17 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             const int di = dqt * 128 + t;
             const bool dactive = dqt * 128 + lq * 32 < P.N;
             float inv = 1.f / due_l;
+            // CL: fold the class key into the row: reference max mm, O and l
+            // scaled by 2^(m - mm), the key's weight 2^(x_c - mm) times v_class
+            float o_scale = 1.f, p_cls = 0.f;
+            const uint4 *v_cls = nullptr;
+            if (CL && dactive) {
+                const float mm = fmaxf(due_m, due_xc);
+                o_scale = ex2_approx(due_m - mm);
+                p_cls = ex2_approx(due_xc - mm);
+                inv = 1.f / (due_l * o_scale + p_cls);
+                v_cls = reinterpret_cast<const uint4 *>(P.v_cls + static_cast<size_t>(D.slice) * P.N * 64);
+            }
             // A part of a split tail item hands its unnormalised state (O, m, l)
             // to the workspace and counts its arrival; the later of the two
             // parts merges the other's state into its own and writes the
@@ -754,6 +786,17 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                             o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), a_self) +
                                                    __fmul_rn(__ldcg(other + (16 * c2 + e) * 128 + t), a_other));
                     }
+                    if (CL) {
+                        // 16 bf16 of v_class (the same row for every thread: broadcast)
+                        const uint4 va = __ldg(v_cls + 2 * c2), vb = __ldg(v_cls + 2 * c2 + 1);
+                        const uint32_t vw[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const uint32_t w = vw[e >> 1];
+                            const float ve = __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+                            o[e] = __float_as_uint(fmaf(__uint_as_float(o[e]), o_scale, p_cls * ve));
+                        }
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
@@ -785,7 +828,11 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             const int i = qt * 128 + t;
             const bool warp_active = qt * 128 + lq * 32 < P.N;
             const int ic = i < P.N ? i : P.N - 1;
-            const int base_i = (ic / W) * G::COLS + (ic % W) + (P.H - 1) * G::COLS + (W - 1);
+            // the row's grid position (CL: token t >= 1 is grid token t - 1); the
+            // class query reads the class-bucket region after the offset table
+            const int pi = CL ? ic - 1 : ic;
+            const int base_i = pi < 0 ? P.cls_base
+                                      : (pi / W) * G::COLS + (pi % W) + (P.H - 1) * G::COLS + (W - 1);
             uint32_t slot = u % G::SLOTS;
             if (HK)
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
@@ -807,15 +854,18 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 }
                 named_bar_sync(group_bar, 128);
             }
+            float xc = -INFINITY;  // CL: the class key's logit for this row
             if (HK) {
                 tc_fence_after();
                 if (warp_active) {
-                    uint32_t r0[32], r1[32];
+                    uint32_t r0[32], r1[32], rk[16];
                     tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off, r0);
                     tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32, r1);
+                    if (CL) tmem_ld16(tG + kColSlot0 + slot * G::NS + lane_off + 64, rk);
                     tmem_ld_wait();
                     tmem_ready(r0);
                     tmem_ready(r1);
+                    if (CL) tmem_ready(rk);
                     if constexpr (X) {
                         // joint id a*span + b: row bucket a (column a) plus column
                         // bucket span + b (staged at table row 32 + b)
@@ -830,6 +880,9 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
 #pragma unroll
                         for (int b = 0; b < 64; ++b)
                             if (b < P.nb) qr_t[b * 128] = __uint_as_float(b < 32 ? r0[b] : r1[b - 32]) * P.c;
+                        // the class key: q . k_class plus the class bucket's term,
+                        // both inside the scaling (eq. 13)
+                        if (CL) xc = __uint_as_float(rk[0]) * P.c + qr_t[(P.nb - 1) * 128];
                     }
                 }
                 tc_fence_before();
@@ -871,6 +924,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             due = true;
             D = I;
             due_m = m;
+            due_xc = xc;
             due_l = l;
         }
         if (due) epilogue();
@@ -891,7 +945,9 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     using G = Geo<W, R>;
     using L = Layout<NG>;
     PPParams p{};
-    const int N = a.H * a.W;
+    constexpr bool CL = (TF & 8) != 0;
+    constexpr uint32_t kRkBytes = CL ? 80 * 128 : kTileBytes / 2;
+    const int N = a.H * a.W + (CL ? 1 : 0);  // tokens (token 0: the class token)
     p.N = N;
     p.H = a.H;
     p.cross = a.cross_span;
@@ -907,7 +963,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
                       : p.slices * p.pairs_full + ((p.qtiles & 1) ? p.slices : 0);
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
     p.lut_pad = static_cast<int>(align_up(G::R * G::COLS + 4, 16));
-    p.nvalid_last = N - (p.nkt - 1) * G::KT;
+    p.nvalid_last = a.H * a.W - (p.nkt - 1) * G::KT;  // grid keys of the last tile
+    // class-bucket region: the class query's offset reads reach back nkt R COLS
+    // bytes from cls_base and forward less than W + 16
+    p.cls_base = CL ? p.lut_len + 32 + p.nkt * G::R * G::COLS : 0;
+    p.cls_len = CL ? 32 + p.nkt * G::R * G::COLS + W + 48 : 0;
+    p.v_cls = static_cast<const uint16_t *>(a.v);
     p.lut = a.lut;
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
     p.bias = a.bias;
@@ -924,7 +985,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_q = off;
         off += nq * NG * kTileBytes;
         p.off_rk = off;
-        if (HK) off += (a.tab_heads > 1 ? nq : 1) * (kTileBytes / 2);
+        if (HK) off += ((a.tab_heads > 1 || CL) ? nq : 1) * kRkBytes;
         p.off_qr = off;
         // each group's QR' table (or bias row)
         p.qr_stride = align_up(std::max(HK ? p.nb * 512 : 0, BM ? 512 : 0), 1024);
@@ -935,7 +996,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_mask = off;
         off += 2 * 4096;
         p.off_lut = off;
-        if (HK || BM) off += p.lut_pad + align_up(p.lut_len, 16) + 16;
+        if (HK || BM) off += p.lut_pad + align_up(p.lut_len + p.cls_len, 16) + 16;
         off = align_up(off, 1024);
         p.off_kv = off;
         const int room = static_cast<int>((cap - std::min(cap, 1024 + off)) / (2 * G::KV_BYTES));
@@ -960,10 +1021,12 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     const uint32_t tbox[3] = {kD, 32, 1};
     const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-    CUtensorMap tq, tk, tv, trk, to;
+    CUtensorMap tq, tk, tv, trk, to, tkc;
+    const uint32_t box_kc[3] = {kD, 16, 1};  // the slice's first 16 keys (class token first)
     if (!encode_tensor_map(&tq, bf, 3, a.q, dims, strides, box, sw) ||
         !encode_tensor_map(&to, bf, 3, a.out, dims, strides, box, sw) ||
         !encode_tensor_map(&tk, bf, 3, a.k, dims, strides, box_kv, sw) ||
+        !encode_tensor_map(&tkc, bf, 3, a.k, dims, strides, box_kc, sw) ||
         !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box_kv, sw) ||
         !encode_tensor_map(&trk, bf, 3, HK ? a.tab_k : a.q, tdims, tstrides, tbox, sw))
         return cudaErrorInvalidValue;
@@ -995,7 +1058,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         }
     }
     return launch_pdl(rpe_pingpong_kernel<W, R, HK, NG, BM, TF>, dim3(grid), dim3(L::kThreads), total, stream,
-                      tq, tk, tv, trk, to, p);
+                      tq, tk, tv, trk, tkc, to, p);
 }
 
 }  // namespace
@@ -1019,6 +1082,10 @@ cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, boo
     if (bm) return (tf & 1) ? launch_pp<W, R, false, NG, true, 1>(a, stream)
                  : sp       ? launch_pp<W, R, false, NG, true, 4>(a, stream)
                             : launch_pp<W, R, false, NG, true, 0>(a, stream);
+    if constexpr (W == 14) {
+        if (a.cls) return (tf & 2) ? launch_pp<W, R, true, NG, false, 10>(a, stream)
+                                   : launch_pp<W, R, true, NG, false, 8>(a, stream);
+    }
     if (hk) {
         switch (tf) {
             case 0: return sp ? launch_pp<W, R, true, NG, false, 4>(a, stream)
@@ -1035,10 +1102,13 @@ cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, boo
 }  // namespace
 
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err) {
-    if (a.d != kD || (a.terms & ~1u) != 0 || a.cls) return false;  // key tiles are whole grid rows
+    if (a.d != kD || (a.terms & ~1u) != 0) return false;
     const bool hk = (a.terms & 1u) != 0;
     const bool bm = a.bias != nullptr;
     if (hk && bm) return false;
+    // a class token: key term, shared or per-head (not Cross) tables, W = 14,
+    // whose score slots hold the 80 columns of the widened QR' product
+    if (a.cls && (!hk || a.cross_span > 0 || a.W != 14)) return false;
     // the QR' product and copy cover 64 buckets; a bias row, one per thread, 128
     if ((hk && a.num_buckets > 64) || (bm && a.num_buckets > 128)) return false;
     if (a.W == 14)
