@@ -83,7 +83,7 @@ DOMINANT = {
     "irpe_k_deit_s": ("rpe_pingpong_kernel<14,5,K>", "hbm", 29005568 + 0),
     "irpe_qkv_deit_s": ("rpe_bf16_kernel<K,Q,V>", "hbm", 29142272 + 2304),
     "irpe_k_56x56": ("rpe_pingpong_kernel<56,1,K,split>", "tensor", 58197504 + 2228736),
-    "irpe_k_r2_deit_s": ("rpe_bf16_kernel<K,ext>", "hbm", 29024768 + 768),
+    "irpe_k_r2_deit_s": ("rpe_pingpong_kernel<14,5,K,128 buckets>", "hbm", None),
     "irpe_k_deit_s_cls": ("rpe_pingpong_kernel<14,5,K,cls>", "hbm", None),
 }
 

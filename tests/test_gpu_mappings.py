@@ -479,3 +479,25 @@ def test_cls_token_two_warpgroup_kernel(B, heads, H, W, per_head):
     tab[..., K - 1, :] = 0
     without = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K, tab_k=tab)
     assert np.max(np.abs(without - ref)) > 3 * TOL_BF16
+
+
+@pytest.mark.parametrize("B,heads,H,W,sampled", [
+    (1, 3, 28, 14, False),   # two-warpgroup kernel, 6-row key tiles, two QR' rounds
+    (2, 2, 1, 14, False),    # one grid row
+    (1, 3, 56, 56, True),    # W = 56
+])
+def test_r2_81_buckets_two_warpgroup_kernel(B, heads, H, W, sampled):
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R20)
+    inp = workloads.irpe_inputs(B, heads, H * W, 64, nb, FLAG_K, "bf16", table_std=1.0, seed=H + W + 61)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, FLAG_K, table_k=g["tab_k"])
+    ids, K = oracle.product_bucket_ids(H, W, *R20)
+    N, S = H * W, B * heads
+    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(N - 40, N)])) if sampled else None
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, FLAG_K,
+                                    tab_k=inp["tab_k"], rows=rows)
+    if sampled:
+        idx = torch.as_tensor(rows, device=out.device)
+        assert _maxerr(out.reshape(S, N, 64)[:, idx], ref.reshape(S, N, 64)[:, rows]) <= TOL_BF16
+    else:
+        assert _maxerr(out, ref) <= TOL_BF16

@@ -380,7 +380,7 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // table form: bit 0, the table (R^K or the bias table) is laid out for the
 // Cross mapping; bit 1, R^K is one table per head; bit 2, the tail items may
 // run split in two parts (see item_at); bit 3, token 0 is a class token (with
-// the key term, W = 14).
+// the key term, W = 14); bit 4, 65..128 buckets (the QR' product in two rounds).
 template <int W, int R, bool HK, int NG, bool BM, int TF>
 __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     rpe_pingpong_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -393,10 +393,13 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     constexpr bool PH = (TF & 2) != 0;  // one R^K per head
     constexpr bool SP = (TF & 4) != 0;  // the tail items may run split
     constexpr bool CL = (TF & 8) != 0;  // token 0 is a class token
+    // 65..128 buckets: QR' in two rounds of 64 buckets (shared R^K of 128 rows)
+    constexpr int NQR = (TF & 16) != 0 ? 2 : 1;
     // R^K goes with each item (per-head tables, or the class key rows)
     constexpr bool RK_ITEM = PH || CL;
-    // the item's R^K buffer: 64 table rows, then (CL) the slice's first 16 keys
-    constexpr uint32_t kRkBytes = CL ? 80 * 128 : kTileBytes / 2;
+    // the R^K buffer: 64 table rows, then (CL) the slice's first 16 keys; or
+    // 128 table rows
+    constexpr uint32_t kRkBytes = CL ? 80 * 128 : NQR * (kTileBytes / 2);
     using G = Geo<W, R>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
@@ -488,11 +491,15 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 prefetch_tmap(&tm_k);
                 prefetch_tmap(&tm_v);
                 if (HK && !RK_ITEM) {
-                    // two 32-row boxes: table rows 0.. and rows tab_row2.. (for
-                    // Cross tables the column buckets land at row 32)
-                    mbar_arrive_expect_tx(&bars.tab_full, kTileBytes / 2);
+                    // 32-row boxes: table rows 0.. and rows tab_row2.. (for Cross
+                    // tables the column buckets land at row 32), then 64.. and 96..
+                    mbar_arrive_expect_tx(&bars.tab_full, kRkBytes);
                     tma_load_3d(sRK, &tm_rk, &bars.tab_full, 0, 0, 0);
                     tma_load_3d(sRK + 4096, &tm_rk, &bars.tab_full, 0, P.tab_row2, 0);
+                    if (NQR == 2) {
+                        tma_load_3d(sRK + 8192, &tm_rk, &bars.tab_full, 0, 64, 0);
+                        tma_load_3d(sRK + 12288, &tm_rk, &bars.tab_full, 0, 96, 0);
+                    }
                 }
                 int g = 0, it = 0;
                 int last_q[2] = {-1, -1};
@@ -624,15 +631,16 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         continue;
                     }
                     const uint64_t dQ = hi128 | ((aQ + qb * NG * kTileBytes) >> 4);
-                    for (int kt = HK ? I.kt0 - 1 : I.kt0; ok && kt < I.kt1; ++kt) {
+                    for (int kt = HK ? I.kt0 - NQR : I.kt0; ok && kt < I.kt1; ++kt) {
                         if (np == G::SLOTS) consume();
                         if (!ok) break;
                         const uint32_t slot = u % G::SLOTS;
                         const uint32_t dS = tG + kColSlot0 + slot * G::NS;
                         uint32_t code;
-                        if (kt < I.kt0) {  // the QR' unit
+                        if (kt < I.kt0) {  // a QR' unit (round kt - kt0 + NQR)
                             tc_fence_after();
-                            const uint32_t rk_off = RK_ITEM ? qb * kRkBytes : 0;
+                            const uint32_t rk_off = (RK_ITEM ? qb * kRkBytes : 0) +
+                                                    (kt - I.kt0 + NQR) * (kTileBytes / 2);
                             const uint64_t dRK = hi128 | (smem_u32(sRK + rk_off) >> 4);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
@@ -888,6 +896,30 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 tc_fence_before();
                 mbar_arrive(&bars.slot_done[wg][slot]);
                 ++u;
+                // the second QR' round: buckets 64.. into rows 64.. of the table
+                if (NQR == 2) {
+                    slot = u % G::SLOTS;
+                    ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
+                                                   kStatusTimeoutMma, &abort_flag)) && ok;
+                    if (ok) {
+                        tc_fence_after();
+                        if (warp_active) {
+                            uint32_t r0[32], r1[32];
+                            tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off, r0);
+                            tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32, r1);
+                            tmem_ld_wait();
+                            tmem_ready(r0);
+                            tmem_ready(r1);
+#pragma unroll
+                            for (int b = 0; b < 64; ++b)
+                                if (64 + b < P.nb)
+                                    qr_t[(64 + b) * 128] = __uint_as_float(b < 32 ? r0[b] : r1[b - 32]) * P.c;
+                        }
+                        tc_fence_before();
+                        mbar_arrive(&bars.slot_done[wg][slot]);
+                        ++u;
+                    }
+                }
             }
             if (due && !epilogue()) {
                 ok = false;
@@ -946,7 +978,8 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
     using L = Layout<NG>;
     PPParams p{};
     constexpr bool CL = (TF & 8) != 0;
-    constexpr uint32_t kRkBytes = CL ? 80 * 128 : kTileBytes / 2;
+    constexpr int NQR = (TF & 16) != 0 ? 2 : 1;
+    constexpr uint32_t kRkBytes = CL ? 80 * 128 : NQR * (kTileBytes / 2);
     const int N = a.H * a.W + (CL ? 1 : 0);  // tokens (token 0: the class token)
     p.N = N;
     p.H = a.H;
@@ -1086,6 +1119,7 @@ cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, boo
         if (a.cls) return (tf & 2) ? launch_pp<W, R, true, NG, false, 10>(a, stream)
                                    : launch_pp<W, R, true, NG, false, 8>(a, stream);
     }
+    if (hk && a.num_buckets > 64) return launch_pp<W, R, true, NG, false, 16>(a, stream);
     if (hk) {
         switch (tf) {
             case 0: return sp ? launch_pp<W, R, true, NG, false, 4>(a, stream)
@@ -1109,8 +1143,10 @@ bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaErr
     // a class token: key term, shared or per-head (not Cross) tables, W = 14,
     // whose score slots hold the 80 columns of the widened QR' product
     if (a.cls && (!hk || a.cross_span > 0 || a.W != 14)) return false;
-    // the QR' product and copy cover 64 buckets; a bias row, one per thread, 128
-    if ((hk && a.num_buckets > 64) || (bm && a.num_buckets > 128)) return false;
+    // the QR' product and copy cover 64 buckets, or 128 in two rounds with one
+    // shared, non-Cross table and no class token; a bias row, one per thread, 128
+    const bool hk128 = a.cross_span == 0 && a.tab_heads == 1 && !a.cls;
+    if ((hk && a.num_buckets > (hk128 ? 128 : 64)) || (bm && a.num_buckets > 128)) return false;
     if (a.W == 14)
         // key tiles of 5 or 6 grid rows (70 or 84 keys in 80 or 96 score
         // columns), whichever leaves fewer score columns per query row
