@@ -251,11 +251,14 @@ def replay_timed(graphs, barrier):
 
 def e2e_run(cfg, dev, steps, barrier):
     """Same metric through the public API with pinned host buffers: every step
-    copies its inputs host->device, runs the path and reads the result back."""
+    copies its inputs host->device, runs the path and reads the result back.
+    The steps are pipelined over three streams (uploads, compute, downloads)
+    with two device buffer sets, so step i + 1's inputs go up while step i runs
+    and step i - 1's result comes down; each step still moves its own bytes."""
     from vision_transformer_attention_gb300 import api, workloads
     base = workloads.config_inputs(cfg)
     host = {k: t.pin_memory() for k, t in base.items() if t is not None and k in ("q", "k", "v")}
-    dq = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    dq = [{k: torch.empty_like(t, device=dev) for k, t in host.items()} for _ in range(2)]
     tabs = {k: (None if base.get(k) is None else base[k].to(dev))
             for k in ("tab_q", "tab_k", "tab_v", "table")}
     out_host = torch.empty_like(base["q"]).pin_memory()
@@ -263,34 +266,55 @@ def e2e_run(cfg, dev, steps, barrier):
     if isinstance(cfg, workloads.IrpeConfig):
         a, b, g = workloads.index_constants(cfg.ratio)
         lut, _, _ = api.rpe_build_bucket_ids(cfg.H, cfg.W, a, b, g, device=dev)
-    out = torch.empty_like(dq["q"])
+    outs = [torch.empty_like(dq[0]["q"]) for _ in range(2)]
+    s_in, s_run, s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    uploaded, computed, downloaded = ([ev() for _ in range(2)] for _ in range(3))
+    used = [False, False]
 
-    def one():
-        for k in ("q", "k", "v"):
-            dq[k].copy_(host[k], non_blocking=True)
-        if lut is not None:
-            api.rpe_attn_fwd(dq["q"], dq["k"], dq["v"], lut, cfg.num_buckets, cfg.H, cfg.W,
-                             cfg.flags, cls_token=cfg.cls, table_q=tabs["tab_q"], table_k=tabs["tab_k"],
-                             table_v=tabs["tab_v"], out=out)
-        else:
-            if cfg.fmap:
-                api.swin_window_attn_fwd_fmap(dq["q"], dq["k"], dq["v"], tabs["table"], cfg.M,
-                                              out=out)
+    def one(i):
+        j = i % 2
+        with torch.cuda.stream(s_in):
+            if used[j]:
+                s_in.wait_event(computed[j])   # step i - 2 has read this input set
+            for k in ("q", "k", "v"):
+                dq[j][k].copy_(host[k], non_blocking=True)
+            uploaded[j].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(uploaded[j])
+            if used[j]:
+                s_run.wait_event(downloaded[j])  # step i - 2's result has left this buffer
+            x = dq[j]
+            if lut is not None:
+                api.rpe_attn_fwd(x["q"], x["k"], x["v"], lut, cfg.num_buckets, cfg.H, cfg.W,
+                                 cfg.flags, cls_token=cfg.cls, table_q=tabs["tab_q"],
+                                 table_k=tabs["tab_k"], table_v=tabs["tab_v"], out=outs[j])
+            elif cfg.fmap:
+                api.swin_window_attn_fwd_fmap(x["q"], x["k"], x["v"], tabs["table"], cfg.M,
+                                              out=outs[j])
             else:
-                api.swin_window_attn_fwd(dq["q"], dq["k"], dq["v"], tabs["table"], cfg.M, out=out)
-        out_host.copy_(out, non_blocking=True)
+                api.swin_window_attn_fwd(x["q"], x["k"], x["v"], tabs["table"], cfg.M, out=outs[j])
+            computed[j].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(computed[j])
+            out_host.copy_(outs[j], non_blocking=True)
+            downloaded[j].record(s_out)
+        used[j] = True
 
-    for _ in range(3):
-        one()
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
-    stream = torch.cuda.current_stream()
+    main = torch.cuda.current_stream()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
-    start.record(stream)
-    for _ in range(steps):
-        one()
-    end.record(stream)
+    start.record(main)
+    for st in (s_in, s_run, s_out):
+        st.wait_event(start)
+    for i in range(steps):
+        one(3 + i)
+    main.wait_stream(s_out)
+    end.record(main)
     torch.cuda.synchronize()
     barrier()
     ms = start.elapsed_time(end)
@@ -423,7 +447,8 @@ def gpu_arm(args):
         "roofline": roofline_of(cfg, flops, nbytes, per_step_s, peaks, peak_src),
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "pipeline": "uploads, compute and downloads on three streams, two device buffer sets"},
         "gpu_launches": args.steps,
         "configs_extra": extra_cfgs,
     }
