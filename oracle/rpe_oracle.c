@@ -21,7 +21,7 @@
  *           embedding table section (clip and shift to [0, 2k]) and the
  *           score / output sections (per-pair double loop).
  *
- * Readings taken where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *   - offsets are query minus key in 2D (the SWIN2D worked example: patch
  *     (0,0) attending (2,2) gives (-2,-2));
  *   - the row offset is the major index of a Product id and of a Swin index;

@@ -1,6 +1,6 @@
 """GPU parity: the CUDA library, called through its C ABI, against the oracle.
 
-Tolerances (written here, derived in the design doc): bucket ids bit-exact;
+Tolerances: bucket ids bit-exact (integer work);
 bf16 attention <= 2e-2 max abs error (bf16 inputs, fp32 accumulation,
 probabilities rounded to bf16 before the value products); fp32 attention
 <= 1e-4 max abs error.
