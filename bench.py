@@ -358,6 +358,27 @@ def cpu_baseline(cfg, budget_s=12.0):
             "seconds": round(dt, 3)}
 
 
+def rank_helpers(dist, dev):
+    """Replica coordination: a barrier, and the maximum of a per-rank float over
+    all ranks (the slowest replica's time). No-ops for a single process."""
+    barrier = (lambda: dist.barrier()) if dist else (lambda: None)
+
+    def max_over_ranks(x):
+        if not dist:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    return barrier, max_over_ranks
+
+
+def job_throughput(world, units_per_rank, seconds_per_step):
+    """Whole-job units/s: every rank processes its own units (weak scaling) in
+    the slowest rank's time."""
+    return world * units_per_rank / seconds_per_step
+
+
 def gpu_arm(args):
     from vision_transformer_attention_gb300 import workloads
     import __graft_entry__
@@ -371,14 +392,7 @@ def gpu_arm(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    barrier = (lambda: dist.barrier()) if dist else (lambda: None)
-
-    def max_over_ranks(x):
-        if not dist:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    barrier, max_over_ranks = rank_helpers(dist, dev)
 
     peaks, peak_src = load_peaks()
     cfg = workloads.CONFIGS[args.workload]
@@ -396,13 +410,13 @@ def gpu_arm(args):
     ms = max_over_ranks(ms)
     clocks = clk.summary()
     per_step_s = ms / 1e3 / args.steps
-    value = world * tokens / per_step_s
+    value = job_throughput(world, tokens, per_step_s)
     achieved_tflops = flops / per_step_s / 1e12
     del graphs
 
     e2e_ms, h2d, d2h = e2e_run(cfg, dev, args.e2e_steps, barrier)
     e2e_ms = max_over_ranks(e2e_ms)
-    e2e_value = world * tokens / (e2e_ms / 1e3 / args.e2e_steps)
+    e2e_value = job_throughput(world, tokens, e2e_ms / 1e3 / args.e2e_steps)
 
     extra_cfgs = {}
     if not args.headline_only:
@@ -419,7 +433,7 @@ def gpu_arm(args):
             del gr
             bound_tc = name == "irpe_k_56x56"
             extra_cfgs[name] = {
-                "tokens_per_s": world * tk / t, "ms_per_step": t * 1e3,
+                "tokens_per_s": job_throughput(world, tk, t), "ms_per_step": t * 1e3,
                 "tflops": f / t / 1e12, "gbs": b / t / 1e9,
                 "tc_frac": f / t / 1e12 / peaks["bf16_tflops"],
                 "hbm_frac": b / t / 1e9 / peaks["hbm_gbs"],
