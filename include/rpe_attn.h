@@ -25,8 +25,9 @@
  *   - Every wait inside a kernel is bounded (2 s of GPU time). A wait that
  *     runs out sets a bit in a per-device status word and the kernel returns
  *     early, leaving its output undefined; rpe_device_status() reads the word.
- *     The word is the library's only device allocation (256 bytes per
- *     device, made on the first call on that device).
+ *     The word (256 bytes per device, made on the first call on that device)
+ *     and the split-tail workspaces described at rpe_attn_fwd are the
+ *     library's only device allocations.
  *   - There is no CPU fallback: without a usable sm_103 GPU the calls
  *     return RPE_ERR_CUDA.
  */
@@ -133,9 +134,22 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                heads, or [heads, num_buckets, d] with RPE_TABLES_PER_HEAD;
  *                NULL for a term whose bit is not set in `terms` (a table
  *                whose bit is off is not read).
- * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids (or
- *                any table of ids indexed the same way; an id outside
- *                [0, num_buckets) is clamped into that range).
+ * bucket_lut   : device int32 [(2H-1) * (2W-1)] from rpe_build_bucket_ids, or
+ *                any table of ids indexed the same way. Every id must lie in
+ *                [0, num_buckets) ([0, num_buckets - 1) with RPE_CLS_TOKEN,
+ *                whose last bucket is the class token's; [0, span^2) for
+ *                Cross tables). A table rpe_build_bucket_ids wrote is known
+ *                to satisfy this; any other table is read back and checked on
+ *                its first use with this grid (a synchronous copy of its
+ *                (2H-1)(2W-1) ids on `stream`; RPE_ERR_UNSUPPORTED if `stream`
+ *                is being captured, so make that first call outside a
+ *                capture) and an id out of range returns RPE_ERR_INVALID_ARG
+ *                before any launch. The check is remembered per device
+ *                address: a table rewritten in place by other means after
+ *                its check is caught by the kernel instead, which sets a
+ *                status bit that rpe_device_status reports as
+ *                RPE_ERR_INVALID_ARG (the id is clamped meanwhile, so no read
+ *                leaves the tables).
  * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention),
  *                plus RPE_TABLES_CROSS for tables of the Cross mapping,
  *                RPE_TABLES_PER_HEAD for one table per head and RPE_CLS_TOKEN
@@ -148,11 +162,15 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  * returns RPE_ERR_UNSUPPORTED.
  * Device memory: the library allocates, on first use per device and never
  * frees, a status word and, for bf16 calls on the two-warpgroup kernel whose
- * last round of (batch, head) work items fills at most half the GPU, a
- * workspace (grown on demand: the call that grows it synchronizes the device,
- * so make the first call of a shape outside stream capture) through which two
- * CTAs merge a split item. Such calls that overlap on one device share the
- * workspace and must not run concurrently.
+ * last round of (batch, head) work items fills at most half the GPU, one
+ * workspace per stream (about 10 MB with 152 SMs, sized once for the largest
+ * tail, never grown) through which two CTAs merge a split item. Calls on
+ * different streams never share a workspace, so overlapping calls are safe; a
+ * CUDA graph captured on a stream uses that stream's workspace, so two
+ * replays of such graphs must not overlap one another or a call on that
+ * stream. A stream's first split call allocates; under stream capture,
+ * where no allocation is made, a stream without a workspace runs every item
+ * whole (same result, a little slower).
  */
 int rpe_attn_fwd(const void *q, const void *k, const void *v,
                  const void *table_q, const void *table_k, const void *table_v,
@@ -229,11 +247,30 @@ int swin_window_attn_fwd(const void *q, const void *k, const void *v,
  *   - All calls share the array, so calls that overlap on the GPU (different
  *     streams, no ordering between them) race on the status word.
  *   - A bounded-wait timeout inside this variant sets a bit in its own word,
- *     not in the word rpe_device_status reads.
+ *     not in the word rpe_device_status reads: swin_noalloc_status reads it.
  */
 int swin_window_attn_fwd_noalloc(const void *q, const void *k, const void *v,
                                  const float *bias_table, int num_windows, int heads,
                                  int M, int d, void *out, void *stream);
+
+/*
+ * swin_noalloc_status -- the status word of swin_window_attn_fwd_noalloc on
+ * the current device (no counterpart on the pages; the same bits as
+ * rpe_device_status). Synchronises the device, copies the word out of the
+ * fixed array (cudaMemcpyFromSymbol, no allocation) into *status and, when
+ * `clear` is non-zero, writes 0 back. Returns RPE_ERR_TIMEOUT if any bit was
+ * set, RPE_ERR_CUDA if a CUDA call failed, else RPE_OK.
+ */
+int swin_noalloc_status(unsigned *status, int clear);
+
+/*
+ * swin_noalloc_status_word -- the device address of that status word on the
+ * current device (a 4-byte unsigned inside the fixed array), for callers that
+ * read or clear it with their own stream-ordered copies instead of the
+ * synchronising swin_noalloc_status. No allocation; the address stays valid
+ * until the process exits.
+ */
+int swin_noalloc_status_word(unsigned **word);
 
 /*
  * swin_window_attn_fwd_fmap -- swin_window_attn_fwd with the window partition
@@ -260,9 +297,11 @@ int swin_window_attn_fwd_fmap(const void *q, const void *k, const void *v,
 
 /*
  * rpe_device_status -- synchronises the current device and returns, through
- * *status, the word the kernels set when a bounded wait ran out (0 = none).
- * Clears the word when `clear` is non-zero. Returns RPE_ERR_TIMEOUT if any
- * bit was set, RPE_ERR_CUDA if synchronising failed, else RPE_OK.
+ * *status, the word the kernels set when a bounded wait ran out (bits 0-4)
+ * or an offset table held an id out of range (bit 5); 0 = none. Clears the
+ * word when `clear` is non-zero. Returns RPE_ERR_TIMEOUT if a wait ran out,
+ * else RPE_ERR_INVALID_ARG if a table was bad, RPE_ERR_CUDA if synchronising
+ * failed, else RPE_OK.
  */
 int rpe_device_status(unsigned *status, int clear);
 

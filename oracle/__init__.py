@@ -20,6 +20,7 @@ Every function is pinned by ``tests/test_oracle_pins.py``; none is
 """
 from __future__ import annotations
 
+import concurrent.futures
 import ctypes
 import os
 import subprocess
@@ -109,6 +110,31 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _out_like(q, out):
+    if out is None:
+        return np.zeros_like(q)
+    assert out.dtype == np.float64 and out.shape == q.shape and out.flags.c_contiguous
+    return out
+
+
+def parallel_slices(run, slices, threads=None):
+    """Calls run(part) on disjoint parts of the slice list from `threads`
+    threads (default: every host core). The C calls release the GIL, so the
+    parts run in parallel; each call writes only its own slices of a shared
+    output. Returns the number of threads used."""
+    _load()  # once, before any thread calls in
+    slices = np.asarray(slices, dtype=np.int32)
+    threads = max(1, min(threads or os.cpu_count() or 1, len(slices)))
+    parts = [p for p in np.array_split(slices, threads) if len(p)]
+    if len(parts) == 1:
+        run(parts[0])
+        return 1
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(parts)) as ex:
+        for f in [ex.submit(run, p) for p in parts]:
+            f.result()
+    return len(parts)
+
+
 def _check(status):
     if status != 0:
         raise ValueError(f"oracle call failed with status {status}")
@@ -166,12 +192,13 @@ def clip_product_bucket_ids(H: int, W: int, k: int):
 
 
 def irpe_attention_ids(q, k, v, ids, num_buckets, flags=0, tab_q=None, tab_k=None,
-                       tab_v=None, bias_in=None, slices=None, rows=None, ids2=None):
+                       tab_v=None, bias_in=None, slices=None, rows=None, ids2=None, out=None):
     """iRPE attention on [B, heads, N, d] with a given [N, N] id map; bias_in is a
     bias-mode table [num_buckets, bias_heads] (bias_heads 1 = shared by all heads);
     ids2, a second [N, N] map whose entries are added (the Cross mapping).
     Contextual tables are [num_buckets, d] (shared by every head) or
-    [heads, num_buckets, d] (one per head)."""
+    [heads, num_buckets, d] (one per head). ``out`` (float64, q's shape) receives
+    the picked slices and is returned; by default a zeroed array."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, heads, N, d = q.shape
     ids = _i32(ids)
@@ -187,7 +214,7 @@ def irpe_attention_ids(q, k, v, ids, num_buckets, flags=0, tab_q=None, tab_k=Non
     bias_in = _f64(bias_in)
     bias_heads = 0 if bias_in is None else (1 if bias_in.ndim == 1 else bias_in.shape[1])
     slices, rows = _i32(slices), _i32(rows)
-    out = np.zeros_like(q)
+    out = _out_like(q, out)
     _check(_load().orc_irpe_attention_ids(
         B, heads, N, d, _ptr(ids), _ptr(ids2), num_buckets, flags, _ptr(q), _ptr(k), _ptr(v),
         _ptr(tab_q), _ptr(tab_k), _ptr(tab_v), tab_heads, _ptr(bias_in), bias_heads,
@@ -271,16 +298,16 @@ def irpe_attention(q, k, v, H, W, alpha, beta, gamma, flags,
     return out
 
 
-def swin_attention(q, k, v, table, M, slices=None):
+def swin_attention(q, k, v, table, M, slices=None, out=None):
     """Swin window attention on [num_windows, heads, M*M, d] with a
-    [(2M-1)^2, heads] bias table."""
+    [(2M-1)^2, heads] bias table (``out`` as for irpe_attention_ids)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     nw, heads, n, d = q.shape
     assert n == M * M
     table = _f64(table)
     assert table.shape == ((2 * M - 1) ** 2, heads)
     slices = _i32(slices)
-    out = np.zeros_like(q)
+    out = _out_like(q, out)
     _check(_load().orc_swin_attention(nw, heads, M, d, _ptr(q), _ptr(k), _ptr(v),
                                       _ptr(table), 0 if slices is None else len(slices),
                                       _ptr(slices), _ptr(out)))

@@ -76,16 +76,23 @@ def test_swin_bf16_small(nw, heads, d, table_std):
     assert _maxerr(out, ref) <= TOL_BF16
 
 
-def test_swin_bf16_swin_t_stage1_sampled():
+def _swin_ref_threads(inp, M):
+    """The oracle on every (window, head) unit, the units split over host cores."""
+    f64 = {k: oracle._f64(t) for k, t in inp.items()}
+    out = np.zeros_like(f64["q"])
+    units = f64["q"].shape[0] * f64["q"].shape[1]
+    oracle.parallel_slices(lambda sl: oracle.swin_attention(
+        f64["q"], f64["k"], f64["v"], f64["table"], M, slices=sl, out=out), np.arange(units))
+    return out
+
+
+@pytest.mark.parametrize("table_std", [0.02, 2.0])
+def test_swin_bf16_swin_t_stage1_whole(table_std):
+    # every one of the 6144 (window, head) units, element by element
     cfg = CONFIGS["swin_t_stage1"]
-    inp, out = _swin_case(cfg.num_windows, cfg.heads, cfg.d, "bf16")
+    inp, out = _swin_case(cfg.num_windows, cfg.heads, cfg.d, "bf16", table_std)
     units = cfg.num_windows * cfg.heads
-    rng = np.random.default_rng(0)
-    sl = np.unique(np.concatenate([rng.choice(units, 96, replace=False), [0, 1, units - 2, units - 1]]))
-    ref = oracle.swin_attention(inp["q"], inp["k"], inp["v"], inp["table"], 7, slices=sl)
-    got = out.reshape(units, 49, cfg.d)[torch.as_tensor(sl, device=out.device)]
-    ref = ref.reshape(units, 49, cfg.d)[sl]
-    assert _maxerr(got, ref) <= TOL_BF16
+    assert _maxerr(out, _swin_ref_threads(inp, 7)) <= TOL_BF16
     # property at any size: every output row is a convex combination of its window's v rows
     v = inp["v"].float().reshape(units, 49, cfg.d).cuda()
     o = out.float().reshape(units, 49, cfg.d)
@@ -190,29 +197,41 @@ def test_irpe_bf16_online_rescale_path():
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
 
 
+def _irpe_ref_threads(inp, H, W, flags, slices):
+    """The oracle on the given (batch, head) slices, split over host cores,
+    with the id map built once."""
+    ids, K = oracle.product_bucket_ids(H, W, *R19)
+    f64 = {k: oracle._f64(t) for k, t in inp.items() if t is not None}
+    out = np.zeros_like(f64["q"])
+    oracle.parallel_slices(lambda sl: oracle.irpe_attention_ids(
+        f64["q"], f64["k"], f64["v"], ids, K, flags, tab_q=f64.get("tab_q"),
+        tab_k=f64.get("tab_k"), tab_v=f64.get("tab_v"), slices=sl, out=out), slices)
+    return out
+
+
 @pytest.mark.parametrize("name", ["irpe_k_deit_s", "irpe_qkv_deit_s"])
-def test_irpe_bf16_deit_s_configs_sampled(name):
+@pytest.mark.parametrize("table_std", [0.02, 1.0])
+def test_irpe_bf16_deit_s_configs_whole(name, table_std):
+    # every one of the 384 (batch, head) slices, element by element, in the
+    # launch configuration bench.py times
     cfg = CONFIGS[name]
-    inp, out = _irpe_run(cfg.B, cfg.heads, cfg.H, cfg.W, cfg.flags)
+    inp, out = _irpe_run(cfg.B, cfg.heads, cfg.H, cfg.W, cfg.flags, table_std)
     S = cfg.B * cfg.heads
-    rng = np.random.default_rng(1)
-    sl = np.unique(np.concatenate([rng.choice(S, 20, replace=False), [0, S - 1]]))
-    ref = _irpe_ref(inp, cfg.H, cfg.W, cfg.flags, slices=sl).reshape(S, cfg.N, 64)[sl]
-    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
-    assert _maxerr(got, ref) <= TOL_BF16
+    assert _maxerr(out, _irpe_ref_threads(inp, cfg.H, cfg.W, cfg.flags, np.arange(S))) <= TOL_BF16
 
 
 @pytest.mark.parametrize("flags", [FLAG_K, FLAG_Q | FLAG_K | FLAG_V])
-def test_irpe_bf16_56x56_sampled(flags):
+def test_irpe_bf16_56x56_whole_slices(flags):
+    # eight whole slices of the 56x56 workload (3136 rows each). With 624 items
+    # on 152 SMs the last 16 items -- the odd last query tiles of slices 32..47
+    # -- run as two parts merged through the workspace: slices 32, 40, 46 and
+    # 47 cover those split items, 0, 1, 17 and 31 whole ones.
     cfg = CONFIGS["irpe_k_56x56"]
     inp, out = _irpe_run(cfg.B, cfg.heads, cfg.H, cfg.W, flags)
     S = cfg.B * cfg.heads
-    rows = np.unique(np.concatenate([np.arange(0, 40), np.arange(1500, 1530),
-                                     np.arange(cfg.N - 40, cfg.N)]))
-    sl = np.array([0, 17, S - 1])
-    ref = _irpe_ref(inp, cfg.H, cfg.W, flags, slices=sl, rows=rows)
-    ref = ref.reshape(S, cfg.N, 64)[sl][:, rows]
-    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
+    sl = np.array([0, 1, 17, 31, 32, 40, 46, S - 1])
+    ref = _irpe_ref_threads(inp, cfg.H, cfg.W, flags, sl).reshape(S, cfg.N, 64)[sl]
+    got = out.reshape(S, cfg.N, 64)[torch.as_tensor(sl, device=out.device)]
     assert _maxerr(got, ref) <= TOL_BF16
     # any size: rows are convex combinations of v (plus the value term when on)
     if not flags & FLAG_V:

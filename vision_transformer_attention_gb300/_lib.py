@@ -33,6 +33,8 @@ SIGNATURES = {
     "rpe_attn_fwd": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _u, _i, _p, _p]),
     "swin_window_attn_fwd": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p]),
     "swin_window_attn_fwd_noalloc": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _p, _p]),
+    "swin_noalloc_status": (_i, [ctypes.POINTER(_u), _i]),
+    "swin_noalloc_status_word": (_i, [ctypes.POINTER(_p)]),
     "swin_window_attn_fwd_fmap": (_i, [_p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _p, _p]),
     "rpe_attn_bias_fwd": (_i, [_p, _p, _p, _p, _i, _p, _i, ctypes.c_uint, _i, _i, _i, _i, _i, _i,
                                _p, _p]),

@@ -180,12 +180,48 @@ def swin_window_attn_fwd_fmap(q, k, v, bias_table, M, out=None):
 
 
 def rpe_device_status(clear=True):
-    """Synchronises the device; returns the in-kernel timeout status word (0 = none)."""
+    """Synchronises the device; returns the device status word (0 = none; bits
+    0-4 a bounded wait ran out, bit 5 an offset table held an id out of range)."""
     st = ctypes.c_uint(0)
     rc = _lib.lib().rpe_device_status(ctypes.byref(st), int(bool(clear)))
-    if rc not in (_lib.RPE_OK, _lib.RPE_ERR_TIMEOUT):
+    if rc not in (_lib.RPE_OK, _lib.RPE_ERR_TIMEOUT, _lib.RPE_ERR_INVALID_ARG) or (
+            rc == _lib.RPE_ERR_INVALID_ARG and st.value == 0):
         check("rpe_device_status", rc)
     return st.value
+
+
+def swin_window_attn_fwd_noalloc(q, k, v, bias_table, M, out=None):
+    """swin_window_attn_fwd (bf16) through the entry point that allocates no
+    device memory: its status word is a word of a fixed array in the library."""
+    _need(q, "q", torch.bfloat16)
+    nw, heads, n, d = q.shape
+    for name, t in (("k", k), ("v", v)):
+        _need(t, name, q.dtype, q.shape, q.device)
+    _need(bias_table, "bias_table", torch.float32, ((2 * M - 1) ** 2, heads), q.device)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need(out, "out", q.dtype, q.shape, q.device)
+    with torch.cuda.device(q.device):
+        check("swin_window_attn_fwd_noalloc", _lib.lib().swin_window_attn_fwd_noalloc(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(bias_table), nw, heads, M, d, _ptr(out), _stream(q)))
+    return out
+
+
+def swin_noalloc_status(clear=True):
+    """Synchronises the device; returns the no-allocation entry point's status word."""
+    st = ctypes.c_uint(0)
+    rc = _lib.lib().swin_noalloc_status(ctypes.byref(st), int(bool(clear)))
+    if rc not in (_lib.RPE_OK, _lib.RPE_ERR_TIMEOUT):
+        check("swin_noalloc_status", rc)
+    return st.value
+
+
+def swin_noalloc_status_word():
+    """Device address (int) of the no-allocation entry point's status word."""
+    w = ctypes.c_void_p(0)
+    check("swin_noalloc_status_word", _lib.lib().swin_noalloc_status_word(ctypes.byref(w)))
+    return w.value
 
 
 def rpe_wait_probe(limit_ns=1_000_000):

@@ -8,9 +8,13 @@
 
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
+#include <map>
 #include <mutex>
+#include <utility>
+#include <vector>
 
 namespace vta {
 namespace {
@@ -18,10 +22,23 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 unsigned *g_status[kMaxDevices] = {};
-float *g_split_ws[kMaxDevices] = {};
-size_t g_split_ws_floats[kMaxDevices] = {};
-int *g_split_cnt[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
+
+// Split-tail workspaces, one per (device, stream), each sized once for the
+// largest tail any launch on that device can have.
+struct SplitWs {
+    float *ws;
+    int *cnt;
+};
+std::map<std::pair<int, cudaStream_t>, SplitWs> g_split;
+
+// Offset tables whose ids are known to lie in [0, bound): the tables
+// rpe_build_bucket_ids wrote and the tables an attention call has checked,
+// keyed by device address.
+struct LutInfo {
+    int H, W, bound;
+};
+std::map<const void *, LutInfo> g_luts;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device() {
@@ -62,33 +79,71 @@ unsigned *device_status_word() {
     return g_status[dev];
 }
 
-bool device_split_workspace(size_t floats, float **ws, int **counters) {
+bool stream_split_workspace(cudaStream_t stream, size_t floats_per_item, float **ws,
+                            int **counters) {
     const int dev = current_device();
     if (dev < 0) return false;
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_split_cnt[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaMalloc(&p, kSplitCounters * sizeof(int)) != cudaSuccess) return false;
-        if (cudaMemset(p, 0, kSplitCounters * sizeof(int)) != cudaSuccess) {
-            cudaFree(p);
+    const auto key = std::make_pair(dev, stream);
+    auto it = g_split.find(key);
+    if (it == g_split.end()) {
+        // no allocation while the stream is being captured: the launch then
+        // runs every item whole
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+            return false;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            sms < 1 || 2 * ((sms + 1) / 2) > kSplitCounters)
+            return false;
+        // a tail has at most half a grid of items, a grid at most one CTA per SM
+        const size_t items = static_cast<size_t>(sms + 1) / 2;
+        void *w = nullptr, *c = nullptr;
+        if (cudaMalloc(&w, items * floats_per_item * sizeof(float)) != cudaSuccess) return false;
+        if (cudaMalloc(&c, kSplitCounters * sizeof(int)) != cudaSuccess ||
+            cudaMemset(c, 0, kSplitCounters * sizeof(int)) != cudaSuccess) {
+            cudaFree(w);
+            if (c != nullptr) cudaFree(c);
             return false;
         }
-        g_split_cnt[dev] = static_cast<int *>(p);
+        it = g_split.emplace(key, SplitWs{static_cast<float *>(w), static_cast<int *>(c)}).first;
     }
-    if (g_split_ws_floats[dev] < floats) {
-        void *p = nullptr;
-        if (cudaMalloc(&p, floats * sizeof(float)) != cudaSuccess) return false;
-        if (g_split_ws[dev] != nullptr) {
-            // an earlier launch may still read the old buffer
-            cudaDeviceSynchronize();
-            cudaFree(g_split_ws[dev]);
-        }
-        g_split_ws[dev] = static_cast<float *>(p);
-        g_split_ws_floats[dev] = floats;
-    }
-    *ws = g_split_ws[dev];
-    *counters = g_split_cnt[dev];
+    *ws = it->second.ws;
+    *counters = it->second.cnt;
     return true;
+}
+
+void lut_register(const int32_t *lut, int H, int W, int bound) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    g_luts[lut] = LutInfo{H, W, bound};
+}
+
+int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream) {
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        auto it = g_luts.find(lut);
+        if (it != g_luts.end() && it->second.H == H && it->second.W == W && it->second.bound <= limit)
+            return RPE_OK;
+    }
+    // a table not yet known: read it back once (a synchronous copy, which a
+    // stream capture does not allow)
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return RPE_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone) return RPE_ERR_UNSUPPORTED;
+    const size_t n = static_cast<size_t>(2 * H - 1) * (2 * W - 1);
+    std::vector<int32_t> host(n);
+    if (cudaMemcpyAsync(host.data(), lut, n * sizeof(int32_t), cudaMemcpyDeviceToHost, stream) !=
+            cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return RPE_ERR_CUDA;
+    int lo = INT_MAX, hi = INT_MIN;
+    for (const int32_t id : host) {
+        lo = id < lo ? id : lo;
+        hi = id > hi ? id : hi;
+    }
+    if (lo < 0 || hi >= limit) return RPE_ERR_INVALID_ARG;
+    lut_register(lut, H, W, hi + 1);
+    return RPE_OK;
 }
 
 int sm_count() {
@@ -164,8 +219,12 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, doub
     if (nb > 256) return RPE_ERR_INVALID_ARG;
     if (!aligned16(bucket_lut) || (ids != nullptr && !aligned16(ids))) return RPE_ERR_INVALID_ARG;
     *num_buckets = nb;
-    return status_of(launch_build_bucket_lut(H, W, mode, alpha, beta, gamma, bucket_lut, ids,
-                                             static_cast<cudaStream_t>(stream)));
+    const int rc = status_of(launch_build_bucket_lut(H, W, mode, alpha, beta, gamma, bucket_lut,
+                                                     ids, static_cast<cudaStream_t>(stream)));
+    // every id the kernel writes lies below the bucket count (for Cross: below
+    // span^2, the joint index)
+    if (rc == RPE_OK) lut_register(bucket_lut, H, W, mode == RPE_MAP_CROSS ? span * span : nb);
+    return rc;
 }
 
 int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_q,
@@ -200,6 +259,15 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
+    } else if (d != 64 || num_buckets > 128 || ((terms & RPE_TERM_Q) && num_buckets > 64)) {
+        // bf16: up to 128 buckets for the key and value terms (two 64-bucket
+        // halves), 64 for the query term
+        return RPE_ERR_UNSUPPORTED;
+    }
+    const int lut_rc = lut_check(bucket_lut, H, W,
+                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st);
+    if (lut_rc != RPE_OK) return lut_rc;
+    if (dtype == RPE_DTYPE_F32) {
         F32AttnArgs a{};
         a.cross_span = cross_span;
         a.cls = cls;
@@ -225,10 +293,6 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }
-    // bf16: up to 128 buckets for the key and value terms (two 64-bucket halves),
-    // 64 for the query term
-    if (d != 64 || num_buckets > 128 || ((terms & RPE_TERM_Q) && num_buckets > 64))
-        return RPE_ERR_UNSUPPORTED;
     RpeBf16Args a{};
     a.q = q;
     a.k = k;
@@ -278,6 +342,14 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
+    } else if (d != 64 || (W != 14 && W != 56) || num_buckets > 128 || cls) {
+        // bf16: the two-warpgroup kernel, which is specialised for these grid widths
+        return RPE_ERR_UNSUPPORTED;
+    }
+    const int lut_rc = lut_check(bucket_lut, H, W,
+                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st);
+    if (lut_rc != RPE_OK) return lut_rc;
+    if (dtype == RPE_DTYPE_F32) {
         F32AttnArgs a{};
         a.cross_span = cross_span;
         a.cls = cls;
@@ -299,8 +371,6 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }
-    // bf16: the two-warpgroup kernel, which is specialised for these grid widths
-    if (d != 64 || (W != 14 && W != 56) || num_buckets > 128 || cls) return RPE_ERR_UNSUPPORTED;
     RpeBf16Args a{};
     a.q = q;
     a.k = k;
@@ -353,7 +423,7 @@ int swin_window_attn_fwd(const void *q, const void *k, const void *v, const floa
         a.scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
         return status_of(launch_attn_f32(a, st));
     }
-    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30))
+    if (M != 7 || (d != 32 && d != 64) || heads > swin_bf16_max_heads() || units >= (1LL << 30))
         return RPE_ERR_UNSUPPORTED;
     SwinBf16Args a{q, k, v, out, bias_table, num_windows, heads, M, d};
     return status_of(launch_swin_bf16(a, st));
@@ -372,7 +442,7 @@ int swin_window_attn_fwd_fmap(const void *q, const void *k, const void *v,
         if (!aligned16(p)) return RPE_ERR_INVALID_ARG;
     const long long units =
         static_cast<long long>(batch) * (img_h / M) * (img_w / M) * static_cast<long long>(heads);
-    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30) ||
+    if (M != 7 || (d != 32 && d != 64) || heads > swin_bf16_max_heads() || units >= (1LL << 30) ||
         img_h >= (1 << 24) || img_w >= (1 << 24))
         return RPE_ERR_UNSUPPORTED;
     SwinFmapArgs a{q, k, v, out, bias_table, batch, img_h, img_w, heads, M, d};
@@ -389,7 +459,8 @@ int rpe_device_status(unsigned *status, int clear) {
         return RPE_ERR_CUDA;
     if (clear && host != 0 && cudaMemset(word, 0, sizeof(host)) != cudaSuccess) return RPE_ERR_CUDA;
     *status = host;
-    return host ? RPE_ERR_TIMEOUT : RPE_OK;
+    if (host & kStatusTimeoutMask) return RPE_ERR_TIMEOUT;
+    return host ? RPE_ERR_INVALID_ARG : RPE_OK;
 }
 
 int rpe_wait_probe(uint64_t limit_ns, void *stream) {

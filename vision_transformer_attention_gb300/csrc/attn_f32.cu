@@ -14,6 +14,7 @@
 // eqs. 22-24) a pair's joint id a*span + b selects table rows a and span + b,
 // and every term is the sum of the two rows' terms.
 #include "vta_internal.h"
+#include "sm103_ptx.cuh"
 
 #include <cmath>
 
@@ -30,7 +31,8 @@ struct SmemF32 {
 };
 
 // The table rows of a pair: {id, -1}, or for Cross tables {a, span + b} of the
-// joint id a*span + b. Ids outside the table are clamped into it.
+// joint id a*span + b. Ids outside the table (which the call's host check and
+// the kernel's scan of the table report) are clamped into it.
 struct Rows {
     int r0, r1;
 };
@@ -45,7 +47,7 @@ __device__ __forceinline__ Rows bucket_of(const F32AttnArgs &a, int i, int j) {
     const int cols = 2 * a.W - 1;
     const int off = (i / a.W - j / a.W + a.H - 1) * cols + (i % a.W - j % a.W + a.W - 1);
     int id = a.lut ? __ldg(a.lut + off) : off;
-    const int nid = a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets;
+    const int nid = (a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets) - a.cls;
     id = id < 0 ? 0 : (id >= nid ? nid - 1 : id);
     if (a.cross_span > 0) return Rows{id / a.cross_span, a.cross_span + id % a.cross_span};
     return Rows{id, -1};
@@ -108,6 +110,17 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(F32AttnArgs a) {
     const float *q = a.q + base;
     const float *k = a.k + base;
     const float *v = a.v + base;
+
+    // one block scans the offset table once: an id outside the table sets the
+    // status bit (bucket_of clamps it, so no read leaves the tables)
+    if (a.lut != nullptr && blockIdx.x == 0 && blockIdx.y == 0) {
+        const int bound = (a.cross_span > 0 ? a.cross_span * a.cross_span : a.num_buckets) - a.cls;
+        const int len = (2 * a.H - 1) * (2 * a.W - 1);
+        for (int e = threadIdx.x; e < len; e += blockDim.x) {
+            const int id = __ldg(a.lut + e);
+            if (id < 0 || id >= bound) atomicOr(a.status, kStatusBadBucket);
+        }
+    }
 
     float qi[kMaxD];
 #pragma unroll
@@ -181,7 +194,10 @@ __global__ void __launch_bounds__(kRows) attn_f32_kernel(F32AttnArgs a) {
 
 }  // namespace
 
-cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream) {
+cudaError_t launch_attn_f32(const F32AttnArgs &args, cudaStream_t stream) {
+    F32AttnArgs a = args;
+    a.status = device_status_word();
+    if (a.status == nullptr) return cudaErrorMemoryAllocation;
     const size_t smem = sizeof(SmemF32);
     cudaError_t err = cudaFuncSetAttribute(attn_f32_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,48 +1,52 @@
-// rpe_attn_pingpong_sm103.cu -- iRPE contextual-key attention (or plain
-// attention) on sm_103a: two query tiles per CTA, each softmaxed by eight
-// warps, with the tensor core fed through a ring of tensor-memory slots.
+// rpe_attn_pingpong_sm103.cu -- iRPE contextual-key attention (or bias mode,
+// or plain attention) on sm_103a: two query tiles per CTA, each softmaxed by
+// one warpgroup with one thread per query row, the tensor core fed through a
+// ring of tensor-memory score slots per tile.
 //
 // Same computation as rpe_attn_sm103.cu for the key term ("Rethinking and
 // Improving Relative Position Encoding for Vision Transformer", eqs. 13, 15
 // and the efficient form of eqs. 26-28): logits (q_i.k_j + q_i.R^K[id])/sqrt(d)
 // with QR = Q R^K^T formed once per query tile on the tensor core and read per
 // score by bucket id, softmax, P V. This kernel is the fast path for the
-// key-term-only and no-term requests on grids of width W in {14, 56}:
+// key-term-only, bias-mode and no-term requests on grids of width W in {14, 56}:
 //
-//   * A CTA takes a pair of 128-row query tiles of one (batch, head) slice;
-//     both share every K/V tile. Each query tile has a softmax group of eight
-//     warps: the two warps that share a tensor-memory lane quarter split each
-//     row's keys in halves, so four warps per SM sub-partition hide one
-//     another's latencies.
-//   * Each group has its own MMA-issuing warp (a single thread pushing small
-//     tcgen05.mma instructions manages about one per 60-130 cycles; two
-//     issuers nearly double the tensor core's intake) and its own ring of
-//     SLOTS tensor-memory slots. A "unit" is either QR = Q R^K^T (once per
-//     item) or one tile's scores; unit u goes into slot u mod SLOTS once unit
-//     u - SLOTS has been consumed (its QR copied out, or its P V issued). The
-//     issuer is a straight sequence of bounded blocking waits.
-//   * Per tile, each half computes its logits x = S c + QR'[id] (log2 units),
-//     writes them back over its scores, and reports its maximum; the two
-//     halves agree on the tile maximum (and on going on) with one bar.red per
-//     lane quarter. The reference max m of a row moves only when a tile's max
-//     exceeds it by more than 2^8, in which case O (earlier tiles) is
-//     rescaled. Then each half writes its probabilities as bf16 pairs over its
-//     own logits, where the P V product reads its A operand.
-//   * Key tiles hold whole grid rows: 84 keys (NS = 96 columns) for W = 14,
-//     56 keys (NS = 64) for W = 56. The offset-table
-//     bytes of one grid row of keys are contiguous, so a row's bucket ids are
-//     read as a few aligned words and taken out with byte permutes. Keys past
-//     the grid (last tile only) get -9984 added by one extra K = 16 product,
-//     so the softmax never tests for them. K/V are loaded as KT-row boxes into
-//     NS-row buffers whose last NS - KT rows stay zero.
-//   * The epilogue stages the bf16 output tile in the group's QR' table (not
-//     needed until the next item) with a 128-byte swizzle and writes it with
-//     one TMA store; rows past the grid fall outside the tensor map.
+//   * One CTA per SM, persistent over items. An item is a pair of 128-row
+//     query tiles of one (batch, head) slice (or a slice's odd last tile);
+//     both tiles share every K/V tile. Warps 0-3 softmax tile 0 and warps 4-7
+//     tile 1, one thread per query row; warp 8 is the TMA producer, warps 9
+//     and 10 the MMA issuers of the two tiles (one elected thread each); warp
+//     11 only takes part in the register split (setmaxnreg: 216 registers for
+//     the softmax warps, 64 for the others).
+//   * Key tiles hold whole grid rows: five or six rows at W = 14 (70 keys in
+//     NS = 80 score columns, or 84 in 96, whichever leaves fewer score
+//     columns per query row), one row (56 keys, NS = 64) at W = 56. K and V
+//     arrive as KT-row TMA boxes in NS-row buffers whose last NS - KT rows
+//     stay zero. Keys past the grid (last tile) get -9984 added by one extra
+//     K = 16 product with constant operands, so the softmax never tests them.
+//   * Each tile's group owns O (64 tensor-memory columns) and a ring of two
+//     score slots. A "unit" is QR' = Q R^K^T (once per item) or one key tile's
+//     scores; unit u goes into slot u mod 2 once unit u - 2 is consumed (its
+//     QR' copied to shared memory, or its P V issued). The issuer is a
+//     straight sequence of bounded blocking waits.
+//   * Per tile each thread reads its row's scores in one tensor-memory round
+//     trip, forms the logits x = S c + QR'[id] (c = log2 e / sqrt d) in
+//     registers -- the bucket ids come from the offset table in shared memory,
+//     read as aligned words per grid row of keys and taken out with byte
+//     permutes, and QR' lives in shared memory as [bucket][row] so every
+//     gather is conflict-free -- then writes p = 2^(x - m) as bf16 pairs over
+//     the scores, where the P V product reads its A operand. The reference max
+//     m moves only when a tile's max exceeds it by more than 2^8 (O is then
+//     rescaled).
+//   * An item's epilogue runs after the next item's QR' copy (so the copy
+//     overlaps the wait for the last P V); it stages the bf16 output tile in
+//     the group's own 16 KB area with a 128-byte swizzle and writes it with
+//     one TMA store (rows past the grid fall outside the tensor map).
+//   * When the last round of items fills at most half the grid, each of its
+//     items runs as two parts (halves of the key tiles) on two CTAs that
+//     merge through a per-stream workspace (see item_at and the epilogue).
 //
-// Warps 0-7: group 0 (warp 4h + q: half h, lane quarter q); 8-15: group 1;
-// warpgroup 4 (warps 16-19): 16 TMA producer, 17 and 18 MMA issuers of groups
-// 0 and 1, 19 idle. Tensor memory (512 columns): group w owns [256w, 256w+256):
-// O at +0 (64 columns), slot s at +64 + s NS.
+// Tensor memory (512 columns): group w owns [256 w, 256 w + 256): O at +0,
+// slot s at +64 + s NS.
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
 
@@ -222,8 +226,8 @@ __device__ __forceinline__ bool red_and(int id, int nthreads, bool v) {
 // has completed. Out of line: it runs only when a row's reference max moves.
 __device__ __forceinline__ bool rescale_o(float alpha, uint32_t tO, uint64_t *pv_bar,
                                        uint32_t pv_parity, const WaitCtl &wc,
-                                       volatile int *abort) {
-    if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort))) return false;
+                                       volatile int *abort, bool sleep) {
+    if (!__all_sync(~0u, mbar_wait(pv_bar, pv_parity, wc, kStatusTimeoutMma, abort, sleep))) return false;
     tc_fence_after();
 #pragma unroll 1
     for (int r = 0; r < 4; ++r) {
@@ -403,6 +407,11 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     using G = Geo<W, R>;
     using L = Layout<NG>;
     constexpr int kThreads = L::kThreads;
+    // Softmax warps wait with the suspending try (fewer issue slots taken
+    // from the warp sharing their scheduler) at W = 14, where that measured
+    // faster, and spin at W = 56, where it measured slower; the single-thread
+    // producer and issuers always spin (their reaction time matters more).
+    constexpr bool kSleep = W == 14;
     extern __shared__ uint8_t smem_raw[];
     // aligned by pointer arithmetic, so the compiler keeps the shared address space
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -466,13 +475,18 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     // everything above touches no input: it may overlap the previous kernel
     griddep_wait();
     if (HK || BM) {
-        // offset table as bytes, ids clamped into [0, nb). Keys past the last
-        // grid row index up to lut_pad bytes before the table; those bytes hold
-        // bucket 0 so every read stays in bounds (those scores are masked).
+        // offset table as bytes. The call checked its ids on the host (once per
+        // table); an id outside [0, bound) -- the class bucket excluded -- sets
+        // the status bit and is clamped so no read leaves shared memory. Keys
+        // past the last grid row index up to lut_pad bytes before the table;
+        // those bytes hold bucket 0 so every read stays in bounds (those scores
+        // are masked).
+        const int bound = P.nb - (CL ? 1 : 0);
         for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
         for (int e = tid; e < P.lut_len; e += kThreads) {
             const int id = __ldg(P.lut + e);
-            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
+            if (id < 0 || id >= bound) atomicOr(wc.status, kStatusBadBucket);
+            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= bound ? bound - 1 : id));
         }
         if (CL)
             for (int e = tid; e < P.cls_len; e += kThreads) sLut[P.lut_len + e] = static_cast<uint8_t>(P.nb - 1);
@@ -510,7 +524,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     const Item I = decode_item<SP>(P, item);
                     const int qb = it % P.nq, quse = it / P.nq;
                     if (!(ok = mbar_wait(&bars.q_empty[qb], (quse & 1) ^ 1, wc, kStatusTimeoutSync,
-                                         &abort_flag)))
+                                         &abort_flag, false)))
                         break;
                     uint8_t *qd = sQ + qb * NG * kTileBytes;
                     // per-head tables travel with the item's Q tiles: the Q buffer's
@@ -534,7 +548,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     for (int kt = I.kt0; kt < I.kt1; ++kt, ++g) {
                         const int st = g % P.nst, use = g / P.nst;
                         if (!(ok = mbar_wait(&bars.kv_empty[st], (use & 1) ^ 1, wc,
-                                             kStatusTimeoutSync, &abort_flag)))
+                                             kStatusTimeoutSync, &abort_flag, false)))
                             break;
                         uint8_t *kb = sKV + st * 2 * G::KV_BYTES;
                         mbar_arrive_expect_tx(&bars.kv_full[st], 2 * G::KT * 128);
@@ -581,7 +595,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 uint32_t u = 0;  // units issued
                 int ci = 0;      // items whose last P V was issued
                 bool ok = true;
-                if (HK && !RK_ITEM) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
+                if (HK && !RK_ITEM) ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag, false);
                 // consume the oldest outstanding unit: wait until the group has
                 // released it, then issue its P V
                 auto consume = [&]() {
@@ -591,10 +605,10 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     pend1 = pend2;
                     --np;
                     ok = ok && mbar_wait(&bars.slot_done[w][cu % G::SLOTS], (cu / G::SLOTS) & 1, wc,
-                                         kStatusTimeoutSync, &abort_flag);
+                                         kStatusTimeoutSync, &abort_flag, false);
                     if (!ok || (x & 0x10u)) return;
                     if (x & 0x20u)
-                        ok = mbar_wait(&bars.o_empty[w], (ci & 1) ^ 1, wc, kStatusTimeoutSync, &abort_flag);
+                        ok = mbar_wait(&bars.o_empty[w], (ci & 1) ^ 1, wc, kStatusTimeoutSync, &abort_flag, false);
                     if (!ok) return;
                     tc_fence_after();
                     const int st = x & 0xF;
@@ -616,7 +630,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 for (int item = item_at<SP>(P, 0); ok && item >= 0; item = item_at<SP>(P, ++it)) {
                     const Item I = decode_item<SP>(P, item);
                     const int qb = it % P.nq;
-                    ok = mbar_wait(&bars.q_full[qb], (it / P.nq) & 1, wc, kStatusTimeoutLoad, &abort_flag);
+                    ok = mbar_wait(&bars.q_full[qb], (it / P.nq) & 1, wc, kStatusTimeoutLoad, &abort_flag, false);
                     if (w == 1 && !I.has_b) {
                         // the outstanding units' P V release K/V stages that the
                         // loads below may be waiting for: issue them first
@@ -624,7 +638,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         for (int kt = I.kt0; ok && kt < I.kt1; ++kt, ++g) {
                             const int st = g % P.nst;
                             ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc, kStatusTimeoutLoad,
-                                           &abort_flag);
+                                           &abort_flag, false);
                             if (ok) mbar_arrive(&bars.kv_empty[st]);
                         }
                         if (ok) mbar_arrive(&bars.q_empty[qb]);
@@ -649,7 +663,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         } else {
                             const int st = g % P.nst;
                             ok = mbar_wait(&bars.kv_full[st], (g / P.nst) & 1, wc, kStatusTimeoutLoad,
-                                           &abort_flag);
+                                           &abort_flag, false);
                             if (!ok) break;
                             tc_fence_after();
                             const uint64_t dK = hi128 | ((aKV + st * 2 * G::KV_BYTES) >> 4);
@@ -715,7 +729,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         float due_m = 0.f, due_l = 1.f, due_xc = -INFINITY;
         auto epilogue = [&]() -> bool {
             const bool okd = ok && __all_sync(~0u, mbar_wait(&bars.o_full[wg], it_w & 1, wc,
-                                                            kStatusTimeoutMma, &abort_flag));
+                                                            kStatusTimeoutMma, &abort_flag, kSleep));
             // the previous TMA store has read the staging tile (the vote's
             // barrier orders this before the group's staging writes)
             if (leader) bulk_wait_read_all();
@@ -844,7 +858,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             uint32_t slot = u % G::SLOTS;
             if (HK)
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
-                                               kStatusTimeoutMma, &abort_flag)) && ok;
+                                               kStatusTimeoutMma, &abort_flag, kSleep)) && ok;
             if (!red_and(group_bar, 128, ok)) {
                 ok = false;
                 break;
@@ -900,7 +914,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 if (NQR == 2) {
                     slot = u % G::SLOTS;
                     ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
-                                                   kStatusTimeoutMma, &abort_flag)) && ok;
+                                                   kStatusTimeoutMma, &abort_flag, kSleep)) && ok;
                     if (ok) {
                         tc_fence_after();
                         if (warp_active) {
@@ -929,7 +943,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             for (int kt = I.kt0; kt < I.kt1; ++kt, ++gw, ++u) {
                 slot = u % G::SLOTS;
                 ok = __all_sync(~0u, mbar_wait(&bars.slot_full[wg][slot], (u / G::SLOTS) & 1, wc,
-                                               kStatusTimeoutMma, &abort_flag)) && ok;
+                                               kStatusTimeoutMma, &abort_flag, kSleep)) && ok;
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
@@ -946,7 +960,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         l *= alpha;
                     }
                     if (kt > I.kt0 && __any_sync(~0u, alpha < 1.f))
-                        ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag);
+                        ok = rescale_o(alpha, tOl, &bars.pv_done[wg], (gw - 1) & 1, wc, &abort_flag, kSleep);
                     l += Tile::probs(tSl, m, xs);
                     tmem_st_wait();
                 }
@@ -1081,7 +1095,7 @@ cudaError_t launch_pp(const RpeBf16Args &a, cudaStream_t stream) {
         if (T > 0 && p.nkt >= 2 && 2 * T <= grid && 2 * T <= kSplitCounters) {
             float *ws = nullptr;
             int *cnt = nullptr;
-            if (device_split_workspace(static_cast<size_t>(T) * 4 * 66 * 128, &ws, &cnt)) {
+            if (stream_split_workspace(stream, 4 * 66 * 128, &ws, &cnt)) {
                 p.whole = p.items - T;
                 p.tail = T;
                 p.ws = ws;

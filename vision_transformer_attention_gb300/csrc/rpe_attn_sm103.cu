@@ -149,11 +149,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 512);
-    // bucket-id table: int32 in global -> uint8 in shared memory
-    // (ids are clamped into [0, nb) so a bad table can never index past shared memory)
-    for (int e = tid; e < P.lut_len; e += kThreads) {
-        const int id = __ldg(P.lut + e);
-        sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= P.nb ? P.nb - 1 : id));
+    // bucket-id table: int32 in global -> uint8 in shared memory. The call
+    // checked its ids on the host (once per table); an id outside [0, bound)
+    // -- the class bucket excluded -- sets the status bit and is clamped so a
+    // bad table can never index past shared memory.
+    {
+        const int bound = P.nb - (EXT && P.cls ? 1 : 0);
+        for (int e = tid; e < P.lut_len; e += kThreads) {
+            const int id = __ldg(P.lut + e);
+            if (id < 0 || id >= bound) atomicOr(wc.status, kStatusBadBucket);
+            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= bound ? bound - 1 : id));
+        }
     }
     // Class token (iRPE section 4.1): entries lut_len..2 lut_len hold the extra
     // bucket nb - 1. The class key's offset term reaches there from every patch

@@ -19,7 +19,9 @@ enum : unsigned {
     kStatusTimeoutSync = 1u << 2,   // a hand-off between warps never arrived
     kStatusTimeoutDrain = 1u << 3,  // draining in-flight work after an abort ran out
     kStatusTimeoutProbe = 1u << 4,  // the self-test wait (nothing ever arrives)
+    kStatusBadBucket = 1u << 5,     // an offset table held an id outside [0, bound)
 };
+constexpr unsigned kStatusTimeoutMask = 0x1Fu;
 
 // Bound on every wait of a launch, and where to report a wait that ran out.
 struct WaitCtl {
@@ -70,6 +72,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended until the phase completes
+// or about hint_ns nanoseconds pass, whichever comes first, so a waiting warp
+// spins far less and leaves issue slots to the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Suspend bound of one try in mbar_wait (the wait's own bound is w.limit_ns).
+constexpr uint32_t kWaitSuspendNs = 20000;
+
 // Non-blocking test: true if the phase with the given parity has completed.
 __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
@@ -88,13 +109,20 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // w.limit_ns of GPU global time; in the latter case it sets `code` in the
 // status word and raises *abort. Returns true only if the phase completed.
 // Never traps and never spins without bound.
+// sleep = false keeps the thread spinning on plain tries instead (for a
+// single-thread role whose reaction time after the phase completes matters
+// more than the issue slots its spinning takes).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const WaitCtl &w,
-                                          unsigned code, volatile int *abort) {
+                                          unsigned code, volatile int *abort, bool sleep = true) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (true) {
-        for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (sleep) {
+            if (mbar_try_wait_sleep(bar, parity, kWaitSuspendNs)) return true;
+        } else {
+            for (int i = 0; i < 16; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+        }
         if (abort != nullptr && *abort) return false;
         if (global_ns() - t0 > w.limit_ns) {
             atomicOr(w.status, code);
@@ -314,6 +342,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         );
+}
+
+// 32 lanes x 8, 4 or 2 consecutive columns (as tmem_ld32; r[0..n-1] written).
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                   "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(taddr));
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {

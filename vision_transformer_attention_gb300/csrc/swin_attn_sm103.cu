@@ -334,8 +334,13 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     }
 }
 
+// The bf16 launch of pre-partitioned windows, shared by swin_window_attn_fwd
+// (status = the library's allocated status word) and the no-allocation entry
+// point (status = a word of its fixed array, cleared on `stream` first because
+// that array keeps the previous call's contents).
 template <int M, int D>
-cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
+cudaError_t launch_swin_tmpl(const SwinBf16Args &a, unsigned *status, bool clear_status,
+                             cudaStream_t stream) {
     using T = SwinTile<M, D>;
     if (a.heads > T::kMaxHeads) return cudaErrorInvalidValue;
     const int units = a.num_windows * a.heads;
@@ -358,8 +363,11 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, cudaStream_t stream) {
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            T::smem_bytes(T::kMaxHeads));
     if (err != cudaSuccess) return err;
-    unsigned *status = device_status_word();
     if (status == nullptr) return cudaErrorMemoryAllocation;
+    if (clear_status) {
+        err = cudaMemsetAsync(status, 0, sizeof(unsigned), stream);
+        if (err != cudaSuccess) return err;
+    }
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
     return launch_pdl(swin_bf16_kernel<M, D, false>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
@@ -407,10 +415,13 @@ cudaError_t launch_swin_fmap_tmpl(const SwinFmapArgs &a, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream) {
-    if (a.M == 7 && a.d == 32) return launch_swin_tmpl<7, 32>(a, stream);
-    if (a.M == 7 && a.d == 64) return launch_swin_tmpl<7, 64>(a, stream);
+    if (a.M == 7 && a.d == 32) return launch_swin_tmpl<7, 32>(a, device_status_word(), false, stream);
+    if (a.M == 7 && a.d == 64) return launch_swin_tmpl<7, 64>(a, device_status_word(), false, stream);
     return cudaErrorInvalidValue;
 }
+
+int swin_bf16_max_heads() { return SwinTile<7, 32>::kMaxHeads < SwinTile<7, 64>::kMaxHeads
+                                       ? SwinTile<7, 32>::kMaxHeads : SwinTile<7, 64>::kMaxHeads; }
 
 cudaError_t launch_swin_bf16_fmap(const SwinFmapArgs &a, cudaStream_t stream) {
     if (a.M == 7 && a.d == 32) return launch_swin_fmap_tmpl<7, 32>(a, stream);
@@ -467,41 +478,6 @@ cudaError_t noalloc_scratch(unsigned **out) {
     return cudaSuccess;
 }
 
-template <int M, int D>
-cudaError_t launch_swin_noalloc_tmpl(const SwinBf16Args &a, unsigned *status,
-                                     cudaStream_t stream) {
-    using T = SwinTile<M, D>;
-    if (a.heads > T::kMaxHeads) return cudaErrorInvalidValue;
-    const int units = a.num_windows * a.heads;
-    const int tiles = (units + 1) / 2;
-    const uint64_t dims[3] = {static_cast<uint64_t>(D), static_cast<uint64_t>(T::kN),
-                              static_cast<uint64_t>(units)};
-    const uint64_t strides[2] = {static_cast<uint64_t>(D) * 2,
-                                 static_cast<uint64_t>(T::kN) * D * 2};
-    const uint32_t box[3] = {static_cast<uint32_t>(D), 64, 2};
-    const CUtensorMapSwizzle swz =
-        (D == 32) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-    CUtensorMap tq, tk, tv, to;
-    if (!encode_tensor_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.q, dims, strides, box, swz) ||
-        !encode_tensor_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.k, dims, strides, box, swz) ||
-        !encode_tensor_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.v, dims, strides, box, swz) ||
-        !encode_tensor_map(&to, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.out, dims, strides, box, swz))
-        return cudaErrorInvalidValue;
-    const int smem = T::smem_bytes(a.heads);
-    cudaError_t err = cudaFuncSetAttribute(swin_bf16_kernel<M, D, false>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           T::smem_bytes(T::kMaxHeads));
-    if (err != cudaSuccess) return err;
-    // the array keeps the previous call's contents: the status word starts at zero
-    err = cudaMemsetAsync(status, 0, kNoAllocWordsPerCall * sizeof(unsigned), stream);
-    if (err != cudaSuccess) return err;
-    const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
-    const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
-    return launch_pdl(swin_bf16_kernel<M, D, false>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
-                      a.bias_table, a.heads, units, tiles, 1, 1, scale_log2e,
-                      WaitCtl{status, kDefaultWaitNs});
-}
-
 }  // namespace
 }  // namespace vta
 
@@ -517,7 +493,7 @@ extern "C" int swin_window_attn_fwd_noalloc(const void *q, const void *k, const 
     for (const void *p : ptrs)
         if ((reinterpret_cast<uintptr_t>(p) & 15u) != 0) return RPE_ERR_INVALID_ARG;
     const long long units = static_cast<long long>(num_windows) * heads;
-    if (M != 7 || (d != 32 && d != 64) || heads > 32 || units >= (1LL << 30))
+    if (M != 7 || (d != 32 && d != 64) || heads > swin_bf16_max_heads() || units >= (1LL << 30))
         return RPE_ERR_UNSUPPORTED;
     // every call needs kNoAllocWordsPerCall words of the fixed array, whatever its shape
     if (kNoAllocWordsPerCall > kNoAllocWords) return RPE_ERR_UNSUPPORTED;
@@ -525,7 +501,36 @@ extern "C" int swin_window_attn_fwd_noalloc(const void *q, const void *k, const 
     if (noalloc_scratch(&status) != cudaSuccess) return RPE_ERR_CUDA;
     SwinBf16Args a{q, k, v, out, bias_table, num_windows, heads, M, d};
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t err = (d == 32) ? launch_swin_noalloc_tmpl<7, 32>(a, status, st)
-                                : launch_swin_noalloc_tmpl<7, 64>(a, status, st);
+    cudaError_t err = (d == 32) ? launch_swin_tmpl<7, 32>(a, status, true, st)
+                                : launch_swin_tmpl<7, 64>(a, status, true, st);
     return err == cudaSuccess ? RPE_OK : RPE_ERR_CUDA;
+}
+
+extern "C" int swin_noalloc_status(unsigned *status, int clear) {
+    using namespace vta;
+    if (status == nullptr) return RPE_ERR_INVALID_ARG;
+    unsigned *word = nullptr;
+    if (noalloc_scratch(&word) != cudaSuccess) return RPE_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return RPE_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaMemcpyFromSymbol(&host, g_swin_noalloc_scratch, sizeof(host), 0,
+                             cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RPE_ERR_CUDA;
+    if (clear && host != 0) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_swin_noalloc_scratch, &zero, sizeof(zero), 0,
+                               cudaMemcpyHostToDevice) != cudaSuccess)
+            return RPE_ERR_CUDA;
+    }
+    *status = host;
+    return host ? RPE_ERR_TIMEOUT : RPE_OK;
+}
+
+extern "C" int swin_noalloc_status_word(unsigned **word) {
+    using namespace vta;
+    if (word == nullptr) return RPE_ERR_INVALID_ARG;
+    unsigned *p = nullptr;
+    if (noalloc_scratch(&p) != cudaSuccess) return RPE_ERR_CUDA;
+    *word = p;
+    return RPE_OK;
 }

@@ -16,13 +16,27 @@ struct WaitCtl;
 // that failed) and the default bound on in-kernel waits.
 unsigned *device_status_word();
 
-// Workspace of the split tail items of the two-warpgroup kernel on the current
-// device: at least `floats` fp32 (grown on demand, never shrunk) and
-// kSplitCounters arrival counters (zero between launches: the last arrival
-// resets its counter). False if an allocation failed. Launches that overlap on
-// one device share both, so they must not run the split path concurrently.
+// Workspace of the split tail items of the two-warpgroup kernel for launches on
+// `stream` of the current device: floats_per_item fp32 for each of up to
+// ceil(SMs / 2) tail items and kSplitCounters arrival counters (zero between
+// launches: the last arrival resets its counter). Allocated on the stream's
+// first use, at that size, and kept: launches on one stream run in order, and
+// launches on different streams use different workspaces, so no two launches
+// in flight share one. False (nothing allocated) while the stream is being
+// captured and has no workspace yet, or if an allocation failed; the launch
+// then runs every item whole.
 constexpr int kSplitCounters = 4096;
-bool device_split_workspace(size_t floats, float **ws, int **counters);
+bool stream_split_workspace(cudaStream_t stream, size_t floats_per_item, float **ws,
+                            int **counters);
+
+// Offset tables of bucket ids. lut_register records that the table at `lut`
+// for an H x W grid holds only ids in [0, bound). lut_check returns RPE_OK if
+// the table is known to hold only ids below `limit`; otherwise it reads the
+// table back once on `stream` (synchronously), checks it and records it:
+// RPE_ERR_INVALID_ARG for an id outside [0, limit), RPE_ERR_UNSUPPORTED if
+// the stream is being captured (no synchronous copy is possible there).
+void lut_register(const int32_t *lut, int H, int W, int bound);
+int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream);
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // Number of SMs of the current device (cached per device).
@@ -72,6 +86,7 @@ struct F32AttnArgs {
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
     int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
     int cls = 0;         // 1: token 0 is a class token, its pairs in bucket num_buckets - 1
+    unsigned *status = nullptr;  // device status word (set by launch_attn_f32)
 };
 cudaError_t launch_attn_f32(const F32AttnArgs &a, cudaStream_t stream);
 
@@ -82,6 +97,8 @@ struct SwinBf16Args {
     int num_windows, heads, M, d;
 };
 cudaError_t launch_swin_bf16(const SwinBf16Args &a, cudaStream_t stream);
+// Most heads the bf16 Swin kernels take (their shared-memory bias table).
+int swin_bf16_max_heads();
 // Swin window attention on channels-last feature maps [batch][img_h][img_w][heads][d]:
 // windows are read from and written back to the maps by the kernel's TMA boxes.
 struct SwinFmapArgs {
