@@ -72,7 +72,7 @@ enum { RPE_TABLES_PER_HEAD = 16 };
  * section 4.1). q, k, v and out then hold N = H * W + 1 tokens, token t >= 1
  * being grid token t - 1, and every pair involving token 0 takes the extra
  * bucket num_buckets - 1 (the offset table's ids lie below it). Not combined
- * with RPE_TABLES_CROSS; bf16 bias mode does not take it. */
+ * with RPE_TABLES_CROSS. */
 enum { RPE_CLS_TOKEN = 32 };
 
 /* Element types of q, k, v, out and the iRPE tables. */
@@ -192,10 +192,12 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
  * bucket_lut, num_buckets: as for rpe_attn_fwd (any mapping).
  * flags        : 0, or RPE_TABLES_CROSS for a Cross-mapping table (the bias
  *                of a pair is then b[a][h] + b[span + b'][h] for its joint
- *                index a * span + b'), or RPE_CLS_TOKEN (fp32 only).
+ *                index a * span + b'), or RPE_CLS_TOKEN (token 0 is a class
+ *                token whose pairs take bias row num_buckets - 1).
  * Supported: RPE_DTYPE_F32 on any grid with d <= 64 and num_buckets <= 256;
- * RPE_DTYPE_BF16 with d == 64, W in {14, 56} and num_buckets <= 128 (Cross as
- * for rpe_attn_fwd).
+ * RPE_DTYPE_BF16 on any grid with d == 64 and num_buckets <= 128 (Cross as
+ * for rpe_attn_fwd; W in {14, 56} without a class token runs on the
+ * two-warpgroup kernel, everything else on the general one).
  * Errors as for rpe_attn_fwd.
  */
 int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,

@@ -101,6 +101,8 @@ def _bias_case(B, heads, H, W, mode, shared, dtype, table_std, seed):
     (14, 14, RPE_MAP_PRODUCT, True, "bf16"),
     (14, 14, RPE_MAP_EUCLIDEAN, False, "bf16"),
     (9, 14, RPE_MAP_PRODUCT, False, "bf16"),     # 126 rows: one query tile per item
+    (6, 9, RPE_MAP_PRODUCT, False, "bf16"),      # general kernel (W not 14 or 56)
+    (20, 13, RPE_MAP_EUCLIDEAN, True, "bf16"),   # general kernel, two key tiles
     (5, 9, RPE_MAP_PRODUCT, False, "f32"),
     (5, 9, RPE_MAP_EUCLIDEAN, True, "f32"),
 ])
@@ -126,9 +128,9 @@ def test_bias_mode_56x56_sampled():
     assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
 
 
-def test_bias_mode_bf16_unsupported_width_is_an_error():
+def test_bias_mode_bf16_unsupported_head_dim_is_an_error():
     lut, _, nb = api.rpe_build_bucket_ids(6, 9, *R19)
-    inp = workloads.irpe_inputs(1, 2, 54, 64, nb, 0, "bf16")
+    inp = workloads.irpe_inputs(1, 2, 54, 32, nb, 0, "bf16")
     g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
     with pytest.raises(RpeError):
         api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], workloads.bias_table(nb, 2).cuda(), lut, nb, 6, 9)
@@ -188,7 +190,7 @@ def test_cross_attention_56x56_sampled():
     assert _maxerr(got, ref.reshape(S, H * W, 64)[sl][:, rows]) <= TOL_BF16
 
 
-@pytest.mark.parametrize("H,W,dtype", [(14, 14, "bf16"), (5, 9, "f32")])
+@pytest.mark.parametrize("H,W,dtype", [(14, 14, "bf16"), (9, 12, "bf16"), (5, 9, "f32")])
 def test_cross_bias_mode_matches_oracle(H, W, dtype):
     lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=RPE_MAP_CROSS)
     d = 64 if dtype == "bf16" else 32
@@ -431,17 +433,27 @@ def test_cls_token_56x56_sampled():
     assert _maxerr(got, ref.reshape(B * heads, N, 64)[sl][:, rows]) <= TOL_BF16
 
 
-def test_cls_bias_mode_fp32():
-    H, W = 6, 7
+@pytest.mark.parametrize("H,W,dtype,shared", [(6, 7, "f32", False), (6, 7, "bf16", False),
+                                              (14, 14, "bf16", True), (9, 20, "bf16", False)])
+def test_cls_bias_mode(H, W, dtype, shared):
+    # the class bucket's bias on every pair with token 0 (bf16: the general kernel)
     lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19)
-    inp = workloads.irpe_inputs(2, 3, H * W + 1, 32, nb + 1, 0, "f32", seed=43)
-    bias = workloads.bias_table(nb + 1, 3, 2.0, seed=44)
+    d = 32 if dtype == "f32" else 64
+    inp = workloads.irpe_inputs(2, 3, H * W + 1, d, nb + 1, 0, dtype, seed=43)
+    bias = workloads.bias_table(nb + 1, 1 if shared else 3, 2.0, seed=44)
+    bias[-1] = 16.0   # the class bucket: about two logits above the rest, so that it shows
     g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
     out = api.rpe_attn_bias_fwd(g["q"], g["k"], g["v"], bias.cuda(), lut, nb + 1, H, W,
                                 cls_token=True)
     ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(H, W, *R19))
-    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=bias.numpy())
-    assert _maxerr(out, ref) <= TOL_F32
+    b = bias.numpy()[:, 0] if shared else bias.numpy()
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=b)
+    assert _maxerr(out, ref) <= (TOL_F32 if dtype == "f32" else TOL_BF16)
+    # negative control: dropping the class bucket's bias moves the output past the tolerance
+    b0 = b.copy()
+    b0[-1] = 0.0
+    off = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, 0, bias_in=b0)
+    assert np.max(np.abs(off - ref)) > 3 * TOL_BF16
 
 
 def test_deit_s_cls_config_sampled():

@@ -73,11 +73,14 @@ def test_host_argument_checks_reject_before_any_launch():
                             0, fake, None) == 2
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64, 64,
                             0, fake, None) == 1
-    # class token with Cross tables, or in bf16 bias mode, is not served
+    # class token with Cross tables is not served
     cls_cross = cross_k | _lib.RPE_CLS_TOKEN
     assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 14, 1, 1, 14, 14, 64,
                             cls_cross, 0, fake, None) == 2
+    # bf16 bias mode needs d == 64 and at most 128 buckets
     assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 50, _lib.RPE_CLS_TOKEN, 1, 1,
+                                 14, 14, 32, 0, fake, None) == 2
+    assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 129, 0, 1, 1,
                                  14, 14, 64, 0, fake, None) == 2
     assert lib.rpe_attn_bias_fwd(fake, fake, fake, fake, 1, fake, 14, 2, 1, 1, 14, 14, 64, 0,
                                  fake, None) == 1

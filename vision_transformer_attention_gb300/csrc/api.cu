@@ -342,8 +342,9 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (dtype == RPE_DTYPE_F32) {
         if (d > 64 || slices > 65535) return RPE_ERR_UNSUPPORTED;
-    } else if (d != 64 || (W != 14 && W != 56) || num_buckets > 128 || cls) {
-        // bf16: the two-warpgroup kernel, which is specialised for these grid widths
+    } else if (d != 64 || num_buckets > 128) {
+        // bf16: the two-warpgroup kernel (W in {14, 56}, no class token) or the
+        // general kernel
         return RPE_ERR_UNSUPPORTED;
     }
     const int lut_rc = lut_check(bucket_lut, H, W,
@@ -387,6 +388,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     a.bias = bias_table;
     a.bias_heads = bias_heads;
     a.cross_span = cross_span;
+    a.cls = cls;
     return status_of(launch_rpe_bf16(a, st));
 }
 

@@ -66,6 +66,12 @@ struct RpeParams {
     int tab_heads, heads;  // tab_heads 1: tables shared by every head; heads: one per head
     int nr;        // 64-row halves of each table: 1, or 2 for 65..128 buckets (K and V terms)
     int cls;       // 1: token 0 is a class token (bucket nb - 1 for all its pairs)
+    // iRPE bias mode (with HK): a scalar per bucket and head, [num_buckets, bias_heads]
+    // fp32, takes the place of the contextual key term: the table a row gathers
+    // from holds the item's head's scaled bias instead of its QR' product, and no
+    // R^K is loaded or multiplied
+    const float *bias;
+    int bias_heads;
     uint32_t off_q, off_kv, off_p, off_rk, off_rq, off_rv, off_qr, off_kr, off_pb, off_kterm,
         off_lut;
     int lut_len;
@@ -181,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tmap(&tm_v);
             uint32_t tab_bytes = 0;
             const int nr = EXT ? P.nr : 1;
-            if (HK) tab_bytes += nr * (kTileBytes / 2);
+            const bool rk = HK && P.bias == nullptr;  // bias mode reads no R^K
+            if (rk) tab_bytes += nr * (kTileBytes / 2);
             if (HQ) tab_bytes += nr * (kTileBytes / 2);
             if (HV) tab_bytes += nr * (kTileBytes / 2);
             // each table as 32-row boxes of table `head` ([tab_heads][rows][d]):
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             auto load_tables = [&](int head) {
                 mbar_arrive_expect_tx(&bars.tab_full, tab_bytes);
-                if (HK) load_table(smem + P.off_rk, &tm_rk, head);
+                if (rk) load_table(smem + P.off_rk, &tm_rk, head);
                 if (HQ) load_table(smem + P.off_rq, &tm_rq, head);
                 if (HV) load_table(smem + P.off_rv, &tm_rv, head);
             };
@@ -262,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_par = parity;
             };
             bool ok = true;
-            const bool per_head = EXT && (HK || HQ || HV) && P.tab_heads > 1;
-            if ((HK || HQ || HV) && !per_head)
+            const bool rk = HK && P.bias == nullptr;  // bias mode: no Q R^K^T
+            const bool per_head = EXT && (rk || HQ || HV) && P.tab_heads > 1;
+            if ((rk || HQ || HV) && !per_head)
                 ok = mbar_wait(&bars.tab_full, 0, wc, kStatusTimeoutLoad, &abort_flag);
             int g = 0, w = 0, pr = 0;
             uint32_t qrc = 0;  // QR rounds issued (one per 64-row half of R^K)
@@ -274,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // QR = Q R^K^T, one 64-bucket half per round through the same
                 // 64 TMEM columns (the softmax warps copy each round out)
-                for (int r = 0; HK && ok && r < (EXT ? P.nr : 1); ++r, ++qrc) {
+                for (int r = 0; rk && ok && r < (EXT ? P.nr : 1); ++r, ++qrc) {
                     if (!(ok = mbar_wait(&bars.qr_empty, (qrc & 1) ^ 1, wc, kStatusTimeoutSync,
                                          &abort_flag)))
                         break;
@@ -382,7 +390,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int base_i = pi < 0 ? P.lut_len + centre : (pi / P.W) * cols + (pi % P.W) + centre;
             const uint8_t *lut_i = sLut + base_i;
             bool qr_ok = true;
-            for (int r = 0; HK && r < (EXT ? P.nr : 1); ++r, ++qrc) {
+            if (HK && P.bias != nullptr) {
+                // bias mode (eq. 14): the item's head's bias for every bucket,
+                // scaled like the logits (inside the 1/sqrt(d) scaling), in this
+                // row of the table; a Cross table's joint id a*span + b takes row
+                // bucket a plus column bucket span + b
+                const int col = P.bias_heads == 1 ? 0 : slice % P.heads;
+                for (int b = 0; b < P.nb; ++b) {
+                    float v;
+                    if (EXT && P.cross)
+                        v = __ldg(P.bias + (b / P.cross) * P.bias_heads + col) +
+                            __ldg(P.bias + (P.cross + b % P.cross) * P.bias_heads + col);
+                    else
+                        v = __ldg(P.bias + b * P.bias_heads + col);
+                    qr_t[b * 128] = v * P.c;
+                }
+            }
+            for (int r = 0; HK && P.bias == nullptr && r < (EXT ? P.nr : 1); ++r, ++qrc) {
                 // one round per item unless EXT: the item counter is the phase
                 const uint32_t qph = EXT ? qrc : static_cast<uint32_t>(w);
                 bool ok = __all_sync(~0u, mbar_wait(&bars.qr_full, qph & 1, wc, kStatusTimeoutMma,
@@ -661,6 +685,8 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
     p.items = slices * p.qtiles;
     p.lut_len = (2 * a.H - 1) * (2 * a.W - 1);
     p.cls = a.cls;
+    p.bias = a.bias;
+    p.bias_heads = a.bias_heads;
     p.lut = a.lut;
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.c = static_cast<float>(kLog2e / std::sqrt(static_cast<double>(kD)));
@@ -675,7 +701,7 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
         p.off_p = off;
         off += 2 * kTileBytes;
         p.off_rk = off;
-        if (HK) off += p.nr * (kTileBytes / 2);
+        if (HK && a.bias == nullptr) off += p.nr * (kTileBytes / 2);
         p.off_rq = off;
         if (HQ) off += p.nr * (kTileBytes / 2);
         p.off_rv = off;
@@ -713,7 +739,8 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
                 !encode_tensor_map(&tv, bf, 3, a.v, dims, strides, box, sw))
                 return cudaErrorInvalidValue;
             // tables not in use get a valid (never read) map over q
-            const void *rk = HK ? a.tab_k : a.q, *rq = HQ ? a.tab_q : a.q, *rv = HV ? a.tab_v : a.q;
+            const void *rk = HK && a.bias == nullptr ? a.tab_k : a.q, *rq = HQ ? a.tab_q : a.q,
+                       *rv = HV ? a.tab_v : a.q;
             if (!encode_tensor_map(&trk, bf, 3, rk, tdims, tstrides, tbox, sw) ||
                 !encode_tensor_map(&trq, bf, 3, rq, tdims, tstrides, tbox, sw) ||
                 !encode_tensor_map(&trv, bf, 3, rv, tdims, tstrides, tbox, sw))
@@ -752,7 +779,15 @@ cudaError_t launch_terms(const RpeBf16Args &a, cudaStream_t stream) {
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
     if (launch_rpe_bf16_pingpong(a, stream, &err)) return err;
-    if (a.bias != nullptr) return cudaErrorInvalidValue;  // bias mode: ping-pong kernel only
+    if (a.bias != nullptr) {
+        // bias mode on any grid (and with a class token): the key-term path with
+        // the bias row in place of QR'
+        RpeBf16Args b = a;
+        b.terms = 1u;
+        b.tab_heads = 1;
+        if (b.cross_span > 0 || b.num_buckets > 64 || b.cls) return launch_tmpl<true, false, false, true>(b, stream);
+        return launch_tmpl<true, false, false, false>(b, stream);
+    }
     if (a.cross_span > 0 || a.num_buckets > 64 || a.tab_heads > 1 || a.cls)
         return launch_terms<true>(a, stream);
     return launch_terms<false>(a, stream);
