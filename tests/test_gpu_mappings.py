@@ -53,6 +53,11 @@ def test_euclidean_ids_bit_exact(H, W, ratio):
 # alone is 2^-6; the value-term case therefore uses table_std 0.5.
 @pytest.mark.parametrize("B,heads,H,W,flags,dtype,table_std", [
     (2, 3, 14, 14, FLAG_K, "bf16", 1.0),                    # two-warpgroup kernel, W = 14
+    (2, 3, 14, 14, FLAG_K | FLAG_Q, "bf16", 1.0),           # same, with the query term
+    # the value term's bucket sums need each id to form one run along a grid row
+    # of keys; Euclidean ids repeat on both sides of the query column, so this
+    # runs on the general kernel
+    (2, 3, 14, 14, FLAG_K | FLAG_Q | FLAG_V, "bf16", 0.5),
     (1, 2, 9, 12, FLAG_K | FLAG_Q | FLAG_V, "bf16", 0.5),   # general kernel
     (1, 2, 5, 9, FLAG_K | FLAG_V, "f32", 1.0),              # fp32 path
 ])
@@ -67,6 +72,47 @@ def test_euclidean_attention_matches_oracle(B, heads, H, W, flags, dtype, table_
     ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
                                     tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
     assert _maxerr(out, ref) <= (TOL_BF16 if dtype == "bf16" else TOL_F32)
+
+
+def _row_runs(lut, H, W):
+    """Python statement of the offset-table property the value term's bucket
+    sums rely on: seen from any query column, each id forms one run along a
+    grid row of W keys."""
+    t = lut.cpu().numpy().reshape(2 * H - 1, 2 * W - 1)
+    for r in range(2 * H - 1):
+        for qx in range(W):
+            seq = [int(t[r, qx - kx + W - 1]) for kx in range(W)]
+            runs = [a for i, a in enumerate(seq) if i == 0 or a != seq[i - 1]]
+            if len(runs) != len(set(runs)):
+                return False
+    return True
+
+
+@pytest.mark.parametrize("mode", [RPE_MAP_PRODUCT, RPE_MAP_EUCLIDEAN, RPE_MAP_CROSS,
+                                  RPE_MAP_CLIP_PRODUCT])
+def test_built_tables_row_run_property(mode):
+    # the library records this property for the tables it builds without reading
+    # them back: true for Product, Cross and clip ids, false for Euclidean
+    for H, W, ratio in [(14, 14, 1.9), (10, 14, 2.0), (14, 14, 3.5)]:
+        lut, _, _ = api.rpe_build_bucket_ids(H, W, *workloads.index_constants(ratio), mode=mode)
+        assert _row_runs(lut, H, W) == (mode != RPE_MAP_EUCLIDEAN)
+
+
+@pytest.mark.parametrize("mode", [RPE_MAP_PRODUCT, RPE_MAP_EUCLIDEAN])
+def test_value_term_with_a_foreign_table(mode):
+    # a table the library did not build is read back once and checked for the
+    # property; either way the result matches the oracle
+    H, W, flags = 14, 14, FLAG_K | FLAG_V
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19, mode=mode)
+    foreign = lut.clone()
+    inp = workloads.irpe_inputs(2, 3, H * W, 64, nb, flags, "bf16", table_std=0.5, seed=31)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], foreign, nb, H, W, flags,
+                           table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, K = _ids(H, W, mode)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, K, flags,
+                                    tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= TOL_BF16
 
 
 def test_euclidean_attention_56x56_sampled():

@@ -171,6 +171,14 @@ def test_irpe_bf16_terms_deit_grid(flags, table_std):
     assert _maxerr(out, _irpe_ref(inp, 14, 14, flags)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("flags", ALL_TERMS)
+def test_irpe_bf16_terms_general_kernel(flags):
+    # a width the two-warpgroup kernel does not take: every term mix on the
+    # general kernel (two query tiles, two key tiles with a ragged second)
+    inp, out = _irpe_run(2, 3, 13, 11, flags, 1.0, seed=flags + 20)
+    assert _maxerr(out, _irpe_ref(inp, 13, 11, flags)) <= TOL_BF16
+
+
 @pytest.mark.parametrize("H,W,flags", [(4, 5, FLAG_K), (1, 1, FLAG_K), (3, 43, FLAG_Q | FLAG_K | FLAG_V),
                                        (16, 16, FLAG_K), (20, 13, FLAG_K | FLAG_V),
                                        (7, 64, FLAG_Q | FLAG_K)])
@@ -250,22 +258,33 @@ def test_irpe_bf16_repeat_is_deterministic():
 # ------------------------------------------------------------------ two-warpgroup path (W in {14, 56})
 
 @pytest.mark.parametrize("H,W,flags", [(20, 14, FLAG_K), (10, 56, FLAG_K), (1, 14, FLAG_K),
-                                       (9, 14, 0), (3, 56, 0), (28, 14, FLAG_K)])
+                                       (9, 14, 0), (3, 56, 0), (28, 14, FLAG_K),
+                                       # query / value terms: pairs of query tiles, ragged
+                                       # second tile (10 x 14: 128 + 12 rows), two items
+                                       # per slice (28 x 14), and grids they leave to the
+                                       # general kernel (odd query-tile counts)
+                                       (10, 14, FLAG_Q | FLAG_K | FLAG_V), (28, 14, FLAG_Q | FLAG_K | FLAG_V),
+                                       (18, 14, FLAG_K | FLAG_V), (28, 14, FLAG_Q),
+                                       (20, 14, FLAG_Q | FLAG_K | FLAG_V), (9, 14, FLAG_V)])
 def test_irpe_bf16_pingpong_grids(H, W, flags):
     # odd and even numbers of query tiles, single-tile grids, ragged last key tile
     inp, out = _irpe_run(2, 3, H, W, flags, table_std=1.0, seed=H + W)
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
 
 
-def test_irpe_bf16_pingpong_rescale_path():
-    # as test_irpe_bf16_online_rescale_path, on a width served by the two-warpgroup kernel
-    H, W, flags = 28, 14, FLAG_K
+@pytest.mark.parametrize("flags", [FLAG_K, FLAG_K | FLAG_V, FLAG_Q | FLAG_K | FLAG_V])
+def test_irpe_bf16_pingpong_rescale_path(flags):
+    # as test_irpe_bf16_online_rescale_path, on a width served by the two-warpgroup
+    # kernel (with the value term, the bucket sums are rescaled with O)
+    H, W = 28, 14
     inp = workloads.irpe_inputs(1, 2, H * W, 64, 49, flags, "bf16", 1.0, seed=7)
     k = inp["k"].float()
     k[:, :, 126:252] *= 6.0
     k[:, :, 252:] *= 12.0
     inp["k"] = k.to(torch.bfloat16)
     inp["v"] = (0.5 * inp["v"].float()).to(torch.bfloat16)
+    if inp["tab_v"] is not None:
+        inp["tab_v"] = (0.5 * inp["tab_v"].float()).to(torch.bfloat16)
     _, out = _irpe_run(1, 2, H, W, flags, inp=inp)
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
 

@@ -37,6 +37,7 @@ std::map<std::pair<int, cudaStream_t>, SplitWs> g_split;
 // keyed by device address.
 struct LutInfo {
     int H, W, bound;
+    bool row_runs;  // each id forms one run along any grid row of keys
 };
 std::map<const void *, LutInfo> g_luts;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -113,17 +114,40 @@ bool stream_split_workspace(cudaStream_t stream, size_t floats_per_item, float *
     return true;
 }
 
-void lut_register(const int32_t *lut, int H, int W, int bound) {
+void lut_register(const int32_t *lut, int H, int W, int bound, bool row_runs) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    g_luts[lut] = LutInfo{H, W, bound};
+    g_luts[lut] = LutInfo{H, W, bound, row_runs};
 }
 
-int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream) {
+// True if, in the offset table h (ids in [0, 256)), the ids that one query
+// column sees along any grid row of W keys form one run each: an id does not
+// come back once another id has followed it.
+bool lut_row_runs(const std::vector<int32_t> &h, int H, int W) {
+    const int cols = 2 * W - 1;
+    for (int r = 0; r < 2 * H - 1; ++r)
+        for (int qx = 0; qx < W; ++qx) {
+            bool ended[256] = {};
+            int prev = -1;
+            for (int kx = 0; kx < W; ++kx) {
+                const int id = h[static_cast<size_t>(r) * cols + (qx - kx + W - 1)];
+                if (id == prev) continue;
+                if (id < 0 || id >= 256 || ended[id]) return false;
+                if (prev >= 0) ended[prev] = true;
+                prev = id;
+            }
+        }
+    return true;
+}
+
+int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream, bool *row_runs) {
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         auto it = g_luts.find(lut);
-        if (it != g_luts.end() && it->second.H == H && it->second.W == W && it->second.bound <= limit)
+        if (it != g_luts.end() && it->second.H == H && it->second.W == W &&
+            it->second.bound <= limit) {
+            if (row_runs != nullptr) *row_runs = it->second.row_runs;
             return RPE_OK;
+        }
     }
     // a table not yet known: read it back once (a synchronous copy, which a
     // stream capture does not allow)
@@ -142,7 +166,9 @@ int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream) 
         hi = id > hi ? id : hi;
     }
     if (lo < 0 || hi >= limit) return RPE_ERR_INVALID_ARG;
-    lut_register(lut, H, W, hi + 1);
+    const bool runs = lut_row_runs(host, H, W);
+    lut_register(lut, H, W, hi + 1, runs);
+    if (row_runs != nullptr) *row_runs = runs;
     return RPE_OK;
 }
 
@@ -223,7 +249,12 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, doub
                                                      ids, static_cast<cudaStream_t>(stream)));
     // every id the kernel writes lies below the bucket count (for Cross: below
     // span^2, the joint index)
-    if (rc == RPE_OK) lut_register(bucket_lut, H, W, mode == RPE_MAP_CROSS ? span * span : nb);
+    // Product, clip and Cross ids are monotone in the column offset for a fixed
+    // row offset, so each id forms one run along a grid row of keys; Euclidean
+    // ids (a distance) repeat on both sides of the query column
+    if (rc == RPE_OK)
+        lut_register(bucket_lut, H, W, mode == RPE_MAP_CROSS ? span * span : nb,
+                     mode != RPE_MAP_EUCLIDEAN);
     return rc;
 }
 
@@ -264,8 +295,10 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
         // halves), 64 for the query term
         return RPE_ERR_UNSUPPORTED;
     }
+    bool row_runs = false;
     const int lut_rc = lut_check(bucket_lut, H, W,
-                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st);
+                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st,
+                                 &row_runs);
     if (lut_rc != RPE_OK) return lut_rc;
     if (dtype == RPE_DTYPE_F32) {
         F32AttnArgs a{};
@@ -312,6 +345,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.cross_span = cross_span;
     a.tab_heads = tab_heads;
     a.cls = cls;
+    a.lut_row_runs = row_runs;
     return status_of(launch_rpe_bf16(a, st));
 }
 
@@ -348,7 +382,8 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
         return RPE_ERR_UNSUPPORTED;
     }
     const int lut_rc = lut_check(bucket_lut, H, W,
-                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st);
+                                 (cross_span > 0 ? cross_span * cross_span : num_buckets) - cls, st,
+                                 nullptr);
     if (lut_rc != RPE_OK) return lut_rc;
     if (dtype == RPE_DTYPE_F32) {
         F32AttnArgs a{};

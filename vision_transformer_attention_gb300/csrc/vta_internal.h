@@ -35,8 +35,10 @@ bool stream_split_workspace(cudaStream_t stream, size_t floats_per_item, float *
 // table back once on `stream` (synchronously), checks it and records it:
 // RPE_ERR_INVALID_ARG for an id outside [0, limit), RPE_ERR_UNSUPPORTED if
 // the stream is being captured (no synchronous copy is possible there).
-void lut_register(const int32_t *lut, int H, int W, int bound);
-int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream);
+// row_runs records (and lut_check reports, when the pointer is not null)
+// whether each id forms one run along any grid row of keys.
+void lut_register(const int32_t *lut, int H, int W, int bound, bool row_runs);
+int lut_check(const int32_t *lut, int H, int W, int limit, cudaStream_t stream, bool *row_runs);
 constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
 
 // Number of SMs of the current device (cached per device).
@@ -120,6 +122,10 @@ struct RpeBf16Args {
     int cross_span = 0;  // > 0: Cross tables (row buckets, then column buckets); ids are joint a*span+b
     int tab_heads = 1;   // contextual tables: 1 shared, or heads (table h for head h)
     int cls = 0;         // 1: token 0 is a class token, its pairs in bucket num_buckets - 1
+    // the offset table's ids form one run per grid row of keys: along each
+    // row of W keys, seen from any query column, an id does not come back
+    // once another id has followed it (Product, clip and Cross tables)
+    bool lut_row_runs = false;
 };
 cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 
@@ -127,6 +133,10 @@ cudaError_t launch_rpe_bf16(const RpeBf16Args &a, cudaStream_t stream);
 // width it is specialised for. Returns false (and launches nothing) when it
 // does not cover the request; *err then stays untouched.
 bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err);
+// The same kernel with the query and / or value terms (W = 14, shared tables,
+// at most 64 buckets, an even number of query tiles, and for the value term
+// an offset table whose ids form one run per grid row of keys).
+bool launch_rpe_bf16_pingpong_qv(const RpeBf16Args &a, cudaStream_t stream, cudaError_t *err);
 
 cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
 
