@@ -1,18 +1,16 @@
-// rpe_pingpong.cuh -- the two-warpgroup iRPE attention kernel template and its
-// launcher, shared by the translation units that instantiate it
-// (rpe_attn_pingpong_sm103.cu: key term, bias mode, no term;
-// rpe_attn_pingpong_qv_sm103.cu: with the query and / or value terms).
+// rpe_pingpong.cuh -- iRPE attention on sm_103a with two query tiles per CTA,
+// each softmaxed by one warpgroup with one thread per query row, the tensor
+// core fed through a ring of tensor-memory score slots per tile: the kernel
+// template and its launcher, instantiated by rpe_attn_pingpong_sm103.cu (key
+// term, bias mode, no term) and rpe_attn_pingpong_qv_sm103.cu (with the query
+// and / or value terms).
 //
-// or plain attention) on sm_103a: two query tiles per CTA, each softmaxed by
-// one warpgroup with one thread per query row, the tensor core fed through a
-// ring of tensor-memory score slots per tile.
-//
-// Same computation as rpe_attn_sm103.cu for the key term ("Rethinking and
-// Improving Relative Position Encoding for Vision Transformer", eqs. 13, 15
-// and the efficient form of eqs. 26-28): logits (q_i.k_j + q_i.R^K[id])/sqrt(d)
-// with QR = Q R^K^T formed once per query tile on the tensor core and read per
-// score by bucket id, softmax, P V. This kernel is the fast path for the
-// key-term-only, bias-mode and no-term requests on grids of width W in {14, 56}:
+// Same computation as rpe_attn_sm103.cu ("Rethinking and Improving Relative
+// Position Encoding for Vision Transformer", eqs. 13-17 and the efficient form
+// of eqs. 26-28): logits (q_i.k_j + q_i.R^K[id] + k_j.R^Q[id])/sqrt(d), softmax,
+// P V plus the value term sum_j p_ij R^V[id], with QR = Q R^K^T formed once
+// per query tile and KR = K R^Q^T once per key tile on the tensor core and read
+// per score by bucket id. It is the fast path on grids of width W in {14, 56}:
 //
 //   * One CTA per SM, persistent over items. An item is a pair of 128-row
 //     query tiles of one (batch, head) slice (or a slice's odd last tile);
@@ -33,14 +31,20 @@
 //     QR' copied to shared memory, or its P V issued). The issuer is a
 //     straight sequence of bounded blocking waits.
 //   * Per tile each thread reads its row's scores in one tensor-memory round
-//     trip, forms the logits x = S c + QR'[id] (c = log2 e / sqrt d) in
-//     registers -- the bucket ids come from the offset table in shared memory,
-//     read as aligned words per grid row of keys and taken out with byte
-//     permutes, and QR' lives in shared memory as [bucket][row] so every
-//     gather is conflict-free -- then writes p = 2^(x - m) as bf16 pairs over
-//     the scores, where the P V product reads its A operand. The reference max
-//     m moves only when a tile's max exceeds it by more than 2^8 (O is then
-//     rescaled).
+//     trip, forms the logits x = S c + QR'[id] (+ KR[j][id]) (c = log2 e /
+//     sqrt d) in registers -- the bucket ids come from the offset table in
+//     shared memory, read as aligned words per grid row of keys and taken out
+//     with byte permutes, and QR' lives in shared memory as [bucket][row] --
+//     then writes p = 2^(x - m) as bf16 pairs over the scores, where the P V
+//     product reads its A operand. The reference max m moves only when a
+//     tile's max exceeds it by more than 2^8 (O is then rescaled).
+//   * Query term (five-row tiles at W = 14): group 0's issuer forms KR of each
+//     key tile in the 64 tensor-memory columns after the two groups' 224;
+//     warps 0-2 of both groups copy it (lane = key) to a shared fp16 table.
+//   * Value term: each row's probabilities go into per-bucket sums PB in
+//     shared memory, one grid row of keys at a time; at the item's end PB
+//     (bf16, in the staging tile) times R^V accumulates into O on the tensor
+//     core.
 //   * An item's epilogue runs after the next item's QR' copy (so the copy
 //     overlaps the wait for the last P V); it stages the bf16 output tile in
 //     the group's own 16 KB area with a 128-byte swizzle and writes it with
@@ -49,8 +53,8 @@
 //     items runs as two parts (halves of the key tiles) on two CTAs that
 //     merge through a per-stream workspace (see item_at and the epilogue).
 //
-// Tensor memory (512 columns): group w owns [256 w, 256 w + 256): O at +0,
-// slot s at +64 + s NS.
+// Tensor memory (512 columns): group w owns [C w, C w + C), C = 256 (224 with
+// the query term): O at +0, slot s at +64 + s NS; KR (query term) at 448.
 #pragma once
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
