@@ -468,15 +468,26 @@ def test_cls_token_matches_oracle(B, heads, H, W, flags, dtype, table_std, ratio
         assert np.max(np.abs(without - ref)) > 3 * TOL_BF16
 
 
-def test_cls_token_56x56_sampled():
-    rows = np.array([0, 1, 2, 1500, 3135, 3136])
-    sl = np.array([0, 4])
+def test_cls_token_56x56_whole_slices():
+    # two whole slices (3137 rows each) of a 56 x 56 grid with the class token,
+    # on the two-warpgroup kernel (its widened QR' product in 96-column slots)
     B, heads, H, W = 1, 6, 56, 56
-    _, out, ref, _, _ = _cls_case(B, heads, H, W, FLAG_K, "bf16", 1.0, seed=41, rows=rows,
-                                  slices=sl)
-    N = H * W + 1
-    got = out.reshape(B * heads, N, 64)[torch.as_tensor(sl, device=out.device)][:, torch.as_tensor(rows, device=out.device)]
-    assert _maxerr(got, ref.reshape(B * heads, N, 64)[sl][:, rows]) <= TOL_BF16
+    consts = workloads.index_constants(1.9)
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *consts)
+    inp = workloads.irpe_inputs(B, heads, H * W + 1, 64, nb + 1, FLAG_K, "bf16", table_std=1.0,
+                                seed=41)
+    g = {k: (None if t is None else t.cuda()) for k, t in inp.items()}
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb + 1, H, W, FLAG_K, cls_token=True,
+                           table_k=g["tab_k"])
+    ids, K = oracle.add_cls_bucket(*oracle.product_bucket_ids(H, W, *consts))
+    sl = np.array([0, 5])
+    f64 = {k: oracle._f64(t) for k, t in inp.items() if t is not None}
+    ref = np.zeros_like(f64["q"])
+    oracle.parallel_slices(lambda s_: oracle.irpe_attention_ids(
+        f64["q"], f64["k"], f64["v"], ids, K, FLAG_K, tab_k=f64["tab_k"], slices=s_, out=ref), sl)
+    N, S = H * W + 1, B * heads
+    got = out.reshape(S, N, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref.reshape(S, N, 64)[sl]) <= TOL_BF16
 
 
 @pytest.mark.parametrize("H,W,dtype,shared", [(6, 7, "f32", False), (6, 7, "bf16", False),
@@ -525,6 +536,9 @@ def test_deit_s_cls_config_sampled():
     (2, 2, 1, 14, False),    # one grid row: 15 tokens, one query tile
     (1, 3, 9, 14, True),     # 127 tokens (one query tile), per-head tables
     (1, 2, 10, 14, True),    # 141 tokens (a pair of query tiles), per-head tables
+    (1, 2, 3, 56, False),    # W = 56: 169 tokens (a pair of query tiles)
+    (2, 2, 2, 56, True),     # 113 tokens (one query tile), per-head tables
+    (1, 2, 5, 56, False),    # 281 tokens (a pair and an odd last tile)
 ])
 def test_cls_token_two_warpgroup_kernel(B, heads, H, W, per_head):
     # the class key is folded into each row after the grid keys and the class

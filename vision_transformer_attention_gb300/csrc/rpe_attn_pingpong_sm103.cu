@@ -25,10 +25,10 @@ cudaError_t launch_width(const RpeBf16Args &a, cudaStream_t stream, bool hk, boo
     if (bm) return (tf & 1) ? launch_pp<W, R, false, NG, true, 1>(a, stream)
                  : sp       ? launch_pp<W, R, false, NG, true, 4>(a, stream)
                             : launch_pp<W, R, false, NG, true, 0>(a, stream);
-    if constexpr (W == 14) {
-        if (a.cls) return (tf & 2) ? launch_pp<W, R, true, NG, false, 10>(a, stream)
-                                   : launch_pp<W, R, true, NG, false, 8>(a, stream);
-    }
+    // a class token: never split (the class key is folded into a whole item's
+    // row state in its epilogue)
+    if (a.cls) return (tf & 2) ? launch_pp<W, R, true, NG, false, 10>(a, stream)
+                               : launch_pp<W, R, true, NG, false, 8>(a, stream);
     if (hk && a.num_buckets > 64) return launch_pp<W, R, true, NG, false, 16>(a, stream);
     if (hk) {
         switch (tf) {
@@ -51,9 +51,9 @@ bool launch_rpe_bf16_pingpong(const RpeBf16Args &a, cudaStream_t stream, cudaErr
     const bool hk = (a.terms & 1u) != 0;
     const bool bm = a.bias != nullptr;
     if (hk && bm) return false;
-    // a class token: key term, shared or per-head (not Cross) tables, W = 14,
-    // whose score slots hold the 80 columns of the widened QR' product
-    if (a.cls && (!hk || a.cross_span > 0 || a.W != 14)) return false;
+    // a class token: key term, shared or per-head (not Cross) tables; the
+    // score slots hold the 80 columns of the widened QR' product
+    if (a.cls && (!hk || a.cross_span > 0)) return false;
     // the QR' product and copy cover 64 buckets, or 128 in two rounds with one
     // shared, non-Cross table and no class token; a bias row, one per thread, 128
     const bool hk128 = a.cross_span == 0 && a.tab_heads == 1 && !a.cls;

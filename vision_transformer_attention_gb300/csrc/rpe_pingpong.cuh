@@ -54,7 +54,9 @@
 //     merge through a per-stream workspace (see item_at and the epilogue).
 //
 // Tensor memory (512 columns): group w owns [C w, C w + C), C = 256 (224 with
-// the query term): O at +0, slot s at +64 + s NS; KR (query term) at 448.
+// the query term): O at +0, slot s at +64 + s NS (s 96 with a class token at
+// W = 56, where NS = 64 is short of the widened QR' product); KR (query
+// term) at 448.
 #pragma once
 #include "vta_internal.h"
 #include "sm103_ptx.cuh"
@@ -472,7 +474,7 @@ __device__ __forceinline__ constexpr uint32_t p_col(int kk) {
 // table form: bit 0, the table (R^K or the bias table) is laid out for the
 // Cross mapping; bit 1, R^K is one table per head; bit 2, the tail items may
 // run split in two parts (see item_at); bit 3, token 0 is a class token (with
-// the key term, W = 14); bit 4, 65..128 buckets (the QR' product in two rounds);
+// the key term); bit 4, 65..128 buckets (the QR' product in two rounds);
 // bit 5, the contextual query term; bit 6, the contextual value term (bits 5
 // and 6: W = 14 with five-row key tiles, shared tables, every item a pair of
 // query tiles).
@@ -516,8 +518,11 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     static_assert(!(HQ || HV) || (W == 14 && R == 5 && NG == 2 && !X && !PH && !SP && !CL && !BM &&
                                   NQR == 1),
                   "query / value terms: W = 14, five-row tiles, shared tables");
-    static_assert(!HQ || 2 * kGroupCols + 64 <= 512 && kColSlot0 + 2 * G::NS <= kGroupCols,
-                  "tensor-memory columns");
+    // score slots: NS columns apart, or 96 with a class token where NS < 80,
+    // so that the widened QR' product (80 columns) fits in either slot
+    constexpr uint32_t kSlotCols = (CL && G::NS < 80) ? 96u : static_cast<uint32_t>(G::NS);
+    static_assert(kColSlot0 + 2 * kSlotCols <= kGroupCols, "tensor-memory columns per group");
+    static_assert(!HQ || 2 * kGroupCols + 64 <= 512, "tensor-memory columns");
     // Softmax warps wait with the suspending try (fewer issue slots taken
     // from the warp sharing their scheduler) at W = 14, where that measured
     // faster, and spin at W = 56, where it measured slower; the single-thread
@@ -746,7 +751,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                     tc_fence_after();
                     const int st = x & 0xF;
                     const uint64_t dV = hi128 | ((aKV + (st * 2 + 1) * G::KV_BYTES) >> 4);
-                    const uint32_t aP = tG + kColSlot0 + (cu % G::SLOTS) * G::NS;
+                    const uint32_t aP = tG + kColSlot0 + (cu % G::SLOTS) * kSlotCols;
                     const uint32_t acc0 = (x & 0x20u) ? 0u : 1u;
 #pragma unroll
                     for (int kk = 0; kk < G::NS / 16; ++kk)
@@ -795,7 +800,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         if (np == G::SLOTS) consume();
                         if (!ok) break;
                         const uint32_t slot = u % G::SLOTS;
-                        const uint32_t dS = tG + kColSlot0 + slot * G::NS;
+                        const uint32_t dS = tG + kColSlot0 + slot * kSlotCols;
                         uint32_t code;
                         if (kt < I.kt0) {  // a QR' unit (round kt - kt0 + NQR)
                             tc_fence_after();
@@ -1046,9 +1051,9 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 tc_fence_after();
                 if (warp_active) {
                     uint32_t r0[32], r1[32], rk[16];
-                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off, r0);
-                    tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32, r1);
-                    if (CL) tmem_ld16(tG + kColSlot0 + slot * G::NS + lane_off + 64, rk);
+                    tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off, r0);
+                    tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off + 32, r1);
+                    if (CL) tmem_ld16(tG + kColSlot0 + slot * kSlotCols + lane_off + 64, rk);
                     tmem_ld_wait();
                     tmem_ready(r0);
                     tmem_ready(r1);
@@ -1090,8 +1095,8 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                         tc_fence_after();
                         if (warp_active) {
                             uint32_t r0[32], r1[32];
-                            tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off, r0);
-                            tmem_ld32(tG + kColSlot0 + slot * G::NS + lane_off + 32, r1);
+                            tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off, r0);
+                            tmem_ld32(tG + kColSlot0 + slot * kSlotCols + lane_off + 32, r1);
                             tmem_ld_wait();
                             tmem_ready(r0);
                             tmem_ready(r1);
@@ -1153,7 +1158,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                                                kStatusTimeoutMma, &abort_flag, kSleep)) && ok;
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tSl = tG + kColSlot0 + slot * G::NS + lane_off;
+                const uint32_t tSl = tG + kColSlot0 + slot * kSlotCols + lane_off;
                 const int e0 = base_i - kt * G::R * G::COLS;
                 using Tile = HalfTile<W, R, HK || BM, 0, BM ? 1 : 128, BM ? 1 : QM, HQ>;
                 if (warp_active) {
