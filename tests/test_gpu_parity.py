@@ -272,6 +272,24 @@ def test_irpe_bf16_pingpong_grids(H, W, flags):
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("flags", [FLAG_Q | FLAG_K | FLAG_V, FLAG_K | FLAG_V])
+def test_irpe_bf16_qv_bucket_count_past_the_fast_layout(flags):
+    # 60 declared buckets (ids 0..48 used): the two-warpgroup kernel's query /
+    # value layout holds at most 51 next to each other, so the request runs on
+    # the general kernel, with the same result as the oracle
+    H, W, nb = 14, 14, 60
+    lut, _, nb49 = api.rpe_build_bucket_ids(H, W, *R19)
+    assert nb49 == 49
+    inp = workloads.irpe_inputs(2, 3, H * W, 64, nb, flags, "bf16", 1.0, seed=61)
+    g = _dev(inp)
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags,
+                           table_q=g["tab_q"], table_k=g["tab_k"], table_v=g["tab_v"])
+    ids, _ = oracle.product_bucket_ids(H, W, *R19)
+    ref = oracle.irpe_attention_ids(inp["q"], inp["k"], inp["v"], ids, nb, flags,
+                                    tab_q=inp["tab_q"], tab_k=inp["tab_k"], tab_v=inp["tab_v"])
+    assert _maxerr(out, ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("flags", [FLAG_K, FLAG_K | FLAG_V, FLAG_Q | FLAG_K | FLAG_V])
 def test_irpe_bf16_pingpong_rescale_path(flags):
     # as test_irpe_bf16_online_rescale_path, on a width served by the two-warpgroup
