@@ -149,7 +149,12 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                its check is caught by the kernel instead, which sets a
  *                status bit that rpe_device_status reports as
  *                RPE_ERR_INVALID_ARG (the id is clamped meanwhile, so no read
- *                leaves the tables).
+ *                leaves the tables). The check also records whether, seen
+ *                from any query column, each id forms one run along a grid
+ *                row of keys (true of Product, clip and Cross tables, false
+ *                of Euclidean ones); the fast value-term path (bf16, W = 14)
+ *                needs it. A table rewritten in place so that this no longer
+ *                holds is reported the same way.
  * terms        : OR of RPE_TERM_K / RPE_TERM_Q / RPE_TERM_V (0 = plain attention),
  *                plus RPE_TABLES_CROSS for tables of the Cross mapping,
  *                RPE_TABLES_PER_HEAD for one table per head and RPE_CLS_TOKEN

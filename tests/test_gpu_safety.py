@@ -4,7 +4,9 @@
   and checked on its first use; an id outside the table's range is refused
   before any launch. A checked table rewritten in place with a bad id is
   caught by the kernels, which set the status bit that rpe_device_status
-  reports (no read leaves the tables meanwhile).
+  reports (no read leaves the tables meanwhile); so is a table rewritten so
+  that its ids no longer form one run per grid row of keys, which the value
+  term's bucket sums rely on.
 - Split tail items: the two-warpgroup kernel merges split items through a
   workspace owned by the launching stream, so launches on two streams may
   overlap; a capture on a stream that has no workspace yet runs every item
@@ -98,6 +100,31 @@ def test_table_rewritten_in_place_sets_the_status_bit(dtype, H, W):
     status = api.rpe_device_status(clear=True)
     assert status & BAD_BUCKET_BIT
     assert bool(torch.isfinite(out.float()).all())
+    assert api.rpe_device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("flags", [FLAG_K | FLAG_V, FLAG_V])
+def test_table_rewritten_without_row_runs_sets_the_status_bit(flags):
+    # the value term's bucket sums need each id to form one run along a grid
+    # row of keys; a Product table (recorded with that property) rewritten in
+    # place with Euclidean ids -- in range, but repeating on both sides of a
+    # query column -- is caught by the kernel
+    H, W = 14, 14
+    lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19)
+    eu, _, nbe = api.rpe_build_bucket_ids(H, W, *R19, mode=_lib.RPE_MAP_EUCLIDEAN)
+    assert nbe <= nb
+    inp = _dev(workloads.irpe_inputs(1, 2, H * W, 64, nb, flags, "bf16", 1.0, seed=8))
+    run = lambda t: api.rpe_attn_fwd(inp["q"], inp["k"], inp["v"], t, nb, H, W, flags,  # noqa: E731
+                                     table_k=inp["tab_k"], table_v=inp["tab_v"])
+    assert api.rpe_device_status(clear=True) == 0
+    lut.copy_(eu)
+    out = run(lut)
+    status = api.rpe_device_status(clear=True)
+    assert status & BAD_BUCKET_BIT
+    assert bool(torch.isfinite(out.float()).all())
+    # the Euclidean table as the library built it is recorded without the
+    # property: the request runs on the general kernel and raises nothing
+    run(eu)
     assert api.rpe_device_status(clear=True) == 0
 
 

@@ -623,7 +623,6 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
-
     if (warp >= 4 * NG) {
         regs_dealloc<L::kRegsControl>();
         if (warp == 4 * NG) {
@@ -856,6 +855,27 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
                 mbar_wait(&bars.fin[w], 0, drain, kStatusTimeoutDrain, nullptr);
             }
             __syncwarp();
+        } else if (HV && blockIdx.x == 0) {
+            // The value term's bucket sums rely on each id forming one run
+            // along a grid row of keys, seen from any query column; the call
+            // checked that once per table. A table rewritten in place since then
+            // is caught here, by the otherwise idle control warp of one CTA (the
+            // table is the same for all): one offset-table row and query column
+            // per lane at a time (ids < 64).
+            for (int e = lane; e < (2 * P.H - 1) * W; e += 32) {
+                const uint8_t *row = sLut + (e / W) * G::COLS + (e % W) + (W - 1);
+                unsigned long long ended = 0ull;
+                int prev = -1;
+                bool bad = false;
+                for (int kx = 0; kx < W; ++kx) {
+                    const int id = row[-kx];
+                    if (id == prev) continue;
+                    bad = bad || ((ended >> id) & 1ull) != 0ull;
+                    if (prev >= 0) ended |= 1ull << prev;
+                    prev = id;
+                }
+                if (bad) atomicOr(wc.status, kStatusBadBucket);
+            }
         }
     } else {
         regs_alloc<L::kRegsSoftmax>();
