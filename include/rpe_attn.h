@@ -323,6 +323,28 @@ int rpe_wait_probe(uint64_t limit_ns, void *stream);
 /* rpe_status_string -- a static description of a status code. */
 const char *rpe_status_string(int status);
 
+/*
+ * rpe_release_stream -- frees the split-tail workspace the library keeps for
+ * `stream` on the current device, if there is one (see rpe_attn_fwd, "Device
+ * memory"); call it before destroying a stream that ran such calls. No work
+ * on the stream that may use the workspace may be pending (cudaFree waits for
+ * the device anyway) and no captured graph that uses it may be replayed
+ * afterwards. The stream's next split call allocates again. Returns RPE_OK
+ * (also when there was nothing to free) or RPE_ERR_CUDA.
+ */
+int rpe_release_stream(void *stream);
+
+/*
+ * rpe_shutdown -- frees every device allocation the library has made (the
+ * status words and the split-tail workspaces, on every device) and forgets
+ * the offset tables it has recorded as checked. Call it when no library work
+ * is pending or being captured; no graph captured before it may be replayed
+ * after it. The next call allocates again. The no-allocation Swin entry
+ * point's fixed array is not an allocation and stays. Returns RPE_OK, or
+ * RPE_ERR_CUDA for the first failure (the rest is still freed).
+ */
+int rpe_shutdown(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -172,6 +172,34 @@ def test_split_tail_launches_on_two_streams_overlap_safely():
         assert _maxerr(got, _split_ref(inp, shape, sl)) <= TOL_BF16
 
 
+def test_release_stream_and_shutdown_free_and_reallocate():
+    # a stream's split-tail workspace can be freed and comes back on its next
+    # split call; rpe_shutdown frees everything (status words included) and
+    # forgets the recorded tables; results stay bit-identical throughout
+    shape, inp = _split_case(seed=23)
+    B, heads, H, W = shape
+    g = _dev(inp)
+    s = torch.cuda.Stream()
+
+    def run():
+        lut, _, nb = api.rpe_build_bucket_ids(H, W, *R19)
+        with torch.cuda.stream(s):
+            out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, FLAG_K, table_k=g["tab_k"])
+        s.synchronize()
+        return out
+
+    first = run()
+    api.rpe_release_stream(s)
+    api.rpe_release_stream(s)  # nothing left to free: still fine
+    assert torch.equal(run(), first)
+    api.rpe_shutdown()
+    assert torch.equal(run(), first)
+    assert api.rpe_device_status(clear=True) == 0
+    sl = np.array([0, B * heads - 1])
+    got = first.reshape(B * heads, H * W, 64)[torch.as_tensor(sl, device=first.device)]
+    assert float((got.float().cpu() - torch.as_tensor(_split_ref(inp, shape, sl))).abs().max()) <= TOL_BF16
+
+
 def test_capture_on_a_stream_without_workspace_runs_items_whole():
     shape, inp = _split_case(63)
     B, heads, H, W = shape

@@ -31,6 +31,13 @@ def test_library_builds_and_exports_every_declared_symbol():
     assert set(_declared_symbols()) == set(_lib.SIGNATURES)
 
 
+def test_release_calls_without_gpu_have_nothing_to_free():
+    from vision_transformer_attention_gb300 import _lib
+    lib = _lib.lib()
+    assert lib.rpe_release_stream(None) == _lib.RPE_OK
+    assert lib.rpe_shutdown() == _lib.RPE_OK
+
+
 def test_status_strings_without_gpu():
     from vision_transformer_attention_gb300 import _lib
     lib = _lib.lib()

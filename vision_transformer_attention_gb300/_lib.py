@@ -41,6 +41,8 @@ SIGNATURES = {
     "rpe_device_status": (_i, [ctypes.POINTER(_u), _i]),
     "rpe_wait_probe": (_i, [_u64, _p]),
     "rpe_status_string": (ctypes.c_char_p, [_i]),
+    "rpe_release_stream": (_i, [_p]),
+    "rpe_shutdown": (_i, []),
 }
 
 _lib = None

@@ -190,6 +190,19 @@ def rpe_device_status(clear=True):
     return st.value
 
 
+def rpe_release_stream(stream=None):
+    """Frees the split-tail workspace the library keeps for `stream` (default:
+    the current stream) on the current device, if there is one."""
+    s = stream if stream is not None else torch.cuda.current_stream()
+    check("rpe_release_stream", _lib.lib().rpe_release_stream(ctypes.c_void_p(s.cuda_stream)))
+
+
+def rpe_shutdown():
+    """Frees every device allocation of the library and forgets the offset
+    tables it recorded as checked; the next call allocates again."""
+    check("rpe_shutdown", _lib.lib().rpe_shutdown())
+
+
 def swin_window_attn_fwd_noalloc(q, k, v, bias_table, M, out=None):
     """swin_window_attn_fwd (bf16) through the entry point that allocates no
     device memory: its status word is a word of a fixed array in the library."""

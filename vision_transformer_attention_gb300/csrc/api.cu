@@ -506,6 +506,39 @@ int rpe_wait_probe(uint64_t limit_ns, void *stream) {
     return status_of(launch_wait_probe(lim, static_cast<cudaStream_t>(stream)));
 }
 
+int rpe_release_stream(void *stream) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return RPE_OK;  // nothing allocated
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_split.find(std::make_pair(dev, static_cast<cudaStream_t>(stream)));
+    if (it == g_split.end()) return RPE_OK;
+    const bool ok = cudaFree(it->second.ws) == cudaSuccess && cudaFree(it->second.cnt) == cudaSuccess;
+    g_split.erase(it);
+    return ok ? RPE_OK : RPE_ERR_CUDA;
+}
+
+int rpe_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int rc = RPE_OK;
+    int cur = -1;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    auto fail = [&]() { if (rc == RPE_OK) rc = RPE_ERR_CUDA; };
+    for (auto &kv : g_split) {
+        if (cudaSetDevice(kv.first.first) != cudaSuccess || cudaFree(kv.second.ws) != cudaSuccess ||
+            cudaFree(kv.second.cnt) != cudaSuccess)
+            fail();
+    }
+    g_split.clear();
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (g_status[d] == nullptr) continue;
+        if (cudaSetDevice(d) != cudaSuccess || cudaFree(g_status[d]) != cudaSuccess) fail();
+        g_status[d] = nullptr;
+    }
+    g_luts.clear();
+    if (have_cur && cudaSetDevice(cur) != cudaSuccess) fail();
+    return rc;
+}
+
 const char *rpe_status_string(int status) {
     switch (status) {
         case RPE_OK: return "ok";
