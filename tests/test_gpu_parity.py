@@ -272,6 +272,32 @@ def test_irpe_bf16_pingpong_grids(H, W, flags):
     assert _maxerr(out, _irpe_ref(inp, H, W, flags)) <= TOL_BF16
 
 
+@pytest.mark.parametrize("B,heads,H,W,flags", [
+    (1, 2, 28, 14, FLAG_K),                    # one item per CTA: the rescale at a group's last tile
+    (1, 2, 10, 56, FLAG_K),                    # same at W = 56
+    (40, 4, 28, 14, FLAG_K),                   # 320 items: some CTAs run three, so an item's last
+    (40, 4, 28, 14, FLAG_Q | FLAG_K | FLAG_V),  # tile is followed by the next item's first unit
+])
+def test_irpe_bf16_pingpong_rescale_at_last_tiles(B, heads, H, W, flags):
+    # the last grid row of keys gets far larger logits, so the reference max
+    # jumps at the last key tile of every item (see the rescale test above for
+    # the bound that halving v and R^V keeps under the tolerance)
+    N = H * W
+    inp = workloads.irpe_inputs(B, heads, N, 64, 49, flags, "bf16", 1.0, seed=13)
+    k = inp["k"].float()
+    k[:, :, N - W:] *= 12.0
+    inp["k"] = k.to(torch.bfloat16)
+    inp["v"] = (0.5 * inp["v"].float()).to(torch.bfloat16)
+    if inp["tab_v"] is not None:
+        inp["tab_v"] = (0.5 * inp["tab_v"].float()).to(torch.bfloat16)
+    _, out = _irpe_run(B, heads, H, W, flags, inp=inp)
+    S = B * heads
+    sl = np.array(sorted({0, 1, S // 2, S - 1}))
+    ref = _irpe_ref_threads(inp, H, W, flags, sl).reshape(S, N, 64)[sl]
+    got = out.reshape(S, N, 64)[torch.as_tensor(sl, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_BF16
+
+
 @pytest.mark.parametrize("flags", [FLAG_Q | FLAG_K | FLAG_V, FLAG_K | FLAG_V])
 def test_irpe_bf16_qv_bucket_count_past_the_fast_layout(flags):
     # 60 declared buckets (ids 0..48 used): the two-warpgroup kernel's query /
