@@ -67,21 +67,28 @@ int orc_piecewise_index(double x, double alpha, double beta, double gamma)
  * Writes ids[i*N + j] for query i and key j, N = H*W. The table half-width
  * is int(beta) (Pitfalls: "use int(beta) for the table size"), so ids lie
  * in [0, (2*int(beta)+1)^2). Returns the number of buckets. */
-int orc_product_bucket_ids(int H, int W, double alpha, double beta, double gamma,
-                           int32_t *ids)
+/* One query row of the Product map: ids_i[j] for query i and every key j. */
+static void product_ids_row(int H, int W, double alpha, double beta, double gamma, int i,
+                            int32_t *ids_i)
 {
     int half = (int)beta;
     int span = 2 * half + 1;
-    int N = H * W;
-    for (int i = 0; i < N; ++i) {
-        int ri = i / W, ci = i % W;
-        for (int j = 0; j < N; ++j) {
-            int rj = j / W, cj = j % W;
-            int row_index = orc_piecewise_index((double)(ri - rj), alpha, beta, gamma);
-            int col_index = orc_piecewise_index((double)(ci - cj), alpha, beta, gamma);
-            ids[(int64_t)i * N + j] = (row_index + half) * span + (col_index + half);
-        }
+    int ri = i / W, ci = i % W;
+    for (int j = 0; j < H * W; ++j) {
+        int rj = j / W, cj = j % W;
+        int row_index = orc_piecewise_index((double)(ri - rj), alpha, beta, gamma);
+        int col_index = orc_piecewise_index((double)(ci - cj), alpha, beta, gamma);
+        ids_i[j] = (row_index + half) * span + (col_index + half);
     }
+}
+
+int orc_product_bucket_ids(int H, int W, double alpha, double beta, double gamma,
+                           int32_t *ids)
+{
+    int span = 2 * (int)beta + 1;
+    int N = H * W;
+    for (int i = 0; i < N; ++i)
+        product_ids_row(H, W, alpha, beta, gamma, i, ids + (int64_t)i * N);
     return span * span;
 }
 
@@ -233,6 +240,59 @@ static double dot(const double *a, const double *b, int d)
  * NULL (term off).
  * rows lists the query rows to compute (NULL: all n); out and attn are
  * written only at those rows. attn may be NULL. Returns 0, or -1 on a bad id. */
+/* One query row of orc_attention: query qi against every key, its ids ids_i[j]
+ * (and ids2_i, or NULL) for key j; e is scratch of n doubles; zi receives the
+ * d outputs and attn_i (or NULL) the n weights. Returns 0, or -1 on a bad id. */
+static int attention_row(int n, int d, const double *qi, const double *k, const double *v,
+                         const int32_t *ids_i, const int32_t *ids2_i, int num_buckets,
+                         const double *tab_k, const double *tab_q, const double *tab_v,
+                         const double *bias, const double *bias_in, double scale,
+                         double *e, double *zi, double *attn_i)
+{
+    double emax = -INFINITY;
+    for (int j = 0; j < n; ++j) {
+        int id = ids_i[j];
+        if (id < 0 || id >= num_buckets) return -1;
+        int id2 = ids2_i ? ids2_i[j] : -1;
+        if (ids2_i && (id2 < 0 || id2 >= num_buckets)) return -1;
+        const double *kj = k + (int64_t)j * d;
+        double logit = dot(qi, kj, d);
+        if (tab_k) logit += dot(qi, tab_k + (int64_t)id * d, d);
+        if (tab_q) logit += dot(kj, tab_q + (int64_t)id * d, d);
+        if (bias_in) logit += bias_in[id];
+        if (ids2_i) {
+            if (tab_k) logit += dot(qi, tab_k + (int64_t)id2 * d, d);
+            if (tab_q) logit += dot(kj, tab_q + (int64_t)id2 * d, d);
+            if (bias_in) logit += bias_in[id2];
+        }
+        logit *= scale;
+        if (bias) logit += bias[id];
+        e[j] = logit;
+        if (logit > emax) emax = logit;
+    }
+    double denom = 0.0;
+    for (int j = 0; j < n; ++j) {
+        e[j] = exp(e[j] - emax);
+        denom += e[j];
+    }
+    for (int c = 0; c < d; ++c) zi[c] = 0.0;
+    for (int j = 0; j < n; ++j) {
+        double a = e[j] / denom;
+        if (attn_i) attn_i[j] = a;
+        const double *vj = v + (int64_t)j * d;
+        for (int c = 0; c < d; ++c) zi[c] += a * vj[c];
+        if (tab_v) {
+            const double *rv = tab_v + (int64_t)ids_i[j] * d;
+            for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
+            if (ids2_i) {
+                rv = tab_v + (int64_t)ids2_i[j] * d;
+                for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
+            }
+        }
+    }
+    return 0;
+}
+
 int orc_attention(int n, int d, const double *q, const double *k, const double *v,
                   const int32_t *ids, const int32_t *ids2, int num_buckets,
                   const double *tab_k, const double *tab_q, const double *tab_v,
@@ -242,54 +302,15 @@ int orc_attention(int n, int d, const double *q, const double *k, const double *
     double *e = (double *)malloc(sizeof(double) * (size_t)n);
     if (!e) return -2;
     int count = rows ? nrows : n;
-    for (int r = 0; r < count; ++r) {
-        int i = rows ? rows[r] : r;
-        const double *qi = q + (int64_t)i * d;
-        double emax = -INFINITY;
-        for (int j = 0; j < n; ++j) {
-            int id = ids[(int64_t)i * n + j];
-            if (id < 0 || id >= num_buckets) { free(e); return -1; }
-            int id2 = ids2 ? ids2[(int64_t)i * n + j] : -1;
-            if (ids2 && (id2 < 0 || id2 >= num_buckets)) { free(e); return -1; }
-            const double *kj = k + (int64_t)j * d;
-            double logit = dot(qi, kj, d);
-            if (tab_k) logit += dot(qi, tab_k + (int64_t)id * d, d);
-            if (tab_q) logit += dot(kj, tab_q + (int64_t)id * d, d);
-            if (bias_in) logit += bias_in[id];
-            if (ids2) {
-                if (tab_k) logit += dot(qi, tab_k + (int64_t)id2 * d, d);
-                if (tab_q) logit += dot(kj, tab_q + (int64_t)id2 * d, d);
-                if (bias_in) logit += bias_in[id2];
-            }
-            logit *= scale;
-            if (bias) logit += bias[id];
-            e[j] = logit;
-            if (logit > emax) emax = logit;
-        }
-        double denom = 0.0;
-        for (int j = 0; j < n; ++j) {
-            e[j] = exp(e[j] - emax);
-            denom += e[j];
-        }
-        double *zi = out + (int64_t)i * d;
-        for (int c = 0; c < d; ++c) zi[c] = 0.0;
-        for (int j = 0; j < n; ++j) {
-            double a = e[j] / denom;
-            if (attn) attn[(int64_t)i * n + j] = a;
-            const double *vj = v + (int64_t)j * d;
-            for (int c = 0; c < d; ++c) zi[c] += a * vj[c];
-            if (tab_v) {
-                const double *rv = tab_v + (int64_t)ids[(int64_t)i * n + j] * d;
-                for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
-                if (ids2) {
-                    rv = tab_v + (int64_t)ids2[(int64_t)i * n + j] * d;
-                    for (int c = 0; c < d; ++c) zi[c] += a * rv[c];
-                }
-            }
-        }
+    int status = 0;
+    for (int r = 0; r < count && status == 0; ++r) {
+        int64_t i = rows ? rows[r] : r;
+        status = attention_row(n, d, q + i * d, k, v, ids + i * n, ids2 ? ids2 + i * n : NULL,
+                               num_buckets, tab_k, tab_q, tab_v, bias, bias_in, scale, e,
+                               out + i * d, attn ? attn + i * n : NULL);
     }
     free(e);
-    return 0;
+    return status;
 }
 
 /* The same slice by the efficient route of iRPE section 3.2 (eqs. 26-28):
@@ -351,7 +372,8 @@ int orc_attention_efficient(int n, int d, const double *q, const double *k, cons
 
 /* iRPE contextual Product attention over q, k, v of shape [B, heads, N, d],
  * N = H*W, with head-shared tables [num_buckets, d] selected by flags
- * (ORC_K | ORC_Q | ORC_V). Bucket ids are built here from the definition.
+ * (ORC_K | ORC_Q | ORC_V). Bucket ids are built here from the definition, for
+ * the listed query rows only (no N x N map when rows are given).
  * slice_list / nslices pick (b*heads + h) slices (NULL: all) and rows /
  * nrows pick query rows within each (NULL: all). Returns 0 on success. */
 int orc_irpe_attention(int B, int heads, int H, int W, int d,
@@ -362,22 +384,30 @@ int orc_irpe_attention(int B, int heads, int H, int W, int d,
                        int nrows, const int32_t *rows, double *out)
 {
     int N = H * W;
-    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)N * N);
-    if (!ids) return -2;
-    int K = orc_product_bucket_ids(H, W, alpha, beta, gamma, ids);
+    /* the id rows of the listed queries only (all N when rows is NULL) */
+    int count_rows = rows ? nrows : N;
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * ((size_t)count_rows * N + 1));
+    double *e = (double *)malloc(sizeof(double) * (size_t)N);
+    if (!ids || !e) { free(ids); free(e); return -2; }
+    for (int r = 0; r < count_rows; ++r)
+        product_ids_row(H, W, alpha, beta, gamma, rows ? rows[r] : r, ids + (int64_t)r * N);
+    int K = (2 * (int)beta + 1) * (2 * (int)beta + 1);
     double scale = 1.0 / sqrt((double)d);
     int count = slice_list ? nslices : B * heads;
     int status = 0;
     for (int s = 0; s < count && status == 0; ++s) {
         int64_t bh = slice_list ? slice_list[s] : s;
         int64_t off = bh * (int64_t)N * d;
-        status = orc_attention(N, d, q + off, k + off, v + off, ids, NULL, K,
-                               (flags & ORC_K) ? tab_k : NULL,
-                               (flags & ORC_Q) ? tab_q : NULL,
-                               (flags & ORC_V) ? tab_v : NULL,
-                               NULL, NULL, scale, nrows, rows, out + off, NULL);
+        for (int r = 0; r < count_rows && status == 0; ++r) {
+            int64_t i = rows ? rows[r] : r;
+            status = attention_row(N, d, q + off + i * d, k + off, v + off, ids + (int64_t)r * N,
+                                   NULL, K, (flags & ORC_K) ? tab_k : NULL,
+                                   (flags & ORC_Q) ? tab_q : NULL, (flags & ORC_V) ? tab_v : NULL,
+                                   NULL, NULL, scale, e, out + off + i * d, NULL);
+        }
     }
     free(ids);
+    free(e);
     return status;
 }
 
