@@ -165,6 +165,16 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  * for fp32, <= 128 for bf16 (<= 64 with RPE_TERM_Q); with RPE_TABLES_CROSS
  * num_buckets even and (num_buckets / 2)^2 <= 64; N <= 65536. Anything else
  * returns RPE_ERR_UNSUPPORTED.
+ * bf16 kernels keep the offset table ((2H-1)(2W-1) bytes, 2(2H-1)(2W-1) + 1
+ * with a class token) and the per-bucket tables of one query tile in one
+ * SM's shared memory. A request for which they do not fit returns
+ * RPE_ERR_UNSUPPORTED before any launch. With 64 buckets the offset table may
+ * take 147,968 bytes for plain attention, 107,008 with the key or the value
+ * term, 105,984 with the query term, 65,024 to 66,048 with two terms and
+ * 24,064 with all three (square grids up to 192, 164, 163, 127 and 78 on a
+ * side); fewer buckets leave a little more room. The key and value terms
+ * together take at most 110 buckets on a 14 x 14 grid, 100 on 56 x 56. fp32
+ * reads the offset table from global memory and has no such limit.
  * Device memory: the library allocates, on first use per device and never
  * frees, a status word and, for bf16 calls on the two-warpgroup kernel whose
  * last round of (batch, head) work items fills at most half the GPU, one

@@ -11,6 +11,9 @@
   workspace owned by the launching stream, so launches on two streams may
   overlap; a capture on a stream that has no workspace yet runs every item
   whole (no allocation inside a capture) and still matches the oracle.
+- Shared-memory limits: a bf16 request whose offset table and bucket tables
+  do not fit in shared memory returns RPE_ERR_UNSUPPORTED before any launch;
+  the largest requests that fit match the oracle.
 """
 import numpy as np
 import pytest
@@ -218,3 +221,40 @@ def test_capture_on_a_stream_without_workspace_runs_items_whole():
     sl = np.array([0, 151, 152, 170, S - 1])
     got = out.reshape(S, H * W, 64)[torch.as_tensor(sl, device=out.device)]
     assert _maxerr(got, _split_ref(inp, shape, sl)) <= TOL_BF16
+
+
+# bf16 requests keep the offset table and one query tile's bucket tables in
+# shared memory: the largest request that fits runs and matches the oracle,
+# one step beyond is refused before any launch (tables of `nb` rows; the
+# Product ids of these grids use the first 49)
+@pytest.mark.parametrize("flags,nb,H", [(FLAG_K, 64, 164), (FLAG_Q | FLAG_K | FLAG_V, 64, 78),
+                                        (FLAG_K | FLAG_V, 110, 14)])
+def test_largest_request_that_fits_in_shared_memory_matches_the_oracle(flags, nb, H):
+    W = H
+    N = H * W
+    lut, _, K = api.rpe_build_bucket_ids(H, W, *R19)
+    inp = workloads.irpe_inputs(1, 2, N, 64, nb, flags, "bf16", 0.5, seed=9)
+    g = _dev(inp)
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags, table_q=g["tab_q"],
+                           table_k=g["tab_k"], table_v=g["tab_v"])
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, W - 1, W, N // 2, N - W, N - 1])
+    tabs = {n: (None if inp[n] is None else inp[n][:K]) for n in ("tab_q", "tab_k", "tab_v")}
+    ref = oracle.irpe_attention(inp["q"], inp["k"], inp["v"], H, W, *R19, flags, rows=rows, **tabs)
+    got = out[:, :, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref[:, :, rows]) <= TOL_BF16
+
+
+@pytest.mark.parametrize("flags,nb,H", [(FLAG_K, 64, 165), (FLAG_Q | FLAG_K | FLAG_V, 64, 79),
+                                        (FLAG_K | FLAG_V, 111, 14), (FLAG_K | FLAG_V, 128, 14)])
+def test_request_beyond_shared_memory_is_unsupported(flags, nb, H):
+    W = H
+    lut, _, _ = api.rpe_build_bucket_ids(H, W, *R19)
+    g = _dev(workloads.irpe_inputs(1, 1, H * W, 64, nb, flags, "bf16", 0.5, seed=5))
+    out = torch.full_like(g["q"], 7.0)
+    with pytest.raises(_lib.RpeError) as e:
+        api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, nb, H, W, flags, table_q=g["tab_q"],
+                         table_k=g["tab_k"], table_v=g["tab_v"], out=out)
+    assert e.value.status == _lib.RPE_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool(torch.all(out == 7.0))  # nothing was launched

@@ -52,6 +52,12 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 int status_of(cudaError_t err) { return err == cudaSuccess ? RPE_OK : RPE_ERR_CUDA; }
 
+// bf16 iRPE launches: a request whose tables do not fit in shared memory comes
+// back as cudaErrorNotSupported before anything is launched
+int status_of_bf16(cudaError_t err) {
+    return err == cudaErrorNotSupported ? RPE_ERR_UNSUPPORTED : status_of(err);
+}
+
 // Kernel of rpe_wait_probe: waits on a barrier that nothing arrives at.
 __global__ void wait_probe_kernel(WaitCtl wc) {
     __shared__ __align__(8) uint64_t bar;
@@ -346,7 +352,7 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v, const void *table_
     a.tab_heads = tab_heads;
     a.cls = cls;
     a.lut_row_runs = row_runs;
-    return status_of(launch_rpe_bf16(a, st));
+    return status_of_bf16(launch_rpe_bf16(a, st));
 }
 
 int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *bias_table,
@@ -424,7 +430,7 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
     a.bias_heads = bias_heads;
     a.cross_span = cross_span;
     a.cls = cls;
-    return status_of(launch_rpe_bf16(a, st));
+    return status_of_bf16(launch_rpe_bf16(a, st));
 }
 
 int swin_window_attn_fwd(const void *q, const void *k, const void *v, const float *bias_table,

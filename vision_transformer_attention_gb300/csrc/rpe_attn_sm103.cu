@@ -754,7 +754,8 @@ cudaError_t launch_tmpl(const RpeBf16Args &a, cudaStream_t stream) {
             return cudaGetLastError();
         }
     }
-    return cudaErrorInvalidValue;  // the bucket table does not fit in shared memory
+    // the offset and bucket tables do not fit in shared memory: nothing launched
+    return cudaErrorNotSupported;
 }
 
 }  // namespace
