@@ -40,6 +40,26 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Division by a divisor fixed for the whole launch, as one multiply-high, an
+// add and a shift (Granlund and Montgomery, "Division by invariant integers
+// using multiplication", 1994, section 4): with l = ceil(log2 d) and
+// m = floor(2^32 (2^l - d) / d) + 1, n / d = (mulhi(m, n) + n) >> l for
+// 0 <= n < 2^31 (the sum then stays below 2^32).
+struct FastDiv {
+    uint32_t d, m, l;
+};
+
+FastDiv make_fastdiv(int d) {
+    FastDiv f{static_cast<uint32_t>(d < 1 ? 1 : d), 0u, 0u};
+    while ((1ull << f.l) < f.d) ++f.l;
+    f.m = static_cast<uint32_t>(((1ull << 32) * ((1ull << f.l) - f.d)) / f.d + 1);
+    return f;
+}
+
+__device__ __forceinline__ int fast_div(const FastDiv &f, int n) {
+    return static_cast<int>((__umulhi(f.m, static_cast<uint32_t>(n)) + static_cast<uint32_t>(n)) >> f.l);
+}
+
 template <int M, int D>
 struct SwinTile {
     static constexpr int kN = M * M;            // tokens per window
@@ -70,8 +90,8 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
                      const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v,
                      const __grid_constant__ CUtensorMap tm_o, const float *__restrict__ bias_table,
-                     int heads, int units, int tiles, int wins_y, int wins_x, float scale_log2e,
-                     WaitCtl wc) {
+                     FastDiv heads, int units, int tiles, FastDiv wins_y, FastDiv wins_x,
+                     float scale_log2e, WaitCtl wc) {
     using T = SwinTile<M, D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -113,9 +133,10 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     griddep_wait();
 
     // Bias table -> shared memory, head-major, pre-multiplied by log2(e).
-    for (int e = tid; e < heads * T::kNB; e += blockDim.x) {
+    const int nheads = static_cast<int>(heads.d);
+    for (int e = tid; e < nheads * T::kNB; e += blockDim.x) {
         const int h = e / T::kNB, b = e % T::kNB;
-        bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * heads + h) * kLog2e;
+        bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * nheads + h) * kLog2e;
     }
     tc_fence_before();
     __syncthreads();
@@ -134,11 +155,12 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
 
     // feature-map coordinates (head, first column, first row, image) of a unit
     auto unit_coords = [&](int u, int &h, int &x0, int &y0, int &b) {
-        h = u % heads;
-        const int win = u / heads;
-        x0 = (win % wins_x) * M;
-        y0 = ((win / wins_x) % wins_y) * M;
-        b = win / (wins_x * wins_y);
+        const int win = fast_div(heads, u);
+        h = u - win * nheads;
+        const int wrow = fast_div(wins_x, win);  // window row over all images
+        x0 = (win - wrow * static_cast<int>(wins_x.d)) * M;
+        b = fast_div(wins_y, wrow);
+        y0 = (wrow - b * static_cast<int>(wins_y.d)) * M;
     };
     auto issue_load = [&](int tile, int stage) {
         uint8_t *sb = stage_base + stage * T::kStageBytes;
@@ -176,15 +198,8 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         const int stage = it & 1;
         uint8_t *sb = stage_base + stage * T::kStageBytes;
 
-        // ---- thread 0: prefetch the next tile, then S = Q K^T for this one
+        // ---- thread 0: S = Q K^T for this tile, then the next tile's loads
         if (tid == 0 && !abort_flag) {
-            const int next = tile + gridDim.x;
-            // the other stage's Q buffer staged the previous tile's output:
-            // its TMA store must have read it before the next load lands there
-            if (next < tiles) {
-                bulk_wait_read_all();
-                issue_load(next, stage ^ 1);
-            }
             if (mbar_wait(&bar_load[stage], load_uses[stage] & 1, wc, kStatusTimeoutLoad,
                           &abort_flag)) {
                 loads_pending &= ~(1u << stage);
@@ -200,6 +215,13 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
                 mma_commit(&bar_s);
                 mma_bar_pending = &bar_s;
                 mma_parity_pending = it & 1;
+                // the other stage's Q buffer staged the previous tile's output:
+                // its TMA store must have read it before the next load lands there
+                const int next = tile + gridDim.x;
+                if (next < tiles) {
+                    bulk_wait_read_all();
+                    issue_load(next, stage ^ 1);
+                }
             }
         }
 
@@ -217,7 +239,8 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
             tmem_ld_wait();
             tmem_ready(s0);
             tmem_ready(s1);
-            const int h = (unit < units ? unit : 0) % heads;
+            const int uu = unit < units ? unit : 0;
+            const int h = uu - fast_div(heads, uu) * nheads;
             const float *bp = bias_s + h * T::kNBPad + bias_base;
             float x[T::kN];
             float mx = -INFINITY;
@@ -371,8 +394,8 @@ cudaError_t launch_swin_tmpl(const SwinBf16Args &a, unsigned *status, bool clear
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
     return launch_pdl(swin_bf16_kernel<M, D, false>, dim3(grid), dim3(128), smem, stream, tq, tk, tv, to,
-                      a.bias_table, a.heads, units, tiles, 1, 1, scale_log2e,
-                      WaitCtl{status, kDefaultWaitNs});
+                      a.bias_table, make_fastdiv(a.heads), units, tiles, make_fastdiv(1),
+                      make_fastdiv(1), scale_log2e, WaitCtl{status, kDefaultWaitNs});
 }
 
 template <int M, int D>
@@ -408,7 +431,8 @@ cudaError_t launch_swin_fmap_tmpl(const SwinFmapArgs &a, cudaStream_t stream) {
     const int grid = std::min(tiles, sm_count() * T::kCtasPerSm);
     const float scale_log2e = static_cast<float>(1.0 / std::sqrt(static_cast<double>(D))) * kLog2e;
     return launch_pdl(swin_bf16_kernel<M, D, true>, dim3(grid), dim3(128), smem, stream, tq, tk,
-                      tv, to, a.bias_table, a.heads, units, tiles, wins_y, wins_x, scale_log2e,
+                      tv, to, a.bias_table, make_fastdiv(a.heads), units, tiles,
+                      make_fastdiv(wins_y), make_fastdiv(wins_x), scale_log2e,
                       WaitCtl{status, kDefaultWaitNs});
 }
 
