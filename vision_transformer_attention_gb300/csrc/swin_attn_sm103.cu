@@ -123,29 +123,24 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 128);
     if constexpr (FM) {
-        // a window's box fills rows 0..n-1 of its 64-row slot; the rest must
-        // hold finite values (zero) for the products
-        for (int e = tid; e < 2 * T::kStageBytes / 16; e += blockDim.x)
-            st_shared_v4(smem_u32(stage_base) + e * 16, 0u, 0u, 0u, 0u);
+        // a window's box fills rows 0..n-1 of its 64-row slot; rows n..63 of
+        // both slots of every operand and stage must hold finite values (zero)
+        // for the products. The boxes never write them, so the first loads
+        // may land while these stores run.
+        constexpr int kPadRows = 64 - T::kN;
+        constexpr int kRowChunks = T::kRowBytes / 16;
+        constexpr int kPadChunks = 2 * 3 * 2 * kPadRows * kRowChunks;  // stages x operands x slots
+        for (int e = tid; e < kPadChunks; e += blockDim.x) {
+            const int c = e % kRowChunks;
+            const int row = (e / kRowChunks) % kPadRows;
+            const int blk = e / (kRowChunks * kPadRows);  // (stage * 3 + operand) * 2 + slot
+            st_shared_v4(smem_u32(stage_base) + (blk >> 1) * T::kOperBytes +
+                             ((blk & 1) * 64 + T::kN + row) * T::kRowBytes + c * 16,
+                         0u, 0u, 0u, 0u);
+        }
         fence_proxy_async_smem();
     }
-    // nothing above reads an input: it may overlap the previous kernel
-    griddep_wait();
-
-    // Bias table -> shared memory, head-major, pre-multiplied by log2(e).
     const int nheads = static_cast<int>(heads.d);
-    for (int e = tid; e < nheads * T::kNB; e += blockDim.x) {
-        const int h = e / T::kNB, b = e % T::kNB;
-        bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * nheads + h) * kLog2e;
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
-
-    constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
-    constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
-    const WaitCtl drain{wc.status, kDefaultWaitNs};
 
     // Thread 0's bookkeeping of work in flight, for draining after an abort.
     uint32_t loads_pending = 0;  // bit s: stage s has a load not yet waited for
@@ -165,11 +160,13 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
     auto issue_load = [&](int tile, int stage) {
         uint8_t *sb = stage_base + stage * T::kStageBytes;
         if constexpr (FM) {
-            const int nu = 2 * tile + 1 < units ? 2 : 1;
-            mbar_arrive_expect_tx(&bar_load[stage], 3 * nu * T::kN * T::kRowBytes);
-            for (int s2 = 0; s2 < nu; ++s2) {
+            // both slots are always loaded (an odd last tile repeats its unit
+            // in slot 1, whose rows are discarded), so no slot's rows 0..n-1
+            // are ever read before a load has written them
+            mbar_arrive_expect_tx(&bar_load[stage], 3 * 2 * T::kN * T::kRowBytes);
+            for (int s2 = 0; s2 < 2; ++s2) {
                 int h, x0, y0, b;
-                unit_coords(2 * tile + s2, h, x0, y0, b);
+                unit_coords(2 * tile + s2 < units ? 2 * tile + s2 : units - 1, h, x0, y0, b);
                 uint8_t *dst = sb + s2 * 64 * T::kRowBytes;
                 tma_load_5d(dst, &tm_q, &bar_load[stage], 0, h, x0, y0, b);
                 tma_load_5d(dst + T::kOperBytes, &tm_k, &bar_load[stage], 0, h, x0, y0, b);
@@ -184,7 +181,26 @@ __global__ void __launch_bounds__(128, SwinTile<M, D>::kCtasPerSm)
         loads_pending |= 1u << stage;
     };
 
+    // nothing above reads an input: it may overlap the previous kernel
+    griddep_wait();
+    // the first tile's loads overlap the bias-table copy below (thread 0
+    // initialised the barriers itself)
     if (tid == 0 && static_cast<int>(blockIdx.x) < tiles) issue_load(blockIdx.x, 0);
+
+    // Bias table -> shared memory, head-major, pre-multiplied by log2(e).
+    for (int e = tid; e < nheads * T::kNB; e += blockDim.x) {
+        const int h = e / T::kNB, b = e % T::kNB;
+        bias_s[h * T::kNBPad + b] = __ldg(bias_table + static_cast<size_t>(b) * nheads + h) * kLog2e;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+    constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+    const WaitCtl drain{wc.status, kDefaultWaitNs};
+
 
     // Per-thread constants: which unit slot and which row of it this thread owns.
     const int slot = tid >> 6;
