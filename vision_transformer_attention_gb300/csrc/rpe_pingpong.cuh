@@ -578,8 +578,15 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
     }
     if (warp == 0) tmem_alloc(&tmem_base_s, 256 * NG);
     // K/V buffers: rows KT..NS-1 are never loaded and must hold finite values
-    for (int e = tid; e < P.nst * 2 * G::KV_BYTES / 16; e += kThreads)
-        st_shared_v4(smem_u32(sKV) + e * 16, 0u, 0u, 0u, 0u);
+    // (the loads write rows 0..KT-1 only, so they may land while these run)
+    {
+        constexpr int kPadChunks = (G::NS - G::KT) * 128 / 16;
+        if constexpr (kPadChunks > 0)
+            for (int e = tid; e < P.nst * 2 * kPadChunks; e += kThreads)
+                st_shared_v4(smem_u32(sKV) + (e / kPadChunks) * G::KV_BYTES + G::KT * 128 +
+                                 (e % kPadChunks) * 16,
+                             0u, 0u, 0u, 0u);
+    }
     // value term: the bucket sums start at zero (each item's staging step
     // zeroes them again)
     if (HV)
@@ -600,29 +607,18 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         }
         fence_proxy_async_smem();
     }
-    // everything above touches no input: it may overlap the previous kernel
-    griddep_wait();
-    if (HK || BM || HQ || HV) {
-        // offset table as bytes. The call checked its ids on the host (once per
-        // table); an id outside [0, bound) -- the class bucket excluded -- sets
-        // the status bit and is clamped so no read leaves shared memory. Keys
-        // past the last grid row index up to lut_pad bytes before the table;
-        // those bytes hold bucket 0 so every read stays in bounds (those scores
-        // are masked).
-        const int bound = P.nb - (CL ? 1 : 0);
-        for (int e = tid; e < P.lut_pad; e += kThreads) sLut[e - P.lut_pad] = 0;
-        for (int e = tid; e < P.lut_len; e += kThreads) {
-            const int id = __ldg(P.lut + e);
-            if (id < 0 || id >= bound) atomicOr(wc.status, kStatusBadBucket);
-            sLut[e] = static_cast<uint8_t>(id < 0 ? 0 : (id >= bound ? bound - 1 : id));
-        }
-        if (CL)
-            for (int e = tid; e < P.cls_len; e += kThreads) sLut[P.lut_len + e] = static_cast<uint8_t>(P.nb - 1);
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
+    // everything above touches no input: it may overlap the previous kernel
+    griddep_wait();
+    // The offset table goes to shared memory on the softmax warps, after the
+    // roles split, so the producer's first loads overlap the copy. Named
+    // barrier 3 tells its readers it is complete: the softmax warps and, with
+    // the value term, the control warp of CTA 0 that checks its row runs.
+    constexpr bool kLut = HK || BM || HQ || HV;
+    const int lut_bar_count = 4 * NG * 32 + ((HV && blockIdx.x == 0) ? 32 : 0);
     if (warp >= 4 * NG) {
         regs_dealloc<L::kRegsControl>();
         if (warp == 4 * NG) {
@@ -856,6 +852,7 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             }
             __syncwarp();
         } else if (HV && blockIdx.x == 0) {
+            named_bar_sync(3, lut_bar_count);
             // The value term's bucket sums rely on each id forming one run
             // along a grid row of keys, seen from any query column; the call
             // checked that once per table. A table rewritten in place since then
@@ -879,6 +876,35 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
         }
     } else {
         regs_alloc<L::kRegsSoftmax>();
+        if (kLut) {
+            // offset table as bytes. The call checked its ids on the host (once
+            // per table); an id outside [0, bound) -- the class bucket excluded --
+            // sets the status bit and is clamped so no read leaves shared memory.
+            // Keys past the last grid row index up to lut_pad bytes before the
+            // table; those bytes hold bucket 0 so every read stays in bounds
+            // (those scores are masked).
+            constexpr int kCopiers = 4 * NG * 32;
+            const int bound = P.nb - (CL ? 1 : 0);
+            auto clamp_id = [&](int id) -> uint32_t {
+                if (id < 0 || id >= bound) atomicOr(wc.status, kStatusBadBucket);
+                return static_cast<uint32_t>(id < 0 ? 0 : (id >= bound ? bound - 1 : id));
+            };
+            for (int e = tid; e < P.lut_pad; e += kCopiers) sLut[e - P.lut_pad] = 0;
+            // four ids per 16-byte load (the table and sLut are 16-byte aligned),
+            // stored as one word of four bytes; then the last lut_len % 4 ids
+            const int n4 = P.lut_len >> 2;
+            for (int e = tid; e < n4; e += kCopiers) {
+                const int4 v = __ldg(reinterpret_cast<const int4 *>(P.lut) + e);
+                reinterpret_cast<uint32_t *>(sLut)[e] =
+                    clamp_id(v.x) | (clamp_id(v.y) << 8) | (clamp_id(v.z) << 16) | (clamp_id(v.w) << 24);
+            }
+            for (int e = 4 * n4 + tid; e < P.lut_len; e += kCopiers)
+                sLut[e] = static_cast<uint8_t>(clamp_id(__ldg(P.lut + e)));
+            if (CL)
+                for (int e = tid; e < P.cls_len; e += kCopiers)
+                    sLut[P.lut_len + e] = static_cast<uint8_t>(P.nb - 1);
+            named_bar_sync(3, lut_bar_count);
+        }
         // ------------------------------------------------ softmax groups
         // One thread per query row. Decisions to go on or stop are uniform per
         // warp within an item and over the whole group twice per item (at its
