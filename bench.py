@@ -78,11 +78,11 @@ def workload_config(cfg):
 # and its DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum
 # from an ncu capture of the kernel as it stands; None when not measured).
 DOMINANT = {
-    "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", 57840640 + 1616128),
-    "swin_t_stage1_fmap": ("swin_bf16_kernel<7,32,fmap>", "hbm", 57851136 + 1450752),
-    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,5,K>", "hbm", 28990208 + 0),
-    "irpe_qkv_deit_s": ("rpe_pingpong_kernel<14,5,K,Q,V>", "hbm", None),
-    "irpe_k_56x56": ("rpe_pingpong_kernel<56,1,K,split>", "tensor", 58168832 + 2622208),
+    "swin_t_stage1": ("swin_bf16_kernel<7,32>", "hbm", 57838336 + 1461504),
+    "swin_t_stage1_fmap": ("swin_bf16_kernel<7,32,fmap>", "hbm", 57843712 + 1441024),
+    "irpe_k_deit_s": ("rpe_pingpong_kernel<14,5,K>", "hbm", 28996864 + 0),
+    "irpe_qkv_deit_s": ("rpe_pingpong_kernel<14,5,K,Q,V>", "hbm", 29055232 + 0),
+    "irpe_k_56x56": ("rpe_pingpong_kernel<56,1,K,split>", "tensor", 58280192 + 2207232),
     "irpe_k_r2_deit_s": ("rpe_pingpong_kernel<14,5,K,128 buckets>", "hbm", None),
     "irpe_k_deit_s_cls": ("rpe_pingpong_kernel<14,5,K,cls>", "hbm", None),
 }
