@@ -114,7 +114,8 @@ enum { RPE_DTYPE_BF16 = 0, RPE_DTYPE_F32 = 1 };
  *                                 RPE_MAP_CROSS [2 * N * N]: the row buckets,
  *                                 then the column buckets.
  *   num_buckets (host int*)       set to the mapping's bucket count.
- * Errors (RPE_ERR_INVALID_ARG): H or W < 1, N*N >= 2^31, alpha <= 0,
+ * Errors (RPE_ERR_INVALID_ARG): H or W < 1 or > 32768, N*N >= 2^31 with ids
+ * requested (without ids any grid the attention calls take is served), alpha <= 0,
  * alpha > beta or beta > gamma or a non-finite constant, an unknown mode, a
  * NULL bucket_lut or num_buckets, more than 256 buckets.
  */

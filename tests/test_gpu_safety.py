@@ -13,7 +13,8 @@
   whole (no allocation inside a capture) and still matches the oracle.
 - Shared-memory limits: a bf16 request whose offset table and bucket tables
   do not fit in shared memory returns RPE_ERR_UNSUPPORTED before any launch;
-  the largest requests that fit match the oracle.
+  the largest requests that fit match the oracle. The largest grid the calls
+  take (256 x 256) runs in fp32 and is refused in bf16.
 """
 import numpy as np
 import pytest
@@ -258,3 +259,28 @@ def test_request_beyond_shared_memory_is_unsupported(flags, nb, H):
     assert e.value.status == _lib.RPE_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert bool(torch.all(out == 7.0))  # nothing was launched
+
+
+def test_largest_grid_runs_in_fp32_and_is_refused_in_bf16():
+    # N = 65536, the most the attention calls take: the library builds the
+    # grid's offset table (no N x N map), fp32 matches the oracle on sampled
+    # rows, and bf16, whose shared memory cannot hold the 511 x 511 table,
+    # is refused before any launch
+    H = W = 256
+    N = H * W
+    lut, _, K = api.rpe_build_bucket_ids(H, W, *R19)
+    inp = workloads.irpe_inputs(1, 1, N, 32, K, FLAG_K, "f32", 2.0, seed=13)
+    g = _dev(inp)
+    out = api.rpe_attn_fwd(g["q"], g["k"], g["v"], lut, K, H, W, FLAG_K, table_k=g["tab_k"])
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, W - 1, W, N // 2 + W // 2, N - W, N - 1])
+    ref = oracle.irpe_attention(inp["q"], inp["k"], inp["v"], H, W, *R19, FLAG_K,
+                                tab_k=inp["tab_k"], rows=rows)[:, :, rows]
+    got = out[:, :, torch.as_tensor(rows, device=out.device)]
+    assert _maxerr(got, ref) <= TOL_F32
+    plain = oracle.irpe_attention(inp["q"], inp["k"], inp["v"], H, W, *R19, 0, rows=rows)[:, :, rows]
+    assert np.max(np.abs(plain - ref)) > 100 * TOL_F32  # the key term matters here
+    b = _dev(workloads.irpe_inputs(1, 1, N, 64, K, FLAG_K, "bf16", 0.5, seed=13))
+    with pytest.raises(_lib.RpeError) as e:
+        api.rpe_attn_fwd(b["q"], b["k"], b["v"], lut, K, H, W, FLAG_K, table_k=b["tab_k"])
+    assert e.value.status == _lib.RPE_ERR_UNSUPPORTED

@@ -55,6 +55,17 @@ def test_host_argument_checks_reject_before_any_launch():
     assert lib.rpe_build_bucket_ids(14, 14, 4, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     assert lib.rpe_build_bucket_ids(14, 14, -1, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
     assert lib.rpe_build_bucket_ids(14, 14, 0, 3.9, 3.8, 15.2, fake, None, ctypes.byref(nb), None) == 1
+    # the N x N expansion needs N * N < 2^31 (a 256 x 256 grid without it is fine,
+    # but needs a GPU); sides above 32768 are refused either way
+    assert lib.rpe_build_bucket_ids(256, 256, 0, 1.9, 3.8, 15.2, fake, fake, ctypes.byref(nb),
+                                    None) == 1
+    assert lib.rpe_build_bucket_ids(32769, 1, 0, 1.9, 3.8, 15.2, fake, None, ctypes.byref(nb),
+                                    None) == 1
+    # an empty batch is invalid; more than 65536 tokens is unsupported
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 49, 0, 1, 14, 14, 64, 1, 0,
+                            fake, None) == 1
+    assert lib.rpe_attn_fwd(fake, fake, fake, None, fake, None, fake, 49, 1, 1, 257, 256, 64, 1, 0,
+                            fake, None) == 2
     # misaligned pointer
     bad = ctypes.c_void_p((1 << 20) + 4)
     assert lib.rpe_attn_fwd(bad, fake, fake, None, fake, None, fake, 49, 1, 1, 14, 14, 64, 1, 0,

@@ -243,8 +243,12 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta, doub
     if (!std::isfinite(alpha) || !std::isfinite(beta) || !std::isfinite(gamma) || alpha <= 0.0 ||
         alpha > beta || beta > gamma || beta >= 127.0)
         return RPE_ERR_INVALID_ARG;
+    // the offset table's (2H-1)(2W-1) entries, and the N x N expansion when asked for,
+    // are indexed with 32-bit ints
     const long long n = static_cast<long long>(H) * W;
-    if (n * n >= (1LL << 31) || H > 32768 || W > 32768) return RPE_ERR_INVALID_ARG;
+    if (H > 32768 || W > 32768 || (2LL * H - 1) * (2LL * W - 1) >= (1LL << 31) ||
+        (ids != nullptr && n * n >= (1LL << 31)))
+        return RPE_ERR_INVALID_ARG;
     const int half = static_cast<int>(beta);
     const int span = 2 * half + 1;
     const int nb = mode == RPE_MAP_EUCLIDEAN ? span : mode == RPE_MAP_CROSS ? 2 * span : span * span;
