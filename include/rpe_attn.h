@@ -162,7 +162,8 @@ int rpe_build_bucket_ids(int H, int W, int mode, double alpha, double beta,
  *                for a class token at token 0 (then N = H * W + 1).
  * Supported: RPE_DTYPE_BF16 with d == 64 (tcgen05 tensor cores, fp32
  * accumulation, probabilities rounded to bf16 before the value products);
- * RPE_DTYPE_F32 with d <= 64 (fp32 on CUDA cores); 1 <= num_buckets <= 256
+ * RPE_DTYPE_F32 with d <= 64 and B * heads <= 65535 (fp32 on CUDA cores);
+ * B * heads * N * d < 2^40 for both; 1 <= num_buckets <= 256
  * for fp32, <= 128 for bf16 (<= 64 with RPE_TERM_Q); with RPE_TABLES_CROSS
  * num_buckets even and (num_buckets / 2)^2 <= 64; N <= 65536. Anything else
  * returns RPE_ERR_UNSUPPORTED.
@@ -210,7 +211,8 @@ int rpe_attn_fwd(const void *q, const void *k, const void *v,
  *                of a pair is then b[a][h] + b[span + b'][h] for its joint
  *                index a * span + b'), or RPE_CLS_TOKEN (token 0 is a class
  *                token whose pairs take bias row num_buckets - 1).
- * Supported: RPE_DTYPE_F32 on any grid with d <= 64 and num_buckets <= 256;
+ * Supported: RPE_DTYPE_F32 on any grid with d <= 64, num_buckets <= 256 and
+ * B * heads <= 65535;
  * RPE_DTYPE_BF16 on any grid with d == 64 and num_buckets <= 128 (Cross as
  * for rpe_attn_fwd; W in {14, 56} without a class token runs on the
  * two-warpgroup kernel, everything else on the general one).
@@ -232,8 +234,10 @@ int rpe_attn_bias_fwd(const void *q, const void *k, const void *v, const float *
  *                (windows already partitioned; token i of a window sits at
  *                (i / M, i % M)).
  * bias_table   : device float32 [(2M-1)^2, heads] (bucket-major).
- * Supported: RPE_DTYPE_BF16 with M == 7 and d in {32, 64} (tcgen05 tensor
- * cores); RPE_DTYPE_F32 with 2 <= M <= 8 and d <= 64 (fp32 on CUDA cores).
+ * Supported: RPE_DTYPE_BF16 with M == 7, d in {32, 64}, heads <= 32 and
+ * num_windows * heads < 2^30 (tcgen05 tensor cores); RPE_DTYPE_F32 with
+ * 2 <= M <= 8, d <= 64 and num_windows * heads <= 65535 (fp32 on CUDA cores).
+ * Anything else returns RPE_ERR_UNSUPPORTED.
  */
 int swin_window_attn_fwd(const void *q, const void *k, const void *v,
                          const float *bias_table, int num_windows, int heads,
