@@ -952,7 +952,6 @@ __global__ void __launch_bounds__(Layout<NG>::kThreads, Layout<NG>::kCtasPerSm)
             if (!red_and(group_bar, 128, okd)) return false;
             tc_fence_after();
             const int dqt = D.qt0 + wg;
-            const int di = dqt * 128 + t;
             const bool dactive = dqt * 128 + lq * 32 < P.N;
             float inv = 1.f / due_l;
             // CL: fold the class key into the row: reference max mm, O and l
